@@ -1,0 +1,345 @@
+/*
+ * vg_oracle.c -- CPU reference for the NVFP4 / row-scaled FP8 verify GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY (see vg_oracle.h).  Plain C99, no blocking, no
+ * fusion, no reordering beyond the definitions below.  Build with
+ * -ffp-contract=off so that every FP32 step of the quantisation recipe is
+ * one IEEE operation with one rounding.
+ *
+ * Sources for what is computed:
+ *  - The product and the 1-8 column widths: mtp7-device-confidence engine
+ *    card, Design table ("GEMVs": FP8 and NVFP4 bytes fed to BF16 MMA
+ *    fragments) and Decode row (verify pass over 2-8 columns).
+ *  - Checks against FP64: same card, Checks section.
+ *  - Round-to-nearest post-training quantisation to NVFP4 / FP8: crit
+ *    landing page, "Models" paragraph; row-scaled FP8: card, Model section.
+ *  - The pages do not define the bit formats.  E2M1 and E4M3 follow the
+ *    public OCP Microscaling and OCP 8-bit floating point definitions; the
+ *    quantisation order (tensor scale amax/(6*448), block scale
+ *    blockamax/6 in tensor-scale units, RNE with saturation) is the plainest
+ *    reading of the recipe.
+ */
+#include "vg_oracle.h"
+
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- decode */
+
+/* E2M1 magnitudes indexed by the low three bits of the code. */
+static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double vgo_e2m1_value(int code)
+{
+    double v = E2M1_MAG[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+double vgo_e4m3_value(int byte)
+{
+    int s = (byte >> 7) & 1;
+    int e = (byte >> 3) & 15;
+    int f = byte & 7;
+    double v;
+    if (e == 15 && f == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)f, -9);                 /* subnormal: f * 2^-9 */
+    else
+        v = ldexp(1.0 + f / 8.0, e - 7);          /* 2^(e-7) * (1 + f/8) */
+    return s ? -v : v;
+}
+
+double vgo_bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ---------------------------------------------------------------- encode */
+
+int vgo_e4m3_encode(float v)
+{
+    int sign = signbit(v) ? 0x80 : 0;
+    double a = fabs((double)v);
+    int ex, E, n;
+    double quantum, r;
+    if (isnan(v))
+        return sign | 0x7F;
+    if (a >= 448.0)
+        return sign | 0x7E;                       /* satfinite */
+    if (a == 0.0)
+        return sign;
+    /* binade of a: a = m * 2^ex with m in [0.5, 1) -> a in [2^(ex-1), 2^ex) */
+    frexp(a, &ex);
+    E = ex - 1;
+    if (E < -6)
+        E = -6;                                   /* subnormal spacing 2^-9 */
+    quantum = ldexp(1.0, E - 3);                  /* 3 mantissa bits */
+    r = nearbyint(a / quantum);                   /* ties to even multiple */
+    n = (int)r;
+    /* value = n * quantum; n in [0, 16].  Re-express as an E4M3 code. */
+    if (E == -6 && n < 8)
+        return sign | n;                          /* subnormal f = n */
+    if (n == 16) {                                /* rounded up a binade */
+        n = 8;
+        E += 1;
+    }
+    /* n in [8, 15]: value = 2^E * n/8 = 2^E * (1 + (n-8)/8) */
+    return sign | ((E + 7) << 3) | (n - 8);
+}
+
+int vgo_e2m1_encode(float v)
+{
+    int sign = signbit(v) ? 8 : 0;
+    float a = fabsf(v);
+    int mag;
+    /* nearest of {0,.5,1,1.5,2,3,4,6}; a midpoint goes to the code with an
+     * even mantissa bit (codes 0,2,4,6 have mantissa 0); above 6 saturates */
+    if (a <= 0.25f)       mag = 0;
+    else if (a < 0.75f)   mag = 1;
+    else if (a <= 1.25f)  mag = 2;
+    else if (a < 1.75f)   mag = 3;
+    else if (a <= 2.5f)   mag = 4;
+    else if (a < 3.5f)    mag = 5;
+    else if (a <= 5.0f)   mag = 6;
+    else                  mag = 7;
+    return sign | mag;
+}
+
+/* ------------------------------------------------------------- quantise */
+
+static int all_finite(const float *W, int64_t n)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        if (!(fabsf(W[i]) <= FLT_MAX))
+            return 0;
+    return 1;
+}
+
+int vgo_nvfp4_quantise(const float *W, int64_t M, int64_t K,
+                       uint8_t *nib, uint8_t *sc, float *gs_out)
+{
+    int64_t m, b, i;
+    float amax = 0.0f, gs;
+    if (!all_finite(W, M * K))
+        return -1;
+    for (i = 0; i < M * K; ++i)
+        if (fabsf(W[i]) > amax)
+            amax = fabsf(W[i]);
+    gs = amax / 2688.0f;                          /* 2688 = 6 * 448 */
+    *gs_out = gs;
+    memset(nib, 0, (size_t)(M * (K / 2)));
+    for (m = 0; m < M; ++m) {
+        for (b = 0; b < K / 16; ++b) {
+            const float *w = W + m * K + b * 16;
+            float bamax = 0.0f, d;
+            int code, j;
+            for (j = 0; j < 16; ++j)
+                if (fabsf(w[j]) > bamax)
+                    bamax = fabsf(w[j]);
+            if (gs == 0.0f) {
+                code = 0;
+            } else {
+                float t = bamax / gs;             /* block max in gs units */
+                float s = t / 6.0f;               /* scale for a max of 6 */
+                code = vgo_e4m3_encode(s);
+            }
+            sc[m * (K / 16) + b] = (uint8_t)code;
+            d = (float)vgo_e4m3_value(code) * gs; /* one FP32 rounding */
+            for (j = 0; j < 16; ++j) {
+                int c = (d == 0.0f) ? 0 : vgo_e2m1_encode(w[j] / d);
+                int64_t k = b * 16 + j;
+                uint8_t *p = nib + m * (K / 2) + k / 2;
+                if (k & 1)
+                    *p = (uint8_t)(*p | (c << 4));
+                else
+                    *p = (uint8_t)(*p | c);
+            }
+        }
+    }
+    return 0;
+}
+
+int vgo_fp8_quantise(const float *W, int64_t M, int64_t K,
+                     uint8_t *q, float *rs_out)
+{
+    int64_t m, k;
+    if (!all_finite(W, M * K))
+        return -1;
+    for (m = 0; m < M; ++m) {
+        const float *w = W + m * K;
+        float ramax = 0.0f, rs;
+        for (k = 0; k < K; ++k)
+            if (fabsf(w[k]) > ramax)
+                ramax = fabsf(w[k]);
+        rs = ramax / 448.0f;
+        rs_out[m] = rs;
+        for (k = 0; k < K; ++k)
+            q[m * K + k] = (uint8_t)((rs == 0.0f) ? 0 : vgo_e4m3_encode(w[k] / rs));
+    }
+    return 0;
+}
+
+/* -------------------------------------------------------------- dequant */
+
+void vgo_nvfp4_dequant(const uint8_t *nib, const uint8_t *sc, float gs,
+                       int64_t M, int64_t K, double *What)
+{
+    int64_t m, k;
+    for (m = 0; m < M; ++m)
+        for (k = 0; k < K; ++k) {
+            uint8_t byte = nib[m * (K / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            What[m * K + k] = vgo_e2m1_value(code)
+                            * vgo_e4m3_value(sc[m * (K / 16) + k / 16])
+                            * (double)gs;
+        }
+}
+
+void vgo_fp8_dequant(const uint8_t *q, const float *rs,
+                     int64_t M, int64_t K, double *What)
+{
+    int64_t m, k;
+    for (m = 0; m < M; ++m)
+        for (k = 0; k < K; ++k)
+            What[m * K + k] = vgo_e4m3_value(q[m * K + k]) * (double)rs[m];
+}
+
+/* ----------------------------------------------------------------- gemv */
+
+typedef struct {
+    int fp8;
+    const uint8_t *nib, *sc, *q;
+    const float *rs;
+    float gs;
+    const uint16_t *x;
+    int N;
+    int64_t M, K;
+    const int64_t *rows;
+    int64_t nrows, r0, r1;
+    double *y, *a;
+    double *xd;                                   /* x decoded, [N][K] */
+} gemv_job;
+
+/* One output row: decode row m of W to FP64, then for every column n the
+ * FP64 sum over k of w*x and of |w*x|, k in increasing order. */
+static void gemv_row(const gemv_job *j, int64_t r, double *wrow)
+{
+    int64_t m = j->rows ? j->rows[r] : r;
+    int64_t k;
+    int n;
+    for (k = 0; k < j->K; ++k) {
+        if (j->fp8) {
+            wrow[k] = vgo_e4m3_value(j->q[m * j->K + k]) * (double)j->rs[m];
+        } else {
+            uint8_t byte = j->nib[m * (j->K / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            wrow[k] = vgo_e2m1_value(code)
+                    * vgo_e4m3_value(j->sc[m * (j->K / 16) + k / 16])
+                    * (double)j->gs;
+        }
+    }
+    for (n = 0; n < j->N; ++n) {
+        const double *xn = j->xd + (int64_t)n * j->K;
+        double s = 0.0, sa = 0.0;
+        for (k = 0; k < j->K; ++k) {
+            double p = wrow[k] * xn[k];               /* exact in FP64 */
+            s += p;
+            sa += fabs(p);
+        }
+        j->y[(int64_t)n * j->nrows + r] = s;
+        j->a[(int64_t)n * j->nrows + r] = sa;
+    }
+}
+
+static void *gemv_worker(void *arg)
+{
+    const gemv_job *j = (const gemv_job *)arg;
+    double *wrow = (double *)malloc(sizeof(double) * (size_t)(j->K ? j->K : 1));
+    int64_t r;
+    for (r = j->r0; r < j->r1; ++r)
+        gemv_row(j, r, wrow);
+    free(wrow);
+    return NULL;
+}
+
+static void gemv_run(gemv_job *base, int threads)
+{
+    int64_t i, total = (int64_t)base->N * base->K;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(total ? total : 1));
+    int t;
+    for (i = 0; i < total; ++i)
+        xd[i] = vgo_bf16_value(base->x[i]);
+    base->xd = xd;
+    if (threads <= 1 || base->nrows < 2 * threads) {
+        base->r0 = 0;
+        base->r1 = base->nrows;
+        gemv_worker(base);
+    } else {
+        pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)threads);
+        gemv_job *jobs = (gemv_job *)malloc(sizeof(gemv_job) * (size_t)threads);
+        for (t = 0; t < threads; ++t) {
+            jobs[t] = *base;
+            jobs[t].r0 = base->nrows * t / threads;
+            jobs[t].r1 = base->nrows * (t + 1) / threads;
+            pthread_create(&tid[t], NULL, gemv_worker, &jobs[t]);
+        }
+        for (t = 0; t < threads; ++t)
+            pthread_join(tid[t], NULL);
+        free(tid);
+        free(jobs);
+    }
+    free(xd);
+}
+
+void vgo_gemv_nvfp4(const uint8_t *nib, const uint8_t *sc, float gs,
+                    const uint16_t *x, int N, int64_t M, int64_t K,
+                    const int64_t *rows, int64_t nrows,
+                    double *y, double *a, int threads)
+{
+    gemv_job j;
+    memset(&j, 0, sizeof j);
+    j.nib = nib; j.sc = sc; j.gs = gs; j.x = x; j.N = N; j.M = M; j.K = K;
+    j.rows = rows; j.nrows = rows ? nrows : M; j.y = y; j.a = a;
+    gemv_run(&j, threads);
+}
+
+void vgo_gemv_fp8(const uint8_t *q, const float *rs,
+                  const uint16_t *x, int N, int64_t M, int64_t K,
+                  const int64_t *rows, int64_t nrows,
+                  double *y, double *a, int threads)
+{
+    gemv_job j;
+    memset(&j, 0, sizeof j);
+    j.fp8 = 1; j.q = q; j.rs = rs; j.x = x; j.N = N; j.M = M; j.K = K;
+    j.rows = rows; j.nrows = rows ? nrows : M; j.y = y; j.a = a;
+    gemv_run(&j, threads);
+}
+
+/* ---------------------------------------------------------------- check */
+
+int64_t vgo_check(const uint16_t *y, const double *yref, const double *a,
+                  int64_t n, double rel, double abs_tol, double *worst)
+{
+    int64_t i, bad = 0;
+    double w = 0.0;
+    for (i = 0; i < n; ++i) {
+        double err = fabs(vgo_bf16_value(y[i]) - yref[i]);
+        double tol = rel * a[i] + abs_tol;
+        double ratio = err / tol;
+        if (!(err <= tol))
+            ++bad;
+        if (!(ratio <= w))                        /* also catches NaN */
+            w = isnan(ratio) ? INFINITY : ratio;
+    }
+    if (worst)
+        *worst = w;
+    return bad;
+}

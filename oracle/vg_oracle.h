@@ -1,0 +1,88 @@
+/*
+ * vg_oracle.h -- plain, slow, obviously correct CPU reference for the
+ * NVFP4 / row-scaled FP8 decode-and-verify GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * CPU-baseline leg of bench.py may load this library.  It shares no code,
+ * header, table or constant with the CUDA path in verify_gemm_gb300/csrc.
+ *
+ * Everything here works on the CANONICAL layout:
+ *   nib[m][k/2]  : E2M1 codes, low nibble = even k, high nibble = odd k
+ *   sc[m][k/16]  : one E4M3 byte per 16-element block along K
+ *   gs           : FP32 tensor scale (dequantisation multiplier)
+ *   q[m][k]      : FP8-E4M3 codes (row-scaled FP8), rs[m] FP32 row scale
+ *   x[n][k]      : BF16 bit patterns, y[n][m] results
+ *
+ * The product being checked is y[N,M] = x[N,K] . dequant(W)[M,K]^T, the
+ * weight-streaming product that the mtp7-device-confidence engine card
+ * (crit-hub), Design table, "GEMVs" row, runs for 1-8 columns, and that
+ * the same card's Measured section ("a verify pass reads 19.26 GB") and
+ * Checks section ("FP8/NVFP4 GEMVs for 1-8 columns ... against FP64")
+ * describe.  Accumulation is FP64; products of decoded weights and BF16
+ * activations are exact in FP64.
+ */
+#ifndef VG_ORACLE_H
+#define VG_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Value of a 4-bit E2M1 code: sign = bit 3, magnitude from the 8-entry
+ * table {0, 0.5, 1, 1.5, 2, 3, 4, 6}. */
+double vgo_e2m1_value(int code);
+
+/* Value of an OCP FP8 E4M3 ("FN") byte: bias 7, subnormals f*2^-9,
+ * 0x7F/0xFF are NaN, no infinities, max 448. */
+double vgo_e4m3_value(int byte);
+
+/* Value of a BF16 bit pattern. */
+double vgo_bf16_value(uint16_t bits);
+
+/* Round-to-nearest-even, saturating E4M3 encoder of an FP32 value
+ * (sign kept; |v| >= 448 gives +-448; NaN gives 0x7F|sign). */
+int vgo_e4m3_encode(float v);
+
+/* Round-to-nearest-even, saturating E2M1 encoder of an FP32 value
+ * (sign bit copied from v, so -0.1 gives 0x8). */
+int vgo_e2m1_encode(float v);
+
+/* NVFP4 round-to-nearest quantisation (load-time re-encoding, crit landing
+ * page, "Models" paragraph: post-training quantisation to NVFP4 by
+ * round-to-nearest).  K % 16 == 0.  Returns 0, or -1 if W holds a NaN/Inf. */
+int vgo_nvfp4_quantise(const float *W, int64_t M, int64_t K,
+                       uint8_t *nib, uint8_t *sc, float *gs_out);
+
+/* Row-scaled FP8-E4M3 quantisation (engine card, Model section: "re-encoded
+ * as row-scaled FP8").  Returns 0, or -1 if W holds a NaN/Inf. */
+int vgo_fp8_quantise(const float *W, int64_t M, int64_t K,
+                     uint8_t *q, float *rs_out);
+
+/* Dequantised weights in FP64 (exact). */
+void vgo_nvfp4_dequant(const uint8_t *nib, const uint8_t *sc, float gs,
+                       int64_t M, int64_t K, double *What);
+void vgo_fp8_dequant(const uint8_t *q, const float *rs,
+                     int64_t M, int64_t K, double *What);
+
+/* y[n][r] = sum_k What[rows[r]][k] * x[n][k] and a[n][r] = sum_k |What x|
+ * in FP64 for the listed rows (rows == NULL: all M rows, r = m).  Output
+ * arrays are [N][nrows].  threads <= 1 runs on the calling thread. */
+void vgo_gemv_nvfp4(const uint8_t *nib, const uint8_t *sc, float gs,
+                    const uint16_t *x, int N, int64_t M, int64_t K,
+                    const int64_t *rows, int64_t nrows,
+                    double *y, double *a, int threads);
+void vgo_gemv_fp8(const uint8_t *q, const float *rs,
+                  const uint16_t *x, int N, int64_t M, int64_t K,
+                  const int64_t *rows, int64_t nrows,
+                  double *y, double *a, int threads);
+
+/* Count elements with |y - yref| > rel*a + abs; *worst gets the largest
+ * |y - yref| / (rel*a + abs).  y is BF16 bits. */
+int64_t vgo_check(const uint16_t *y, const double *yref, const double *a,
+                  int64_t n, double rel, double abs_tol, double *worst);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,432 @@
+"""Pins of the CPU oracle against things other than the oracle itself.
+
+Each check here is independent of the oracle's own formulas: golden values
+fixed by the public format definitions or derived by hand from the recipe,
+a library routine (torch's float8_e4m3fn casts), brute-force nearest-value
+search with an explicit tie rule, exact rational arithmetic
+(fractions.Fraction), closed forms and invariants.  Together they are chosen
+so that a dropped term, a wrong sign, index or nibble order, a transposed
+operand or a wrong rounding rule in the oracle fails at least one of them
+(tests/test_oracle_mutants.py plants such mistakes and checks that).
+"""
+import math
+import random
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from conftest import read_golden
+
+
+def _golden_table(name):
+    out = {}
+    for code, val in read_golden(name):
+        out[int(code, 16)] = float(val)
+    return out
+
+
+E2M1 = _golden_table("e2m1_codes.txt")
+E4M3_T = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+E4M3_POS = np.array([E4M3_T[b] for b in range(0x7F)])        # finite, >= 0
+E2M1_POS = np.array([E2M1[c] for c in range(8)])
+
+
+def _same(a, b):
+    if math.isnan(a) or math.isnan(b):
+        return math.isnan(a) and math.isnan(b)
+    return a == b and math.copysign(1, a) == math.copysign(1, b)
+
+
+def _bits_to_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def _bf16_values(bits):
+    return _bits_to_bf16(bits).double().numpy()
+
+
+# -------------------------------------------------------------- brute force
+
+def _nearest_code(a, table):
+    """Brute-force nearest of |a| in table[code]; a tie goes to the even code."""
+    d = np.abs(table - a)
+    best = d.min()
+    cands = np.nonzero(d == best)[0]
+    even = [c for c in cands if c % 2 == 0]
+    return int(even[0] if even else cands[0])
+
+
+def bf_e4m3(v):
+    v = float(np.float32(v))
+    sign = 0x80 if math.copysign(1, v) < 0 else 0
+    a = abs(v)
+    if a >= 448.0:
+        return sign | 0x7E
+    return sign | _nearest_code(a, E4M3_POS)
+
+
+def bf_e2m1(v):
+    v = float(np.float32(v))
+    sign = 8 if math.copysign(1, v) < 0 else 0
+    a = abs(v)
+    if a > 6.0:
+        return sign | 7
+    return sign | _nearest_code(a, E2M1_POS)
+
+
+# ------------------------------------------------------------------ decode
+
+def test_e2m1_golden(orc):
+    assert len(E2M1) == 16
+    for code, v in E2M1.items():
+        assert _same(orc.e2m1_value(code), v), hex(code)
+
+
+def test_e4m3_golden(orc):
+    for b, v in _golden_table("e4m3_codes.txt").items():
+        assert _same(orc.e4m3_value(b), v), hex(b)
+
+
+def test_e4m3_all_codes_match_torch(orc):
+    for b in range(256):
+        assert _same(orc.e4m3_value(b), float(E4M3_T[b])), hex(b)
+
+
+def test_e4m3_invariants(orc):
+    vals = [orc.e4m3_value(b) for b in range(0x7F)]
+    assert all(vals[i] < vals[i + 1] for i in range(len(vals) - 1))
+    assert vals[-1] == 448.0 and vals[1] == 2.0 ** -9 and vals[0] == 0.0
+    assert math.isnan(orc.e4m3_value(0x7F)) and math.isnan(orc.e4m3_value(0xFF))
+    for b in range(0x7F):
+        assert _same(orc.e4m3_value(b | 0x80), -vals[b])
+
+
+def test_bf16_decode_matches_torch(orc):
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 1 << 16, size=3000, dtype=np.uint16)
+    ref = _bf16_values(bits)
+    for b, r in zip(bits, ref):
+        assert _same(orc.bf16_value(int(b)), float(r))
+
+
+# ------------------------------------------------------------------ encode
+
+def test_e4m3_encode_identity_on_codes(orc):
+    for b in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert orc.e4m3_encode(orc.e4m3_value(b)) == b, hex(b)
+
+
+def test_e4m3_encode_midpoints_go_to_even(orc):
+    for b in range(0x7E):
+        lo, hi = E4M3_T[b], E4M3_T[b + 1]
+        mid = (lo + hi) / 2
+        assert float(np.float32(mid)) == mid
+        want = b if b % 2 == 0 else b + 1
+        assert orc.e4m3_encode(mid) == want
+        assert orc.e4m3_encode(-mid) == want | 0x80
+        below = float(np.nextafter(np.float32(mid), np.float32(0)))
+        above = float(np.nextafter(np.float32(mid), np.float32(1e9)))
+        assert orc.e4m3_encode(below) == b
+        assert orc.e4m3_encode(above) == b + 1
+
+
+def test_e4m3_encode_bruteforce_random(orc):
+    rnd = random.Random(11)
+    vals = [0.0, -0.0, 448.0, 449.0, 464.0, 480.0, 1e30, -1e30, float("inf"),
+            2.0 ** -10, 2.0 ** -9, 1.5 * 2.0 ** -10, 3e-45]
+    vals += [rnd.choice([-1, 1]) * 2.0 ** rnd.uniform(-13, 10) for _ in range(20000)]
+    for v in vals:
+        assert orc.e4m3_encode(v) == bf_e4m3(v), v
+
+
+def test_e4m3_encode_matches_torch_in_range(orc):
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(20000) * 60).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for x, r in zip(v, ref):
+        assert orc.e4m3_encode(float(x)) == int(r), x
+
+
+def test_e2m1_encode_bruteforce(orc):
+    rnd = random.Random(12)
+    vals = [0.0, -0.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 7.0, 1e9]
+    for lo, hi in zip([0, .5, 1, 1.5, 2, 3, 4], [.5, 1, 1.5, 2, 3, 4, 6]):
+        m = (lo + hi) / 2
+        vals += [m, float(np.nextafter(np.float32(m), np.float32(0))),
+                 float(np.nextafter(np.float32(m), np.float32(9)))]
+    vals += [rnd.uniform(-8, 8) for _ in range(20000)]
+    for v in vals:
+        assert orc.e2m1_encode(v) == bf_e2m1(v), v
+        assert orc.e2m1_encode(-v) == bf_e2m1(-v), -v
+
+
+# -------------------------------------------------------- golden examples
+
+def _parse_example(name):
+    d = {"w": [], "codes": []}
+    for r in read_golden(name):
+        if r[0] in ("w", "codes"):
+            d[r[0]].append(r[1:])
+        else:
+            d[r[0]] = r[1:]
+    return d
+
+
+def _nibble(nib, m, k):
+    return (int(nib[m, k // 2]) >> (4 * (k % 2))) & 15
+
+
+def test_nvfp4_golden_example(orc):
+    ex = _parse_example("nvfp4_example.txt")
+    W = np.array([[float(v) for blk in ex["w"] for v in blk]], np.float32)
+    assert W.shape == (1, int(ex["K"][0]))
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    assert gs == float(ex["gs"][0])
+    assert [int(s) for s in sc[0]] == [int(s, 16) for s in ex["scales"]]
+    codes = [int(c, 16) for blk in ex["codes"] for c in blk]
+    assert [_nibble(nib, 0, k) for k in range(W.shape[1])] == codes
+    x = np.full((1, W.shape[1]), 0x3F80, np.uint16)            # BF16 1.0
+    y, a = orc.gemv_nvfp4(nib, sc, gs, x)
+    assert y[0, 0] == float(ex["y_ones"][0])
+    assert a[0, 0] == float(ex["a_ones"][0])
+
+
+def test_fp8_golden_example(orc):
+    ex = _parse_example("fp8_example.txt")
+    W = np.array([[float(v) for v in r] for r in ex["w"]], np.float32)
+    q, rs = orc.fp8_quantise(W)
+    assert rs[0] == float(ex["rs"][0]) and rs[2] == 0.0
+    for m, row in enumerate(ex["codes"]):
+        assert [int(c) for c in q[m]] == [int(c, 16) for c in row], m
+
+
+# ------------------------------------------------------ quantiser pinning
+
+def _rand_w(seed, M, K, std=0.02):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn((M, K), generator=g) * std).numpy()
+
+
+def test_nvfp4_quantiser_decisions_bruteforce(orc):
+    W = _rand_w(21, 8, 96)
+    W[3, 16:32] = 0.0                                  # a zero block
+    W[5, 32:48] *= 1e-5                                # a subnormal-scale block
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    f32 = np.float32
+    assert gs == f32(np.abs(W).max()) / f32(2688.0)
+    assert sc[3, 1] == 0 and sc[5, 2] < 8              # zero and subnormal scale
+    for m in range(W.shape[0]):
+        for b in range(W.shape[1] // 16):
+            blk = W[m, 16 * b:16 * b + 16]
+            s = (f32(np.abs(blk).max()) / f32(gs)) / f32(6.0)
+            assert sc[m, b] == bf_e4m3(s), (m, b)
+            d = f32(E4M3_T[sc[m, b]]) * f32(gs)
+            for j, w in enumerate(blk):
+                want = 0 if d == 0 else bf_e2m1(f32(w) / d)
+                assert _nibble(nib, m, 16 * b + j) == want, (m, b, j)
+
+
+def test_nvfp4_quantiser_invariants(orc):
+    W = _rand_w(22, 16, 256)
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    What = orc.nvfp4_dequant(nib, sc, gs, *W.shape)
+    for m in range(W.shape[0]):
+        for b in range(W.shape[1] // 16):
+            d = E4M3_T[sc[m, b]] * gs
+            q = W[m, 16 * b:16 * b + 16] / d
+            deq = What[m, 16 * b:16 * b + 16] / d
+            # every element within the largest half-gap of the E2M1 grid
+            assert np.all(np.abs(q - deq) <= 1.0 + 1e-6)
+            # the block maximum lands on the top of the grid (magnitude code 7)
+            j = int(np.argmax(np.abs(W[m, 16 * b:16 * b + 16])))
+            assert _nibble(nib, m, 16 * b + j) & 7 == 7
+    # power-of-two scaling of W scales gs and leaves every code unchanged
+    nib2, sc2, gs2 = orc.nvfp4_quantise(W * np.float32(8.0))
+    assert gs2 == gs * 8 and np.array_equal(nib, nib2) and np.array_equal(sc, sc2)
+
+
+def test_nvfp4_requantise_is_idempotent(orc):
+    for seed in range(4):
+        W = _rand_w(30 + seed, 8, 128)
+        nib, sc, gs = orc.nvfp4_quantise(W)
+        W2 = orc.nvfp4_dequant(nib, sc, gs, *W.shape).astype(np.float32)
+        nib2, sc2, gs2 = orc.nvfp4_quantise(W2)
+        assert gs2 == gs and np.array_equal(sc, sc2) and np.array_equal(nib, nib2)
+
+
+def test_fp8_quantiser_decisions_and_invariants(orc):
+    W = _rand_w(23, 6, 64)
+    W[2] = 0.0
+    q, rs = orc.fp8_quantise(W)
+    f32 = np.float32
+    for m in range(W.shape[0]):
+        assert rs[m] == f32(np.abs(W[m]).max()) / f32(448.0)
+        for k in range(W.shape[1]):
+            want = 0 if rs[m] == 0 else bf_e4m3(f32(W[m, k]) / rs[m])
+            assert q[m, k] == want
+        if rs[m] > 0:
+            assert (q[m, int(np.argmax(np.abs(W[m])))] & 0x7F) == 0x7E
+    W2 = orc.fp8_dequant(q, rs, *W.shape).astype(np.float32)
+    q2, rs2 = orc.fp8_quantise(W2)
+    assert np.array_equal(rs, rs2) and np.array_equal(q, q2)
+
+
+# --------------------------------------------------------------- the GEMV
+
+def _x_bits(seed, N, K, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn((N, K), generator=g) * scale).to(torch.bfloat16)
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+def _exact(wv, x_bits):
+    """Exact rational y[n][m], a[n][m] from Fraction weights wv[m][k]."""
+    xv = _bf16_values(x_bits)
+    xs = [[Fraction(float(v)) for v in row] for row in xv]
+    N, M, K = len(xs), len(wv), len(wv[0])
+    y = [[sum(wv[m][k] * xs[n][k] for k in range(K)) for m in range(M)] for n in range(N)]
+    a = [[sum(abs(wv[m][k] * xs[n][k]) for k in range(K)) for m in range(M)]
+         for n in range(N)]
+    return y, a
+
+
+def test_gemv_nvfp4_bruteforce_4x16(orc):
+    for seed in range(3):
+        M, K, N = 4, 16, 3
+        W = _rand_w(40 + seed, M, K)
+        nib, sc, gs = orc.nvfp4_quantise(W)
+        x = _x_bits(50 + seed, N, K)
+        y, a = orc.gemv_nvfp4(nib, sc, gs, x)
+        # weights decoded from the golden tables, exact rationals
+        wv = [[Fraction(E2M1[_nibble(nib, m, k)]) * Fraction(float(E4M3_T[sc[m, k // 16]]))
+               * Fraction(gs) for k in range(K)] for m in range(M)]
+        ye, ae = _exact(wv, x)
+        u = 2.0 ** -53
+        for n in range(N):
+            for m in range(M):
+                assert abs(Fraction(y[n, m]) - ye[n][m]) <= (K - 1) * u * ae[n][m]
+                assert abs(Fraction(a[n, m]) - ae[n][m]) <= (K - 1) * u * ae[n][m]
+
+
+def test_gemv_fp8_bruteforce_4x16(orc):
+    M, K, N = 4, 16, 2
+    W = _rand_w(44, M, K)
+    q, rs = orc.fp8_quantise(W)
+    x = _x_bits(54, N, K)
+    y, a = orc.gemv_fp8(q, rs, x)
+    wv = [[Fraction(float(E4M3_T[q[m, k]])) * Fraction(float(rs[m])) for k in range(K)]
+          for m in range(M)]
+    ye, ae = _exact(wv, x)
+    for n in range(N):
+        for m in range(M):
+            assert abs(Fraction(y[n, m]) - ye[n][m]) <= (K - 1) * 2.0 ** -53 * ae[n][m]
+            assert abs(Fraction(a[n, m]) - ae[n][m]) <= (K - 1) * 2.0 ** -53 * ae[n][m]
+
+
+def test_gemv_rows_columns_and_threads_are_independent(orc):
+    W = _rand_w(45, 32, 64)
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    x = _x_bits(55, 5, 64)
+    y, a = orc.gemv_nvfp4(nib, sc, gs, x)
+    rows = np.array([31, 0, 7, 7], np.int64)
+    ys, as_ = orc.gemv_nvfp4(nib, sc, gs, x[2:4], rows=rows)
+    assert np.array_equal(ys, y[2:4][:, rows]) and np.array_equal(as_, a[2:4][:, rows])
+    y4, _ = orc.gemv_nvfp4(nib, sc, gs, x, threads=4)
+    assert np.array_equal(y4, y)
+
+
+def test_gemv_linearity_in_x(orc):
+    M, K = 16, 128
+    W = _rand_w(46, M, K)
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    x1 = _bits_to_bf16(_x_bits(56, 1, K))
+    x2 = _bits_to_bf16(_x_bits(57, 1, K))
+    mask = torch.arange(K) % 3 == 0
+    x1 = torch.where(mask, x1, torch.zeros_like(x1))
+    x2 = torch.where(mask, torch.zeros_like(x2), x2)
+    alpha, beta = 4.0, -0.25
+    xs = (alpha * x1.float() + beta * x2.float()).to(torch.bfloat16)
+    assert torch.equal(xs.float(), alpha * x1.float() + beta * x2.float())
+
+    def bits(t):
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    y1, a1 = orc.gemv_nvfp4(nib, sc, gs, bits(x1))
+    y2, a2 = orc.gemv_nvfp4(nib, sc, gs, bits(x2))
+    ys, _ = orc.gemv_nvfp4(nib, sc, gs, bits(xs))
+    bound = K * 2.0 ** -52 * (abs(alpha) * a1 + abs(beta) * a2)
+    assert np.all(np.abs(ys - (alpha * y1 + beta * y2)) <= bound)
+
+
+def test_gemv_zero_block_contributes_nothing(orc):
+    M, K = 8, 64
+    W = _rand_w(47, M, K)
+    W[:, 16:32] = 0.0
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    assert np.all(sc[:, 1] == 0) and np.all(nib[:, 8:16] == 0)
+    x = _x_bits(58, 2, K)
+    x0 = x.copy()
+    x0[:, 16:32] = 0
+    y, _ = orc.gemv_nvfp4(nib, sc, gs, x)
+    y0, _ = orc.gemv_nvfp4(nib, sc, gs, x0)
+    assert np.array_equal(y, y0)
+    # an all-zero matrix gives gs = 0, zero codes and y = 0
+    nibz, scz, gsz = orc.nvfp4_quantise(np.zeros((3, 32), np.float32))
+    assert gsz == 0.0 and not nibz.any() and not scz.any()
+    yz, az = orc.gemv_nvfp4(nibz, scz, gsz, x[:, :32])
+    assert not yz.any() and not az.any()
+
+
+def test_gemv_all_max_nibble_closed_form(orc):
+    M, K, N = 3, 64, 2
+    nib = np.full((M, K // 2), 0x77, np.uint8)
+    sc = np.full((M, K // 16), 0x7E, np.uint8)
+    gs = 0.03125
+    x = _x_bits(59, N, K)
+    y, a = orc.gemv_nvfp4(nib, sc, gs, x)
+    xv = _bf16_values(x)
+    for n in range(N):
+        want = 2688.0 * gs * math.fsum(xv[n])
+        wanta = 2688.0 * gs * math.fsum(np.abs(xv[n]))
+        assert np.all(np.abs(y[n] - want) <= K * 2.0 ** -53 * wanta)
+        assert np.all(np.abs(a[n] - wanta) <= K * 2.0 ** -53 * wanta)
+
+
+def test_gemv_textbook_reduction(orc):
+    """Scales 1.0 (0x38) and gs = 1: y equals numpy's float64 x @ e2m1(W).T."""
+    rng = np.random.default_rng(60)
+    M, K, N = 12, 64, 3
+    codes = rng.integers(0, 16, size=(M, K))
+    nib = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sc = np.full((M, K // 16), 0x38, np.uint8)
+    x = _x_bits(61, N, K)
+    y, _ = orc.gemv_nvfp4(nib, sc, 1.0, x)
+    wv = np.vectorize(lambda c: E2M1[int(c)])(codes).astype(np.float64)
+    assert np.array_equal(y, _bf16_values(x) @ wv.T)
+
+
+def test_gemv_fp8_textbook_reduction(orc):
+    """Row scales 1.0: y equals numpy's float64 x @ e4m3(Q).T."""
+    rng = np.random.default_rng(62)
+    M, K, N = 10, 48, 2
+    q = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x01                       # no NaN codes
+    rs = np.ones(M, np.float32)
+    x = _x_bits(63, N, K, scale=0.25)
+    y, _ = orc.gemv_fp8(q, rs, x)
+    assert np.array_equal(y, _bf16_values(x) @ E4M3_T[q].T)
+
+
+def test_check_counts_out_of_tolerance(orc):
+    yref = np.array([1.0, -2.0, 100.0, 0.0])
+    a = np.array([10.0, 10.0, 1000.0, 0.0])
+    ok = torch.tensor(yref, dtype=torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bad, worst = orc.check(ok, yref, a)
+    assert bad == 0 and worst <= 1.0
+    off = ok.copy()
+    off[2] = torch.tensor([104.5], dtype=torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)[0]
+    bad, worst = orc.check(off, yref, a)          # 4.5 > 4e-3*1000 + 1e-6
+    assert bad == 1 and worst > 1.0
