@@ -1,0 +1,344 @@
+"""Benchmark: achieved HBM GB/s and us per fused verify pass.
+
+One step = one fused, ordered verify pass (all products of the layer stack
+for N = 8 columns) over the full synthetic workload: 64 layers x (NVFP4
+q, k, v, o 5120x5120; NVFP4 gate+up 34816x5120; row-scaled FP8 down
+5120x17408) + NVFP4 head 151936x5120 = 16.34 GB of weight+scale bytes read
+per pass.  ``value`` is those bytes per second, with weights and x resident
+in HBM; ``e2e`` is the same metric through the public API with x copied from
+pinned host memory and y copied back inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 it runs under torchrun, one independent replica per GPU (the
+product has no exchange step), and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and µs per NVFP4 verify pass, N=1–8"
+WORKLOAD = ("verify stack: 64 layers x (NVFP4 q,k,v,o 5120x5120; NVFP4 gate+up 34816x5120 "
+            "as two 17408x5120 halves; row-scaled FP8 down 5120x17408) + NVFP4 head "
+            "151936x5120; W ~ N(0,0.02) RTN-quantised, x BF16 ~ N(0,1); seed 4")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--N", type=int, default=8)
+    ap.add_argument("--widths", default="1,2,4", help="extra widths reported per pass")
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(p) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == "stream_kernel" and parts[1] == "verify_stack_N8":
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) >= 9:
+                    rows.append(c)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device=None):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def cpu_sample(seconds: float):
+    """Time the CPU oracle's GEMV on a bounded sample of the workload: the
+    first layer's q (NVFP4 5120x5120) and down (FP8 5120x17408) and 2048 rows
+    of the head, N = 8, all host threads, repeated for about `seconds`."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from verify_gemm_gb300.inputs import HIDDEN, INTERMEDIATE, generator, draw_weight, draw_x
+
+    orc = oracle.get()
+    threads = os.cpu_count() or 1
+    g = generator(4)
+    Wq = draw_weight(g, HIDDEN, HIDDEN).numpy()
+    Wd = draw_weight(g, HIDDEN, INTERMEDIATE).numpy()
+    Wh = draw_weight(g, 2048, HIDDEN).numpy()
+    x5 = draw_x(g, 8, HIDDEN).view(torch.int16).numpy().view(np.uint16)
+    x17 = draw_x(g, 8, INTERMEDIATE).view(torch.int16).numpy().view(np.uint16)
+    nq, sq, gq = orc.nvfp4_quantise(Wq)
+    qd, rd = orc.fp8_quantise(Wd)
+    nh, sh, gh = orc.nvfp4_quantise(Wh)
+    nbytes = (HIDDEN * HIDDEN * 9 // 16 + 4) + (HIDDEN * INTERMEDIATE + 4 * HIDDEN) \
+        + (2048 * HIDDEN * 9 // 16)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        orc.gemv_nvfp4(nq, sq, gq, x5, threads=threads)
+        orc.gemv_fp8(qd, rd, x17, threads=threads)
+        orc.gemv_nvfp4(nh, sh, gh, x5, threads=threads)
+        done += nbytes
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"oracle FP64 GEMV, N=8, on layer-0 q (NVFP4 5120x5120), down (FP8 "
+                       f"5120x17408) and 2048 head rows, {done / nbytes:.0f} rounds in "
+                       f"{el:.1f} s; same GB/s unit (weight+scale bytes)")}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cb = cpu_sample(max(2.0, args.cpu_seconds / 2))
+    per = []
+    for _ in range(args.warmup):
+        cpu_sample(0.5)
+    for _ in range(args.steps):
+        per.append(cpu_sample(max(0.5, args.cpu_seconds / max(1, args.steps)))["value"])
+    value = statistics.median(per)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 16_335_298_560 / (value * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "N": args.N},
+            "cpu_baseline": dict(cb, value=value),
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import verify_gemm_gb300 as vg
+    from verify_gemm_gb300 import build as vbuild
+    from verify_gemm_gb300.workloads import build_stack
+
+    vbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    st = build_stack(args.N, device=dev, layers=args.layers)
+    plan = st.plan(ordered=True)
+    nbytes = st.bytes
+    torch.cuda.synchronize()
+
+    def timed(run, steps, warmup):
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(stream)
+        for i in range(steps):
+            run()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+        return sum(per), per
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    total_ms, per = timed(plan.run, args.steps, args.warmup)
+    clk = clocks.stop()
+    if plan.check() != 0:
+        raise RuntimeError("verify pass reported a device error")
+    total_ms = max_over_ranks(total_ms, world, dev)
+    value = nbytes * args.steps * world / (total_ms / 1e3) / 1e9
+    kernel_ms = statistics.mean(per)
+    achieved = nbytes / (kernel_ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+
+    extra = {}
+    unordered = st.plan(ordered=False)
+    u_ms, _ = timed(unordered.run, max(3, args.steps // 2), 2)
+    unordered.close()
+    extra["unordered_gbs"] = nbytes * max(3, args.steps // 2) / (u_ms / 1e3) / 1e9
+    widths = {}
+    for w in [int(v) for v in args.widths.split(",") if v]:
+        if w == args.N:
+            continue
+        xs = [torch.randn((w, m.K), device=dev).to(torch.bfloat16) for m in st.mats]
+        ys = [torch.empty((w, m.M), dtype=torch.bfloat16, device=dev) for m in st.mats]
+        pw = vg.VerifyPlan([(wt, x, y, m.group) for m, wt, x, y in
+                            zip(st.mats, st.weights, xs, ys)], w, ordered=True)
+        ms, _ = timed(pw.run, max(3, args.steps // 2), 2)
+        if pw.check() != 0:
+            raise RuntimeError("verify pass reported a device error")
+        pw.close()
+        us = ms / max(3, args.steps // 2) * 1e3
+        widths[str(w)] = {"us_per_pass": round(us, 1), "GBps": round(nbytes / us / 1e3, 1)}
+        del xs, ys
+    widths[str(args.N)] = {"us_per_pass": round(total_ms / args.steps * 1e3, 1),
+                           "GBps": round(nbytes / (total_ms / args.steps) / 1e6, 1)}
+
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.empty(st.x_all.shape, dtype=st.x_all.dtype, pin_memory=True)
+        x_host.copy_(st.x_all)
+        y_host = torch.empty(st.y_all.shape, dtype=st.y_all.dtype, pin_memory=True)
+
+        def e2e_step():
+            st.x_all.copy_(x_host, non_blocking=True)
+            plan.run()
+            y_host.copy_(st.y_all, non_blocking=True)
+
+        e_ms, _ = timed(e2e_step, args.steps, args.warmup)
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": nbytes * args.steps * world / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": st.x_all.numel() * 2,
+               "d2h_bytes_per_step": st.y_all.numel() * 2}
+    plan.close()
+
+    cb = None
+    if rank == 0 and world == 1:
+        cb = cpu_sample(args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4/fp8-e4m3 weights x bf16 -> f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "N": args.N, "mode": "ordered",
+                       "bytes_per_pass": nbytes, "matrices": len(st.mats),
+                       "pct_of_8TBps": round(100 * value / world / 8000, 1),
+                       "l2": "inputs 16.3 GB per pass >> 126 MB L2; no flush needed",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": profiled_traffic(),
+                         "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
+            "per_width": widths, **extra,
+            "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
+        }
+        if cb is not None:
+            line["cpu_baseline"] = cb
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+/*
+ * vgemm.h -- C ABI of the GB300 (sm_103a) NVFP4 / row-scaled FP8 verify-GEMV
+ * library (libvgemm.so).
+ *
+ * The library computes the weight-streaming product of LLM decode and
+ * speculative verification,
+ *
+ *     y[N, M] = x[N, K] . dequant(W)[M, K]^T,     N = 1..8 columns,
+ *
+ * with W in NVFP4 (E2M1 codes, one E4M3 scale per 16 elements along K, one
+ * FP32 tensor scale) or row-scaled FP8-E4M3, x and y in BF16 and FP32
+ * accumulation.  This is the "GEMVs" row of the Design table on the
+ * mtp7-device-confidence engine card (crit-hub): FP8 and NVFP4 weights fed
+ * to BF16 tensor-core fragments for 1-8 columns, where the verify pass of
+ * the card's Decode row runs 2-8 columns and a decode step one.  The
+ * card's Measured section states what makes it the hot path: a verify pass
+ * reads every weight once (19.26 GB), so its time is the weight-read time;
+ * the crit README's quality-mode comparison says the same ("a decode pass
+ * reads every weight once").
+ *
+ * Conventions (all entry points):
+ *  - Plain C; nothing throws across the ABI; every call returns a
+ *    vg_status.  Argument and alignment errors are detected on the host and
+ *    returned before anything is launched.
+ *  - Pointers marked "device" are CUDA device (or managed) memory owned by
+ *    the caller; "host" pointers are host memory.  Device pointers must be
+ *    16-byte aligned.  No entry point allocates device memory per call,
+ *    except vg_verify_plan_create, which allocates the plan's own tables
+ *    once.
+ *  - Work is enqueued on the caller's stream (a cudaStream_t; NULL is the
+ *    legacy default stream) and runs asynchronously, except where a
+ *    function says it synchronises.
+ *  - BF16 values travel as uint16_t bit patterns.
+ *  - Limits: 1 <= N <= 8, M >= 1, K >= 16, K % 16 == 0, M * K < 2^40.
+ *
+ * Device weight layout (the "packed" form; canonical forms are below):
+ *  NVFP4 codes are stored in 16-row tiles.  Each tile is a run of 64-column
+ *  units of 512 bytes, arranged so that every lane of a warp reads one
+ *  16-byte vector per unit holding 16 consecutive K positions of two rows
+ *  (one scale block of each), with the bits of each code placed for a
+ *  cheap in-register decode to BF16.  Block scales live in a separate
+ *  buffer, 256 bytes per tile per 256 columns, re-encoded losslessly so
+ *  that E4M3 subnormal scales decode like normal ones.  Row-scaled FP8
+ *  codes use 1024-byte units of the same shape; their FP32 row scales are
+ *  a plain [M] array.  Rows past M and columns past K are zero padding.
+ *  The packed buffers are opaque: use the pack / unpack / from_canonical
+ *  calls to move between them and the canonical layout.
+ *
+ * Canonical layout (the plain stored form, as the engine card's Design
+ * table "Weights" row calls it):
+ *  NVFP4: nib[M][K/2] uint8 (low nibble = even k, high nibble = odd k),
+ *         sc[M][K/16] uint8 E4M3 bytes, gscale FP32 multiplier.
+ *  FP8:   q[M][K] uint8 E4M3 bytes, rowscale[M] FP32 multipliers.
+ */
+#ifndef VGEMM_H
+#define VGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that this header does not
+ * need the CUDA headers. */
+typedef struct CUstream_st *vg_stream_t;
+
+typedef enum vg_status {
+    VG_OK = 0,
+    VG_ERR_INVALID_ARG = 1,   /* bad size, null pointer, non-finite weight */
+    VG_ERR_ALIGNMENT = 2,     /* a device pointer is not 16-byte aligned */
+    VG_ERR_UNSUPPORTED = 3,   /* no sm_103a device, or a limit exceeded */
+    VG_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    VG_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+    VG_ERR_WORKSPACE = 6      /* workspace missing or too small */
+} vg_status;
+
+/* Weight formats of vg_matrix_desc.format. */
+enum { VG_FMT_NVFP4 = 0, VG_FMT_FP8_ROWSCALE = 1 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *vg_status_string(vg_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int vg_version(void);
+
+/* Last CUDA error string seen by the library on this host thread, or "". */
+const char *vg_last_cuda_error(void);
+
+/* ------------------------------------------------------------- sizes */
+
+/* Bytes of the packed NVFP4 code buffer (*w_bytes) and block-scale buffer
+ * (*scale_bytes) for an M x K matrix.  Either output may be NULL. */
+vg_status vg_nvfp4_sizes(int64_t M, int64_t K, size_t *w_bytes, size_t *scale_bytes);
+
+/* Bytes of the packed row-scaled FP8 code buffer for an M x K matrix. */
+vg_status vg_fp8_sizes(int64_t M, int64_t K, size_t *w_bytes);
+
+/* ----------------------------------------------------- quantise / pack */
+
+/* NVFP4 round-to-nearest quantisation of an FP32 matrix into the packed
+ * layout (load-time re-encoding: the crit landing page's "Models"
+ * paragraph names round-to-nearest post-training quantisation to NVFP4;
+ * the engine card's Model section re-encodes the head to NVFP4 at load).
+ *   W           device FP32 [M][K], row-major, leading dimension K.
+ *   w_out       device, vg_nvfp4_sizes(...).w_bytes bytes (written).
+ *   scales_out  device, vg_nvfp4_sizes(...).scale_bytes bytes (written;
+ *               also used as scratch for the amax reduction).
+ *   gscale_out  host; receives the FP32 tensor scale (dequant multiplier).
+ * Recipe, in FP32 IEEE arithmetic: gs = amax|W| / 2688; per 16-block
+ * s = (blockamax / gs) / 6, scale code = E4M3(s) rounded to nearest even
+ * with saturation; d = E4M3value(code) * gs; code of w = E2M1(w / d) to
+ * nearest even with saturation (all codes 0 when d == 0).
+ * Synchronises the stream once (to read amax).  NaN/Inf in W gives
+ * VG_ERR_INVALID_ARG. */
+vg_status vg_nvfp4_pack(const float *W, int64_t M, int64_t K,
+                        void *w_out, void *scales_out, float *gscale_out,
+                        vg_stream_t stream);
+
+/* Row-scaled FP8-E4M3 quantisation (engine card, Model section: the draft
+ * layer "re-encoded as row-scaled FP8"):  rs[m] = rowamax / 448,
+ * code = E4M3(w / rs[m]) rounded to nearest even with saturation (all codes
+ * 0 when rs[m] == 0).
+ *   W            device FP32 [M][K].
+ *   w_out        device, vg_fp8_sizes bytes.
+ *   rowscale_out device FP32 [M].
+ * Synchronises once (to check the row scales).  NaN/Inf in W gives
+ * VG_ERR_INVALID_ARG. */
+vg_status vg_fp8_pack(const float *W, int64_t M, int64_t K,
+                      void *w_out, float *rowscale_out, vg_stream_t stream);
+
+/* Packed NVFP4 -> canonical nib[M][K/2] and sc[M][K/16] (device). */
+vg_status vg_nvfp4_unpack(const void *w, const void *scales, int64_t M, int64_t K,
+                          uint8_t *nib_out, uint8_t *sc_out, vg_stream_t stream);
+
+/* Packed FP8 -> canonical q[M][K] (device). */
+vg_status vg_fp8_unpack(const void *w, int64_t M, int64_t K, uint8_t *q_out,
+                        vg_stream_t stream);
+
+/* Canonical NVFP4 (device nib, sc) -> packed layout.  Scale bytes must be
+ * non-negative and not NaN (E4M3 bytes 0x00..0x7E); otherwise
+ * VG_ERR_INVALID_ARG.  Blocks whose scale is 0 are stored with zero codes
+ * (their value is 0 either way).  Synchronises once. */
+vg_status vg_nvfp4_from_canonical(const uint8_t *nib, const uint8_t *sc,
+                                  int64_t M, int64_t K, void *w_out, void *scales_out,
+                                  vg_stream_t stream);
+
+/* Canonical FP8 codes (device q[M][K]) -> packed layout.  NaN codes
+ * (0x7F, 0xFF) give VG_ERR_INVALID_ARG.  Synchronises once; w_out's first
+ * bytes are used as scratch for the check before being written. */
+vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t K, void *w_out,
+                                vg_stream_t stream);
+
+/* ------------------------------------------------------------ the GEMV */
+
+/* Workspace bytes that vg_gemv_nvfp4 / vg_gemv_fp8_rowscale need for an
+ * M x K matrix on the current device (format: VG_FMT_*).  The workspace
+ * holds per-row-block arrival counters, a device error word and the FP32
+ * partial sums of row blocks whose K range is split between two or more
+ * thread blocks.  It must be zero-filled once when allocated; every call
+ * leaves it zero-filled again.  Calls that share a workspace must not
+ * overlap on the GPU. */
+vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes);
+
+/* y[n][m] = bf16( sum_k x[n][k] * dequant(W)[m][k] ), NVFP4 weights.
+ *   w, scales   device, packed by vg_nvfp4_pack / vg_nvfp4_from_canonical.
+ *   gscale      FP32 tensor scale (from the pack).
+ *   x           device BF16 [N][K], row-major, 16-byte aligned.
+ *   y           device BF16 [N][M], row-major (written).
+ *   workspace   device, >= vg_gemv_workspace_size bytes (see there).
+ * Accumulation is FP32; y is rounded to nearest even.  The result for
+ * column n does not depend on N or on the other columns, and a repeated
+ * call gives the same bits. */
+vg_status vg_gemv_nvfp4(const void *w, const void *scales, float gscale,
+                        const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
+                        void *workspace, size_t workspace_bytes, vg_stream_t stream);
+
+/* Same for row-scaled FP8 weights: dequant(W)[m][k] = E4M3(q[m][k]) * rowscale[m].
+ *   rowscale  device FP32 [M]. */
+vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale,
+                               const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
+                               void *workspace, size_t workspace_bytes, vg_stream_t stream);
+
+/* Reads and clears the device error word of a GEMV workspace (synchronous).
+ * *device_error receives 0, or a nonzero code if a bounded wait inside a
+ * kernel ran out (then the workspace is also re-zeroed). */
+vg_status vg_gemv_workspace_check(void *workspace, size_t workspace_bytes,
+                                  int *device_error, vg_stream_t stream);
+
+/* -------------------------------------------------- fused verify pass */
+
+/* One matrix of a verify pass (a layer stack).  Matrices must be listed
+ * with non-decreasing group; group g+1 depends on group g. */
+typedef struct vg_matrix_desc {
+    int32_t format;          /* VG_FMT_NVFP4 or VG_FMT_FP8_ROWSCALE */
+    int32_t group;           /* dependency group */
+    int64_t M, K;
+    const void *w;           /* device, packed codes */
+    const void *scales;      /* device, packed block scales (NVFP4), else NULL */
+    const float *rowscale;   /* device FP32 [M] (FP8), else NULL */
+    float gscale;            /* tensor scale (NVFP4) */
+    const uint16_t *x;       /* device BF16 [N][K] */
+    uint16_t *y;             /* device BF16 [N][M] */
+} vg_matrix_desc;
+
+typedef struct vg_verify_plan vg_verify_plan;
+
+/* Options of vg_verify_plan_create_ex (zero-initialise, then set). */
+typedef struct vg_plan_options {
+    int32_t ordered;          /* 1: group g's products wait for group g-1 (default);
+                                 0: no waits (an upper bound) */
+    int32_t max_ctas;         /* 0: one thread block per SM */
+    int64_t wait_timeout_ns;  /* bound of every device-side wait; 0: 2 s */
+    int32_t hold_group;       /* fault-injection: if >= 0, the completion of this
+                                 group is never signalled, so the next group's
+                                 wait runs out (VG_ERR_TIMEOUT); -1: off */
+    int32_t reserved;
+} vg_plan_options;
+
+/* Plan a fused verify pass over `count` matrices for N columns: one
+ * persistent, cooperative launch streams every weight once, groups in
+ * order (engine card, Decode row: the verify pass for the drafts made, 2-8
+ * columns; Measured section: 19.26 GB read per pass).  Allocates the
+ * plan's descriptor table, counters and partial-sum space once.
+ * Descriptors (pointers included) are copied; buffer contents may change
+ * between passes. */
+vg_status vg_verify_plan_create(const vg_matrix_desc *mats, int count, int N,
+                                int ordered, vg_verify_plan **plan_out);
+vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,
+                                   const vg_plan_options *opt, vg_verify_plan **plan_out);
+
+/* Enqueue one verify pass on `stream`.  Passes of one plan must not overlap
+ * on the GPU. */
+vg_status vg_verify_pass(vg_verify_plan *plan, vg_stream_t stream);
+
+/* Synchronises the stream, reads the plan's device error word and, if it is
+ * set, clears it and resets the plan's counters.  *device_error: 0 or a
+ * nonzero code (a bounded wait ran out).  Returns VG_ERR_TIMEOUT if set. */
+vg_status vg_verify_plan_check(vg_verify_plan *plan, vg_stream_t stream, int *device_error);
+
+/* Weight+scale bytes one pass streams (the algorithmic byte count). */
+vg_status vg_verify_plan_bytes(const vg_verify_plan *plan, int64_t *bytes);
+
+/* Number of thread blocks the pass launches. */
+vg_status vg_verify_plan_grid(const vg_verify_plan *plan, int *ctas);
+
+vg_status vg_verify_plan_destroy(vg_verify_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VGEMM_H */

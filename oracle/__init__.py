@@ -62,6 +62,8 @@ def _declare(lib):
         "vgo_e2m1_encode": (ctypes.c_int, [ctypes.c_float]),
         "vgo_nvfp4_quantise": (ctypes.c_int, [P, i64, i64, P, P, P]),
         "vgo_fp8_quantise": (ctypes.c_int, [P, i64, i64, P, P]),
+        "vgo_amax": (ctypes.c_float, [P, i64]),
+        "vgo_nvfp4_quantise_gs": (None, [P, i64, i64, ctypes.c_float, P, P]),
         "vgo_nvfp4_dequant": (None, [P, P, ctypes.c_float, i64, i64, P]),
         "vgo_fp8_dequant": (None, [P, P, i64, i64, P]),
         "vgo_gemv_nvfp4": (None, [P, P, ctypes.c_float, P, ctypes.c_int, i64, i64,
@@ -134,6 +136,19 @@ class Oracle:
         if self.lib.vgo_nvfp4_quantise(_ptr(W), M, K, _ptr(nib), _ptr(sc), _ptr(gs)):
             raise ValueError("non-finite weight")
         return nib, sc, float(gs[0])
+
+    def amax(self, W):
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        return float(self.lib.vgo_amax(_ptr(W), W.size))
+
+    def nvfp4_quantise_gs(self, W, gs):
+        """Per-block NVFP4 quantisation of rows W [R, K] with a given gs."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        M, K = W.shape
+        nib = np.zeros((M, K // 2), np.uint8)
+        sc = np.zeros((M, K // 16), np.uint8)
+        self.lib.vgo_nvfp4_quantise_gs(_ptr(W), M, K, float(gs), _ptr(nib), _ptr(sc))
+        return nib, sc
 
     def fp8_quantise(self, W):
         """FP32 [M, K] -> (q uint8 [M, K], rs float32 [M])."""

@@ -123,18 +123,20 @@ static int all_finite(const float *W, int64_t n)
     return 1;
 }
 
-int vgo_nvfp4_quantise(const float *W, int64_t M, int64_t K,
-                       uint8_t *nib, uint8_t *sc, float *gs_out)
+float vgo_amax(const float *W, int64_t n)
 {
-    int64_t m, b, i;
-    float amax = 0.0f, gs;
-    if (!all_finite(W, M * K))
-        return -1;
-    for (i = 0; i < M * K; ++i)
+    int64_t i;
+    float amax = 0.0f;
+    for (i = 0; i < n; ++i)
         if (fabsf(W[i]) > amax)
             amax = fabsf(W[i]);
-    gs = amax / 2688.0f;                          /* 2688 = 6 * 448 */
-    *gs_out = gs;
+    return amax;
+}
+
+void vgo_nvfp4_quantise_gs(const float *W, int64_t M, int64_t K, float gs,
+                           uint8_t *nib, uint8_t *sc)
+{
+    int64_t m, b;
     memset(nib, 0, (size_t)(M * (K / 2)));
     for (m = 0; m < M; ++m) {
         for (b = 0; b < K / 16; ++b) {
@@ -164,6 +166,17 @@ int vgo_nvfp4_quantise(const float *W, int64_t M, int64_t K,
             }
         }
     }
+}
+
+int vgo_nvfp4_quantise(const float *W, int64_t M, int64_t K,
+                       uint8_t *nib, uint8_t *sc, float *gs_out)
+{
+    float gs;
+    if (!all_finite(W, M * K))
+        return -1;
+    gs = vgo_amax(W, M * K) / 2688.0f;            /* 2688 = 6 * 448 */
+    *gs_out = gs;
+    vgo_nvfp4_quantise_gs(W, M, K, gs, nib, sc);
     return 0;
 }
 

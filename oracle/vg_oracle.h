@@ -54,6 +54,14 @@ int vgo_e2m1_encode(float v);
 int vgo_nvfp4_quantise(const float *W, int64_t M, int64_t K,
                        uint8_t *nib, uint8_t *sc, float *gs_out);
 
+/* Largest |W[i]| over n elements (FP32, exact). */
+float vgo_amax(const float *W, int64_t n);
+
+/* The per-block part of vgo_nvfp4_quantise for a given tensor scale gs,
+ * so that a subset of rows can be quantised with the whole matrix's gs. */
+void vgo_nvfp4_quantise_gs(const float *W, int64_t M, int64_t K, float gs,
+                           uint8_t *nib, uint8_t *sc);
+
 /* Row-scaled FP8-E4M3 quantisation (engine card, Model section: "re-encoded
  * as row-scaled FP8").  Returns 0, or -1 if W holds a NaN/Inf. */
 int vgo_fp8_quantise(const float *W, int64_t M, int64_t K,

@@ -1,0 +1,394 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+* Packers: GPU pack -> unpack equals the oracle's quantisation bit for bit.
+* GEMV: every element within |y - y_ref| <= 4e-3 * sum|w x| + 1e-6, at
+  sizes that span several tiles, chunks and row blocks plus ragged tails,
+  and at the full workload sizes (all rows where the oracle is quick,
+  sampled rows for the 151936-row head).
+* Properties the pages ask of the operator (engine card, Checks section:
+  FP8/NVFP4 GEMVs for 1-8 columns with column invariance; crit README,
+  Kernel workbench: the same bits on a repeat).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def vg():
+    from verify_gemm_gb300 import build
+
+    build.build()
+    import verify_gemm_gb300 as vg
+
+    torch.cuda.init()
+    return vg
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def rand_w(seed, M, K, std=0.02):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((M, K), generator=g) * std
+
+
+def rand_x(seed, N, K, outliers=0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((N, K), generator=g)
+    if outliers:
+        x[:, torch.randperm(K, generator=g)[:outliers]] *= 20
+    return x.to(torch.bfloat16)
+
+
+def assert_close(orc, y_gpu, yref, a, what=""):
+    bad, worst = orc.check(bits(y_gpu), yref, a)
+    assert bad == 0, f"{what}: {bad} elements out of tolerance (worst ratio {worst:.3g})"
+    return worst
+
+
+# ------------------------------------------------------------------ packers
+
+PACK_SHAPES = [(256, 512), (17, 80), (48, 16), (1, 16), (130, 1040), (300, 2064), (64, 5120)]
+
+
+@pytest.mark.parametrize("M,K", PACK_SHAPES)
+def test_nvfp4_pack_is_bit_exact(vg, orc, M, K):
+    W = rand_w(M * 7 + K, M, K)
+    W[0, :16] = 0.0                                       # zero block
+    if M > 2:
+        W[2, 16:32 if K > 16 else 16] *= 1e-5             # tiny (subnormal) scale
+    wt = vg.nvfp4_pack(W.cuda())
+    nib_g, sc_g = vg.nvfp4_unpack(wt)
+    nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+    assert wt.gscale == gs
+    assert np.array_equal(sc_g.cpu().numpy(), sc)
+    assert np.array_equal(nib_g.cpu().numpy(), nib)
+
+
+@pytest.mark.parametrize("M,K", PACK_SHAPES)
+def test_fp8_pack_is_bit_exact(vg, orc, M, K):
+    W = rand_w(M * 11 + K, M, K)
+    W[M // 2] = 0.0                                       # zero row
+    wt = vg.fp8_pack(W.cuda())
+    q, rs = orc.fp8_quantise(W.numpy())
+    assert np.array_equal(wt.rowscale.cpu().numpy(), rs)
+    assert np.array_equal(vg.fp8_unpack(wt).cpu().numpy(), q)
+
+
+def test_nvfp4_all_zero_matrix(vg, orc):
+    wt = vg.nvfp4_pack(torch.zeros(32, 64, device="cuda"))
+    assert wt.gscale == 0.0
+    y = vg.gemv(wt, rand_x(1, 3, 64).cuda())
+    assert not y.float().any()
+
+
+def test_pack_rejects_non_finite(vg):
+    for bad in (float("nan"), float("inf")):
+        W = torch.zeros(16, 32, device="cuda")
+        W[3, 5] = bad
+        with pytest.raises(vg.VGError):
+            vg.nvfp4_pack(W)
+        with pytest.raises(vg.VGError):
+            vg.fp8_pack(W)
+
+
+def test_from_canonical_round_trip(vg):
+    rng = np.random.default_rng(3)
+    M, K = 40, 320
+    nib = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    sc = rng.integers(1, 0x7F, (M, K // 16), dtype=np.uint8)     # no zero, no NaN
+    wt = vg.nvfp4_from_canonical(torch.from_numpy(nib).cuda(), torch.from_numpy(sc).cuda(), 0.5)
+    n2, s2 = vg.nvfp4_unpack(wt)
+    assert np.array_equal(n2.cpu().numpy(), nib) and np.array_equal(s2.cpu().numpy(), sc)
+    # a zero scale stores zero codes (the block's value is 0 either way)
+    sc[1, 2] = 0
+    wt = vg.nvfp4_from_canonical(torch.from_numpy(nib).cuda(), torch.from_numpy(sc).cuda(), 0.5)
+    n2, _ = vg.nvfp4_unpack(wt)
+    assert not n2.cpu().numpy()[1, 16:24].any()
+    # negative or NaN scale bytes are rejected
+    for b in (0x80, 0x7F):
+        sc[0, 0] = b
+        with pytest.raises(vg.VGError):
+            vg.nvfp4_from_canonical(torch.from_numpy(nib).cuda(), torch.from_numpy(sc).cuda(), 1.0)
+    q = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0
+    f8 = vg.fp8_from_canonical(torch.from_numpy(q).cuda(), torch.ones(M, device="cuda"))
+    assert np.array_equal(vg.fp8_unpack(f8).cpu().numpy(), q)
+    q[3, 3] = 0xFF
+    with pytest.raises(vg.VGError):
+        vg.fp8_from_canonical(torch.from_numpy(q).cuda(), torch.ones(M, device="cuda"))
+
+
+# --------------------------------------------------------------------- GEMV
+
+GEMV_SHAPES = [
+    (256, 512, (1,)),             # tiny workload shape
+    (17, 80, (1, 3, 8)),          # ragged rows, K tail inside a unit
+    (272, 1088, (1, 2, 5, 8)),    # 17 tiles (two row blocks), K tail chunk
+    (520, 2560, (8,)),            # several row blocks x chunks: stream-K splits
+    (4096, 576, (2,)),            # many row blocks, short K
+]
+
+
+@pytest.mark.parametrize("M,K,Ns", GEMV_SHAPES)
+def test_gemv_nvfp4_parity(vg, orc, M, K, Ns):
+    W = rand_w(M + 3 * K, M, K)
+    wt = vg.nvfp4_pack(W.cuda())
+    nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+    ws = vg.workspace_for(wt)
+    for N in Ns:
+        x = rand_x(N + M, N, K, outliers=min(8, K // 16))
+        y = vg.gemv(wt, x.cuda(), workspace=ws)
+        yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
+        assert_close(orc, y, yref, a, f"nvfp4 {M}x{K} N={N}")
+    assert vg.workspace_error(ws) == 0
+    assert not ws[256:].any(), "workspace must be left zero-filled"
+
+
+@pytest.mark.parametrize("M,K,Ns", GEMV_SHAPES)
+def test_gemv_fp8_parity(vg, orc, M, K, Ns):
+    W = rand_w(M + 5 * K, M, K)
+    wt = vg.fp8_pack(W.cuda())
+    q, rs = orc.fp8_quantise(W.numpy())
+    ws = vg.workspace_for(wt)
+    for N in Ns:
+        x = rand_x(N + 2 * M, N, K)
+        y = vg.gemv(wt, x.cuda(), workspace=ws)
+        yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
+        assert_close(orc, y, yref, a, f"fp8 {M}x{K} N={N}")
+    assert vg.workspace_error(ws) == 0
+
+
+def test_gemv_all_max_codes_closed_form(vg, orc):
+    M, K, N = 32, 256, 4
+    nib = torch.full((M, K // 2), 0x77, dtype=torch.uint8)
+    sc = torch.full((M, K // 16), 0x7E, dtype=torch.uint8)
+    wt = vg.nvfp4_from_canonical(nib.cuda(), sc.cuda(), 2.0 ** -9)
+    x = rand_x(9, N, K)
+    y = vg.gemv(wt, x.cuda())
+    yref, a = orc.gemv_nvfp4(nib.numpy(), sc.numpy(), 2.0 ** -9, bits(x))
+    assert_close(orc, y, yref, a, "all-max")
+    want = 2688.0 * 2.0 ** -9 * x.double().sum(1)[:, None]
+    scale = 2688.0 * 2.0 ** -9 * x.double().abs().sum(1)[:, None]
+    assert torch.all((y.double().cpu() - want).abs() <= 4e-3 * scale + 1e-6)
+
+
+def test_column_invariance_and_repeat_bits(vg):
+    """Column j's bits do not depend on N (1..8) or the other columns, and a
+    repeated call gives the same bits."""
+    M, K = 1040, 2048
+    for fmt in ("nvfp4", "fp8"):
+        W = rand_w(77, M, K).cuda()
+        wt = vg.nvfp4_pack(W) if fmt == "nvfp4" else vg.fp8_pack(W)
+        x8 = rand_x(78, 8, K).cuda()
+        ref = vg.gemv(wt, x8)
+        for N in range(1, 9):
+            xn = x8[:N].clone()
+            y = vg.gemv(wt, xn)
+            assert torch.equal(y.view(torch.int16), ref[:N].view(torch.int16)), (fmt, N)
+        x_other = x8.clone()
+        x_other[1:] = rand_x(79, 7, K).cuda()
+        y = vg.gemv(wt, x_other)
+        assert torch.equal(y[0].view(torch.int16), ref[0].view(torch.int16))
+        assert torch.equal(vg.gemv(wt, x8).view(torch.int16), ref.view(torch.int16))
+
+
+def test_output_canaries_untouched(vg):
+    M, K, N = 17, 96, 3
+    wt = vg.nvfp4_pack(rand_w(5, M, K).cuda())
+    buf = torch.full((N * M + 64,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    y = buf[32:32 + N * M].view(N, M)
+    vg.gemv(wt, rand_x(6, N, K).cuda(), y=y)
+    assert torch.all(buf[:32] == 12345.0) and torch.all(buf[32 + N * M:] == 12345.0)
+
+
+def test_workspace_too_small_is_rejected(vg):
+    wt = vg.nvfp4_pack(rand_w(1, 64, 64).cuda())
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(vg.VGError) as e:
+        vg.gemv(wt, rand_x(1, 1, 64).cuda(), workspace=ws)
+    assert e.value.status == 6
+
+
+# ------------------------------------------------------- full-size workloads
+
+def _full_nvfp4(vg, orc, W, Ns, outliers=0, seed=0, rows=None):
+    """Pack on the GPU, quantise on the CPU (whole matrix or sampled rows
+    with the whole matrix's tensor scale), compare y."""
+    Wd = W.cuda()
+    wt = vg.nvfp4_pack(Wd)
+    Wh = W.numpy()
+    gs = orc.amax(Wh) / np.float32(2688.0)
+    assert wt.gscale == np.float32(gs)
+    if rows is None:
+        nib, sc, gs2 = orc.nvfp4_quantise(Wh)
+        assert gs2 == wt.gscale
+        sel = slice(None)
+    else:
+        nib, sc = orc.nvfp4_quantise_gs(Wh[rows], wt.gscale)
+        sel = rows
+    nib_g, sc_g = vg.nvfp4_unpack(wt)
+    assert np.array_equal(nib_g.cpu().numpy()[sel], nib)
+    assert np.array_equal(sc_g.cpu().numpy()[sel], sc)
+    ws = vg.workspace_for(wt)
+    for N in Ns:
+        x = rand_x(seed + N, N, W.shape[1], outliers)
+        y = vg.gemv(wt, x.cuda(), workspace=ws)
+        yref, a = orc.gemv_nvfp4(nib, sc, wt.gscale, bits(x), threads=THREADS)
+        assert_close(orc, y[:, sel] if rows is not None else y, yref, a, f"N={N}")
+
+
+def test_full_projection_5120_outliers(vg, orc):
+    from verify_gemm_gb300.inputs import draw_workload
+
+    Ws, xs = draw_workload("proj", 1)
+    wt = vg.nvfp4_pack(Ws[0].cuda())
+    nib, sc, gs = orc.nvfp4_quantise(Ws[0].numpy())
+    assert gs == wt.gscale
+    x = xs[5120]
+    y = vg.gemv(wt, x.cuda())
+    yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
+    assert_close(orc, y, yref, a, "proj")
+
+
+def test_full_gate_up_fused(vg, orc):
+    """34816x5120 as two 17408x5120 halves with their own tensor scales,
+    run as one fused group, N in {1, 2, 4, 8}."""
+    from verify_gemm_gb300.inputs import draw_workload
+
+    for N in (1, 2, 4, 8):
+        Ws, xs = draw_workload("gateup", N)
+        x = xs[5120].cuda()
+        wts = [vg.nvfp4_pack(W.cuda()) for W in Ws]
+        ys = [torch.empty(N, 17408, dtype=torch.bfloat16, device="cuda") for _ in wts]
+        plan = vg.VerifyPlan([(wt, x, y, 0) for wt, y in zip(wts, ys)], N)
+        plan.run()
+        assert plan.check() == 0
+        for W, wt, y in zip(Ws, wts, ys):
+            nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+            assert gs == wt.gscale
+            yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(xs[5120]), threads=THREADS)
+            assert_close(orc, y, yref, a, f"gate/up N={N}")
+        plan.close()
+
+
+def test_full_down_fp8_and_head(vg, orc):
+    from verify_gemm_gb300.inputs import draw_workload
+
+    Ws, xs = draw_workload("down_head", 8)
+    down, head = Ws
+    wt = vg.fp8_pack(down.cuda())
+    q, rs = orc.fp8_quantise(down.numpy())
+    assert np.array_equal(wt.rowscale.cpu().numpy(), rs)
+    for N in (1, 8):
+        x = xs[17408][:N]
+        y = vg.gemv(wt, x.cuda())
+        yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
+        assert_close(orc, y, yref, a, f"down N={N}")
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(151936 - 64, 151936),
+                                     rng.integers(0, 151936, 768)]))
+    _full_nvfp4(vg, orc, head, (1, 8), seed=3, rows=rows)
+
+
+# ------------------------------------------------------------- verify pass
+
+def _small_stack(vg, N, ordered, layers=2, down_fmt="fp8"):
+    from verify_gemm_gb300.workloads import build_stack
+
+    return build_stack(N, layers=layers, hidden=256, inter=704, vocab=1000, down_fmt=down_fmt,
+                       seed=9)
+
+
+@pytest.mark.parametrize("ordered", [True, False])
+@pytest.mark.parametrize("N", [1, 8])
+def test_verify_pass_small_stack(vg, orc, N, ordered):
+    from verify_gemm_gb300.inputs import draw_stack_matrix
+
+    st = _small_stack(vg, N, ordered)
+    plan = st.plan(ordered=ordered)
+    for _ in range(2):                      # counters are left clean for a repeat
+        st.y_all.zero_()
+        plan.run()
+        assert plan.check() == 0
+        for m, wt, x, y in zip(st.mats, st.weights, st.xs, st.ys):
+            W, _ = draw_stack_matrix(m, N, 9, "cuda")
+            Wh = W.cpu().numpy()
+            if m.fmt == "nvfp4":
+                nib, sc, gs = orc.nvfp4_quantise(Wh)
+                assert gs == wt.gscale
+                yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
+            else:
+                q, rs = orc.fp8_quantise(Wh)
+                yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
+            assert_close(orc, y, yref, a, m.name)
+    plan.close()
+
+
+def test_verify_pass_ordered_and_unordered_agree(vg):
+    st = _small_stack(vg, 4, True, layers=3)
+    outs = []
+    for ordered in (True, False):
+        st.y_all.zero_()
+        plan = st.plan(ordered=ordered, max_ctas=40)
+        plan.run()
+        assert plan.check() == 0
+        outs.append(st.y_all.clone())
+        plan.close()
+    # the two modes split K between blocks at different points, so their FP32
+    # sums may round differently: they agree within the tolerance scale
+    assert torch.allclose(outs[0].float(), outs[1].float(), rtol=2e-2, atol=1e-2)
+
+
+def test_verify_pass_wait_timeout_reports_error(vg):
+    """A group whose completion is never signalled makes the next group's
+    bounded wait run out: the pass returns, the plan reports a timeout, and
+    after the reset the same plan runs clean."""
+    st = _small_stack(vg, 2, True)
+    plan = st.plan(ordered=True, wait_timeout_ns=2_000_000, hold_group=0)
+    plan.run()
+    torch.cuda.synchronize()
+    err = plan.check()
+    assert err == 3
+    plan.close()
+    plan = st.plan(ordered=True)
+    plan.run()
+    assert plan.check() == 0
+    plan.close()
+
+
+def test_full_stack_sampled(vg, orc):
+    """The 64-layer stack + head in the launch configuration the benchmark
+    times (ordered, N = 8): sampled matrices checked row-sampled."""
+    from verify_gemm_gb300.inputs import draw_stack_matrix
+    from verify_gemm_gb300.workloads import build_stack
+
+    N = 8
+    st = build_stack(N)
+    plan = st.plan(ordered=True)
+    plan.run()
+    assert plan.check() == 0
+    rng = np.random.default_rng(1)
+    picks = [0, 3, 4, 6, len(st.mats) // 2 + 2, len(st.mats) - 2, len(st.mats) - 1]
+    for i in picks:
+        m, wt, x, y = st.mats[i], st.weights[i], st.xs[i], st.ys[i]
+        W, _ = draw_stack_matrix(m, N, 4, "cuda")
+        rows = np.unique(np.concatenate([[0, m.M - 1], rng.integers(0, m.M, 256)]))
+        Wh = W.cpu().numpy()
+        if m.fmt == "nvfp4":
+            assert wt.gscale == np.float32(orc.amax(Wh)) / np.float32(2688.0)
+            nib, sc = orc.nvfp4_quantise_gs(Wh[rows], wt.gscale)
+            yref, a = orc.gemv_nvfp4(nib, sc, wt.gscale, bits(x), threads=THREADS)
+        else:
+            q, rs = orc.fp8_quantise(Wh[rows])
+            yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
+        assert_close(orc, y[:, rows], yref, a, m.name)
+    plan.close()

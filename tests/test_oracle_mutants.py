@@ -31,7 +31,7 @@ MUTANTS = {
     "abs sum not absolute": ("sa += fabs(p);", "sa += p;"),
     "e2m1 tie rule": ("if (a <= 0.25f)", "if (a < 0.25f)"),
     "e4m3 rounding half-up": ("nearbyint(a / quantum)", "floor(a / quantum + 0.5)"),
-    "tensor scale constant": ("amax / 2688.0f", "amax / 2680.0f"),
+    "tensor scale constant": ("/ 2688.0f;", "/ 2680.0f;"),
     "block scale divisor": ("float s = t / 6.0f;", "float s = t / 4.0f;"),
     "fp8 row scale divisor": ("rs = ramax / 448.0f;", "rs = ramax / 447.0f;"),
     "fp8 scale dropped in gemv": ("* (double)j->rs[m];", ";"),

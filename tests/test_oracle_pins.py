@@ -430,3 +430,12 @@ def test_check_counts_out_of_tolerance(orc):
         np.uint16)[0]
     bad, worst = orc.check(off, yref, a)          # 4.5 > 4e-3*1000 + 1e-6
     assert bad == 1 and worst > 1.0
+
+
+def test_quantise_rows_with_given_gs_matches_whole_matrix(orc):
+    W = _rand_w(70, 40, 96)
+    nib, sc, gs = orc.nvfp4_quantise(W)
+    assert orc.amax(W) == np.abs(W).max()
+    rows = [0, 17, 39]
+    nr, sr = orc.nvfp4_quantise_gs(W[rows], gs)
+    assert np.array_equal(nr, nib[rows]) and np.array_equal(sr, sc[rows])

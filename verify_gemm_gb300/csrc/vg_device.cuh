@@ -1,0 +1,240 @@
+// vg_device.cuh -- device-side building blocks shared by the pack and GEMV
+// kernels: packed-layout constants, inline PTX for mbarriers, bulk copies,
+// BF16 tensor-core MMA and BF16x2 multiplies, and the in-register decode of
+// the packed NVFP4 / FP8 codes.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vg {
+
+// ---------------------------------------------------------------- layout
+// A row tile is 16 rows (the M of one m16n8k16 MMA).  A unit is 64 columns
+// of one row tile: 32 lanes x 16 bytes of NVFP4 codes (512 B) or 32 lanes x
+// 32 bytes of FP8 codes (1024 B).  Lane l = 4*g + t holds rows g and g+8 of
+// the tile at columns 64u + 16t .. 64u + 16t + 15, i.e. exactly one NVFP4
+// scale block of each of its two rows.
+constexpr int kTileRows = 16;
+constexpr int kUnitK = 64;
+constexpr int kNvUnitBytes = 512;
+constexpr int kF8UnitBytes = 1024;
+// NVFP4 block scales: per tile, per chunk of 4 units (256 columns), 32 lanes
+// x 8 bytes: [unit 0..3][row g, row g+8].
+constexpr int kNvChunkUnits = 4;
+constexpr int kNvScaleChunkBytes = 256;
+constexpr int kF8ChunkUnits = 2;
+
+// A row block is 16 row tiles (256 rows); one pipeline stage holds one
+// chunk of every tile of a row block.
+constexpr int kBlockTiles = 16;
+constexpr int kConsumerWarps = 8;            // 2 row tiles per warp
+constexpr int kTilesPerWarp = kBlockTiles / kConsumerWarps;
+constexpr int kStageNvCodeBytes = kBlockTiles * kNvChunkUnits * kNvUnitBytes;   // 32768
+constexpr int kStageBytes = kStageNvCodeBytes + kBlockTiles * kNvScaleChunkBytes;  // 36864
+constexpr int kStages = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
+
+static_assert(kF8ChunkUnits * kF8UnitBytes == kNvChunkUnits * kNvUnitBytes,
+              "an FP8 chunk fills the NVFP4 code slot of a tile");
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------ decode constants
+// NVFP4 code bit positions inside a packed 32-bit word.  A word holds the 8
+// codes of one MMA (k16 step) for one lane: four BF16x2 A-fragment
+// registers R0..R3 (rows g, g+8, g, g+8 x column pairs (0,1), (0,1), (2,3),
+// (2,3)); the low half of each register is the first column of its pair.
+// Target BF16 bits of a code (m, e0, e1, s) are 6, 7, 8, 15: the value of
+// those bits alone is e2m1 * 2^-126 (exponent 0 covers the 0.5 code as a
+// BF16 subnormal).  R0 sits at the target bits, R1 three bits lower, R2 six
+// bits lower; R3 fills the rest (m 13, e0 14, e1 10, s 11) and is moved by
+// one multiply that adds shifted copies without carries.
+constexpr uint32_t kNvMask = 0x81C081C0u;
+constexpr uint32_t kNvR3Pick = 0x00D800D8u;  // bits 3,4,6,7 (+16) after >> 7
+constexpr uint32_t kNvR3Spread = 0x821u;     // x1 (m, e0), x32 (e1), x2048 (s)
+// Bit position (low half) of code bit b in {m, e0, e1, s} for register r.
+__host__ __device__ constexpr int nv_bitpos(int r, int b) {
+  return r == 0 ? (b == 3 ? 15 : 6 + b)
+       : r == 1 ? (b == 3 ? 12 : 3 + b)
+       : r == 2 ? (b == 3 ? 9 : 0 + b)
+       : (b == 0 ? 13 : b == 1 ? 14 : b == 2 ? 10 : 11);
+}
+
+// Packed scale code: an 8-bit float with 5 exponent bits and 3 mantissa
+// bits whose exponent is the E4M3 exponent + 3, so E4M3 subnormal scales
+// become normal numbers.  BF16 bits of (code << 4) + kScaleBias decode to
+// scale * 2^118; multiplied by the code bits above (e2m1 * 2^-126) this
+// gives e2m1 * scale * 2^-8 exactly.  The epilogue multiplies by 2^8 * gs.
+constexpr uint32_t kScaleBias = 235u << 7;   // 0x7580 per half
+constexpr uint32_t kScaleBias2 = (kScaleBias << 16) | kScaleBias;
+constexpr float kNvEpilogueScale = 256.0f;
+// FP8 codes placed into BF16 bits ((b & 0x7f) << 4 | sign << 15) are worth
+// e4m3 * 2^-120; one multiply by 2^120 (BF16 0x7B80) restores them.
+constexpr uint32_t kF8Restore2 = 0x7B807B80u;
+
+// E4M3 byte (0x00..0x7E) -> packed scale code, and back.
+__host__ __device__ inline uint32_t scale_code_from_e4m3(uint32_t b) {
+  const uint32_t e = b >> 3, f = b & 7;
+  if (e != 0) return b + 24;
+  // subnormal f * 2^-9 as exponent-5 codes: f=1..7 -> (1,0) (2,0) (2,4) (3,0) (3,2) (3,4) (3,6)
+  constexpr uint8_t sub[8] = {0, 8, 16, 20, 24, 26, 28, 30};
+  return sub[f];
+}
+__host__ __device__ inline uint32_t e4m3_from_scale_code(uint32_t d) {
+  if (d >= 32) return d - 24;
+  switch (d) {
+    case 8: return 1;
+    case 16: return 2;
+    case 20: return 3;
+    case 24: return 4;
+    case 26: return 5;
+    case 28: return 6;
+    case 30: return 7;
+    default: return 0;
+  }
+}
+
+#ifdef __CUDACC__
+// ------------------------------------------------------------ small PTX
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase with `parity` completed, false when
+// `deadline` (globaltimer ns) passed first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline) {
+  if (mbar_try_wait(bar, parity)) return true;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() > deadline) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (tx bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Read-only 16-byte global load through L1 (x is reused by every warp).
+__device__ __forceinline__ uint4 ldg128(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ----------------------------------------------------- in-register decode
+// Four BF16x2 A-fragment registers of one NVFP4 word, each multiplied by
+// the packed scale of its row (fg for rows g, fg8 for rows g+8).
+__device__ __forceinline__ void nv_decode(uint32_t w, uint32_t fg, uint32_t fg8, uint32_t &a0,
+                                          uint32_t &a1, uint32_t &a2, uint32_t &a3) {
+  const uint32_t r0 = w & kNvMask;
+  const uint32_t r1 = (w << 3) & kNvMask;
+  const uint32_t r2 = (w << 6) & kNvMask;
+  const uint32_t r3 = (((w >> 7) & kNvR3Pick) * kNvR3Spread) & kNvMask;
+  a0 = bmul2(r0, fg);
+  a1 = bmul2(r1, fg8);
+  a2 = bmul2(r2, fg);
+  a3 = bmul2(r3, fg8);
+}
+
+// BF16x2 {F, F} of the packed scale byte number `byte` (0..3) of `word`.
+__device__ __forceinline__ uint32_t nv_scale_pair(uint32_t word, uint32_t byte) {
+  const uint32_t dup = prmt(word, 0u, 0x4040u | (byte * 0x0101u));
+  return dup * 16u + kScaleBias2;
+}
+
+// Two BF16x2 registers of one FP8 word (bytes 0,2 -> ra; bytes 1,3 -> rb).
+__device__ __forceinline__ void f8_decode(uint32_t w, uint32_t &ra, uint32_t &rb) {
+  const uint32_t pa = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
+  const uint32_t pb = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
+  ra = bmul2(pa, kF8Restore2);
+  rb = bmul2(pb, kF8Restore2);
+}
+#endif  // __CUDACC__
+
+}  // namespace vg

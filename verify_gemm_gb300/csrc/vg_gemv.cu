@@ -1,0 +1,732 @@
+// vg_gemv.cu -- the weight-streaming GEMV for N = 1..8 BF16 columns over
+// NVFP4 or row-scaled FP8 weights, as a single product and as a fused,
+// ordered verify pass over a layer stack.
+//
+// What it computes: y[N,M] = x[N,K] . dequant(W)[M,K]^T with FP32
+// accumulation (mtp7-device-confidence engine card, Design table, "GEMVs"
+// row; the verify pass of the Decode row runs it for 2-8 columns, a draft
+// step for one).  Why it is the hot path: a verify pass reads every weight
+// once (card, Measured section: 19.26 GB per pass, its time set by the read
+// rate), so the kernel is built to stream bytes at HBM speed.
+//
+// Design (sm_103a):
+//  * Persistent thread blocks, one per SM: 8 consumer warps + 1 producer
+//    warp.  The producer streams one pipeline stage per work item with 1-D
+//    bulk copies (cp.async.bulk) into a 4-deep shared-memory ring guarded by
+//    mbarriers; the weights never pass through registers of the producer.
+//  * A work item is one chunk (256 columns NVFP4, 128 FP8) of a row block of
+//    16 tiles (256 rows); each consumer warp owns 2 tiles and decodes its
+//    codes in registers to BF16 A fragments (bit placement + one BF16x2
+//    multiply by the block scale, exact) and runs mma.m16n8k16 with x as the
+//    B fragment (x read through L1, shared by all warps), accumulating FP32.
+//  * Items are split between thread blocks stream-K style (contiguous item
+//    ranges of equal length), so every SM streams the same number of bytes.
+//    A row block whose K range is split between blocks is summed from FP32
+//    partials by the last block to arrive, in block order (deterministic,
+//    no spinning); the counter it used is reset for the next call.
+//  * Verify pass: matrices are grouped; in ordered mode the consumers of
+//    group g wait (bounded) until group g-1 has completed every row block,
+//    while the producer keeps prefetching group g's weights.  All waits are
+//    bounded by a timeout on %globaltimer and report an error word instead
+//    of hanging.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "vg_device.cuh"
+#include "vg_internal.h"
+
+namespace vg {
+
+struct MatDev {
+  const uint8_t *w;
+  const uint8_t *sc;
+  const float *rowscale;
+  const uint16_t *x;
+  uint16_t *y;
+  float mult;        // epilogue multiplier (NVFP4: 256 * gscale)
+  int fmt;
+  int64_t M, K, MT, KU, KC, RB;
+  int64_t item0;     // first item of this matrix within its phase
+  int64_t rb_base;   // first arrival counter of this matrix
+};
+
+struct PhaseDev {
+  int64_t items;
+  int64_t rbs;
+  int mat_begin, mat_end;
+};
+
+struct Params {
+  const MatDev *mats;       // nullptr: use mat0 / phase0
+  const PhaseDev *phases;
+  int nphases;
+  int N;
+  int ordered;
+  int hold_phase;
+  int grid;
+  uint64_t timeout_ns;
+  uint32_t *cnt;
+  uint32_t *done;           // per-phase completed row blocks (ordered only)
+  uint32_t *ctas_done;
+  float *partials;          // [grid][2][16 tiles][32 lanes][4]
+  int *error;
+  MatDev mat0;
+  PhaseDev phase0;
+};
+
+constexpr int kPartialFloats = kBlockTiles * 32 * 4;   // one slot
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStages * 8 + 64;
+constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3;
+
+__host__ __device__ inline int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ inline int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__host__ __device__ inline int64_t item_begin(int64_t T, int64_t G, int64_t b) {
+  return T * b / G;
+}
+// Block that owns item i of a phase of T items split over G blocks.
+__device__ inline int64_t owner(int64_t T, int64_t G, int64_t i) { return ((i + 1) * G - 1) / T; }
+
+__device__ inline void set_error(int *error, int code) { atomicCAS(error, 0, code); }
+
+// Per-CTA walk over the (matrix, row block, chunk) items of one phase.
+struct Cursor {
+  const MatDev *mats;
+  int mi, mend;
+  MatDev m;
+  __device__ void start(const MatDev *all, const PhaseDev &ph) {
+    mats = all;
+    mi = ph.mat_begin;
+    mend = ph.mat_end;
+    m = mats[mi];
+  }
+  __device__ void seek(int64_t item) {
+    while (item >= m.item0 + m.RB * m.KC && mi + 1 < mend) m = mats[++mi];
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+  volatile int *sflag = reinterpret_cast<volatile int *>(bars + 2 * kStages);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t b = blockIdx.x;
+  const MatDev *mats = p.mats ? p.mats : &p.mat0;
+  const PhaseDev *phases = p.mats ? p.phases : &p.phase0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    sflag[0] = 0;
+    sflag[1] = 0;
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ================================================================ producer
+    const uint64_t policy = policy_evict_first();
+    int64_t it = 0;
+    bool aborted = false;
+    for (int ph = 0; ph < p.nphases && !aborted; ++ph) {
+      const PhaseDev P = phases[ph];
+      const int64_t G = i64min(p.grid, P.items);
+      if (b >= G) continue;
+      Cursor cur;
+      cur.start(mats, P);
+      const int64_t i1 = item_begin(P.items, G, b + 1);
+      for (int64_t i = item_begin(P.items, G, b); i < i1; ++i, ++it) {
+        cur.seek(i);
+        const MatDev &m = cur.m;
+        const int s = int(it % kStages);
+        const uint32_t par = uint32_t(it / kStages) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, par ^ 1u, globaltimer() + p.timeout_ns)) {
+          if (lane == 0) set_error(p.error, kErrEmptyWait);
+          aborted = true;
+          break;
+        }
+        const int64_t rel = i - m.item0, rb = rel / m.KC, c = rel % m.KC;
+        const int64_t tiles = i64min(kBlockTiles, m.MT - rb * kBlockTiles);
+        const bool nv = m.fmt == VG_FMT_NVFP4;
+        const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
+        const int64_t nu = i64min(cu, m.KU - c * cu);
+        const uint32_t code_bytes = uint32_t(nu * (nv ? kNvUnitBytes : kF8UnitBytes));
+        const uint32_t bytes = uint32_t(tiles) * (code_bytes + (nv ? kNvScaleChunkBytes : 0));
+        const uint32_t stage = smem_addr(smem + s * kStageBytes);
+        const uint32_t full = full0 + 8 * s;
+        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+        __syncwarp();
+        const int r = lane & 15;
+        if (r < tiles) {
+          const int64_t mt = rb * kBlockTiles + r;
+          if (lane < 16) {
+            const uint8_t *src = m.w + (mt * m.KU + c * cu) * (nv ? kNvUnitBytes : kF8UnitBytes);
+            bulk_g2s(stage + r * (kNvChunkUnits * kNvUnitBytes), src, code_bytes, full, policy);
+          } else if (nv) {
+            const uint8_t *src = m.sc + (mt * m.KC + c) * kNvScaleChunkBytes;
+            bulk_g2s(stage + kStageNvCodeBytes + r * kNvScaleChunkBytes, src,
+                     kNvScaleChunkBytes, full, policy);
+          }
+        }
+      }
+    }
+    // Never leave the block while a bulk copy may still be writing shared
+    // memory: wait (bounded) for the last stages issued.
+    for (int64_t k = i64max(0, it - kStages); k < it; ++k) {
+      const int s = int(k % kStages);
+      mbar_wait(full0 + 8 * s, uint32_t(k / kStages) & 1u, globaltimer() + p.timeout_ns);
+    }
+  } else {
+    // =============================================================== consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int N = p.N;
+    int64_t it = 0;
+    bool aborted = false;
+    float acc[kTilesPerWarp][4];
+    for (int ph = 0; ph < p.nphases; ++ph) {
+      const PhaseDev P = phases[ph];
+      const int64_t G = i64min(p.grid, P.items);
+      if (b >= G) continue;
+      // ordered verify: group ph's products wait for group ph-1
+      if (p.ordered && ph > 0) {
+        if (tid == 0) {
+          int ok = 1;
+          if (!aborted) {
+            const volatile uint32_t *d = p.done + (ph - 1);
+            const uint32_t target = uint32_t(phases[ph - 1].rbs);
+            const uint64_t deadline = globaltimer() + p.timeout_ns;
+            while (*d < target) {
+              if (globaltimer() > deadline) {
+                ok = 0;
+                set_error(p.error, kErrDepWait);
+                break;
+              }
+              __nanosleep(64);
+            }
+            __threadfence();
+          }
+          sflag[0] = ok ? 0 : 1;
+        }
+        named_bar(1, kConsumerWarps * 32);
+        if (sflag[0]) aborted = true;
+        named_bar(1, kConsumerWarps * 32);
+      }
+      Cursor cur;
+      cur.start(mats, P);
+      const int64_t i0 = item_begin(P.items, G, b), i1 = item_begin(P.items, G, b + 1);
+      int64_t piece_start = i0;
+      for (int64_t i = i0; i < i1; ++i, ++it) {
+        cur.seek(i);
+        const MatDev &m = cur.m;
+        const int64_t rel = i - m.item0, rb = rel / m.KC, c = rel % m.KC;
+        if (c == 0 || i == i0) {
+          piece_start = i;
+#pragma unroll
+          for (int q = 0; q < kTilesPerWarp; ++q)
+            acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+        }
+        const int s = int(it % kStages);
+        const uint32_t par = uint32_t(it / kStages) & 1u;
+        if (!aborted && !mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)) {
+          if (lane == 0) set_error(p.error, kErrFullWait);
+          aborted = true;
+        }
+        if (!aborted) {
+          const uint32_t stage = smem_addr(smem + s * kStageBytes);
+          const bool nv = m.fmt == VG_FMT_NVFP4;
+          const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
+          const int nu = int(i64min(cu, m.KU - c * cu));
+          const int64_t tiles = i64min(kBlockTiles, m.MT - rb * kBlockTiles);
+          const int tile0 = warp * kTilesPerWarp;
+          uint2 scw[kTilesPerWarp];
+          if (nv) {
+#pragma unroll
+            for (int q = 0; q < kTilesPerWarp; ++q)
+              scw[q] = lds64(stage + kStageNvCodeBytes + (tile0 + q) * kNvScaleChunkBytes + lane * 8);
+          }
+          const uint16_t *xrow = m.x + int64_t(g) * m.K;
+          for (int uu = 0; uu < nu; ++uu) {
+            const int64_t kg = (c * cu + uu) * kUnitK + 16 * t;
+            uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+            if (g < N && kg < m.K) {
+              xa = ldg128(xrow + kg);
+              xb = ldg128(xrow + kg + 8);
+            }
+            const uint32_t bx[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int q = 0; q < kTilesPerWarp; ++q) {
+              if (tile0 + q >= tiles) continue;
+              const uint32_t base = stage + (tile0 + q) * (kNvChunkUnits * kNvUnitBytes);
+              if (nv) {
+                const uint4 wv = lds128(base + uu * kNvUnitBytes + lane * 16);
+                const uint32_t sw = uu < 2 ? scw[q].x : scw[q].y;
+                const uint32_t sb = uint32_t(uu & 1) * 2u;
+                const uint32_t fg = nv_scale_pair(sw, sb), fg8 = nv_scale_pair(sw, sb + 1);
+                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t a0, a1, a2, a3;
+                  nv_decode(wd[j], fg, fg8, a0, a1, a2, a3);
+                  mma_bf16(acc[q], a0, a1, a2, a3, bx[2 * j], bx[2 * j + 1]);
+                }
+              } else {
+                const uint4 w0 = lds128(base + uu * kF8UnitBytes + lane * 32);
+                const uint4 w1 = lds128(base + uu * kF8UnitBytes + lane * 32 + 16);
+                const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t a0, a1, a2, a3;
+                  f8_decode(wd[2 * j], a0, a1);
+                  f8_decode(wd[2 * j + 1], a2, a3);
+                  mma_bf16(acc[q], a0, a1, a2, a3, bx[2 * j], bx[2 * j + 1]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+
+        // ------------------------------------------- end of a row-block piece
+        if (c != m.KC - 1 && i != i1 - 1) continue;
+        const bool full_piece = (piece_start - m.item0) % m.KC == 0 && c == m.KC - 1;
+        const int64_t mt0 = rb * kBlockTiles + warp * kTilesPerWarp;
+        bool write_out = true;
+        if (!full_piece) {
+          // partial sums: stash, count arrivals, the last arrival reduces
+          const int slot = int(2 * b + (piece_start == i0 ? 0 : 1));
+          float *part = p.partials + int64_t(slot) * kPartialFloats;
+          if (!aborted) {
+#pragma unroll
+            for (int q = 0; q < kTilesPerWarp; ++q)
+              *reinterpret_cast<float4 *>(part + ((warp * kTilesPerWarp + q) * 32 + lane) * 4) =
+                  make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+            __threadfence();
+          }
+          named_bar(1, kConsumerWarps * 32);
+          const int64_t first = m.item0 + rb * m.KC, last = first + m.KC - 1;
+          const int64_t bf = owner(P.items, G, first), bl = owner(P.items, G, last);
+          if (tid == 0) {
+            int is_last = 0;
+            if (!aborted) {
+              uint32_t *cnt = p.cnt + m.rb_base + rb;
+              const uint32_t old = atomicAdd(cnt, 1u);
+              is_last = old == uint32_t(bl - bf);
+              if (is_last) *cnt = 0u;
+            }
+            sflag[1] = is_last;
+          }
+          named_bar(1, kConsumerWarps * 32);
+          write_out = sflag[1] != 0;
+          named_bar(1, kConsumerWarps * 32);
+          if (write_out) {
+            __threadfence();
+#pragma unroll
+            for (int q = 0; q < kTilesPerWarp; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+            for (int64_t bb = bf; bb <= bl; ++bb) {
+              const int64_t sslot = 2 * bb + (item_begin(P.items, G, bb) >= first ? 0 : 1);
+              const float *src = p.partials + sslot * kPartialFloats;
+#pragma unroll
+              for (int q = 0; q < kTilesPerWarp; ++q) {
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4 *>(src + ((warp * kTilesPerWarp + q) * 32 + lane) * 4));
+                acc[q][0] += v.x;
+                acc[q][1] += v.y;
+                acc[q][2] += v.z;
+                acc[q][3] += v.w;
+              }
+            }
+          }
+        }
+        if (write_out) {
+          if (!aborted) {
+#pragma unroll
+            for (int q = 0; q < kTilesPerWarp; ++q) {
+              const int64_t mt = mt0 + q;
+              if (mt >= m.MT) continue;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int64_t row = mt * kTileRows + g + 8 * h;
+                if (row >= m.M) continue;
+                const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int n = 2 * t + e;
+                  if (n < N) {
+                    const __nv_bfloat16 v = __float2bfloat16_rn(acc[q][2 * h + e] * mult);
+                    m.y[int64_t(n) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
+                  }
+                }
+              }
+            }
+          }
+          if (p.done) {
+            __threadfence();
+            named_bar(1, kConsumerWarps * 32);
+            if (tid == 0 && !aborted && ph != p.hold_phase) atomicAdd(p.done + ph, 1u);
+          }
+        }
+      }
+    }
+  }
+
+  // The last block out resets the per-phase completion counters.
+  __syncthreads();
+  if (p.done && tid == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(p.ctas_done, 1u);
+    if (old == uint32_t(p.grid - 1)) {
+      for (int ph = 0; ph < p.nphases; ++ph) p.done[ph] = 0u;
+      *p.ctas_done = 0u;
+      __threadfence();
+    }
+  }
+}
+
+// ================================================================ host side
+
+namespace {
+
+struct DeviceInfo {
+  int sms = 0;
+  int cc = 0;
+  bool attr_set = false;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+vg_status device_info(int *dev_out, DeviceInfo **info) {
+  int dev = 0;
+  VG_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return VG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.attr_set) {
+    int major = 0, minor = 0;
+    VG_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    VG_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    VG_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    d.cc = major * 10 + minor;
+    if (d.cc != 103) return VG_ERR_UNSUPPORTED;
+    VG_CUDA(cudaFuncSetAttribute(stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes));
+    d.attr_set = true;
+  }
+  *dev_out = dev;
+  *info = &d;
+  return VG_OK;
+}
+
+MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, const float *rs,
+                float gscale, const uint16_t *x, uint16_t *y) {
+  MatDev m;
+  std::memset(&m, 0, sizeof m);
+  m.w = static_cast<const uint8_t *>(w);
+  m.sc = static_cast<const uint8_t *>(sc);
+  m.rowscale = rs;
+  m.x = x;
+  m.y = y;
+  m.fmt = fmt;
+  m.mult = fmt == VG_FMT_NVFP4 ? kNvEpilogueScale * gscale : 1.0f;
+  m.M = M;
+  m.K = K;
+  m.MT = ceil_div(M, kTileRows);
+  m.KU = ceil_div(K, kUnitK);
+  m.KC = ceil_div(m.KU, fmt == VG_FMT_NVFP4 ? kNvChunkUnits : kF8ChunkUnits);
+  m.RB = ceil_div(m.MT, kBlockTiles);
+  return m;
+}
+
+int64_t algorithmic_bytes(const MatDev &m) {
+  return m.fmt == VG_FMT_NVFP4 ? m.M * m.K / 2 + m.M * m.K / 16 + 4 : m.M * m.K + 4 * m.M;
+}
+
+// Single-GEMV workspace: [error word | counters | partial slots].
+constexpr size_t kWsHead = 256;
+size_t ws_counters_bytes(int64_t RB) { return size_t((RB * 4 + 255) / 256 * 256); }
+size_t ws_bytes(int64_t RB, int grid) {
+  return kWsHead + ws_counters_bytes(RB) + size_t(grid) * 2 * kPartialFloats * sizeof(float);
+}
+
+vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace_bytes,
+                      vg_stream_t stream) {
+  int dev;
+  DeviceInfo *di;
+  if (vg_status s = device_info(&dev, &di)) return s;
+  const int64_t T = m0.RB * m0.KC;
+  const int grid = int(i64min(di->sms, T));
+  if (!workspace || workspace_bytes < ws_bytes(m0.RB, grid)) return VG_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return VG_ERR_ALIGNMENT;
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  p.nphases = 1;
+  p.N = N;
+  p.ordered = 0;
+  p.hold_phase = -1;
+  p.grid = grid;
+  p.timeout_ns = 2000000000ull;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  p.error = reinterpret_cast<int *>(ws);
+  p.cnt = reinterpret_cast<uint32_t *>(ws + kWsHead);
+  p.partials = reinterpret_cast<float *>(ws + kWsHead + ws_counters_bytes(m0.RB));
+  p.mat0 = m0;
+  p.phase0.items = T;
+  p.phase0.rbs = m0.RB;
+  p.phase0.mat_begin = 0;
+  p.phase0.mat_end = 1;
+  stream_kernel<<<grid, kThreads, kSmemBytes, as_cuda(stream)>>>(p);
+  VG_LAUNCH_CHECK();
+  return VG_OK;
+}
+
+}  // namespace
+}  // namespace vg
+
+using namespace vg;
+
+struct vg_verify_plan {
+  int dev = 0;
+  int N = 0;
+  int grid = 0;
+  int ordered = 1;
+  int nphases = 0;
+  int64_t bytes = 0;
+  Params params;
+  MatDev *d_mats = nullptr;
+  PhaseDev *d_phases = nullptr;
+  uint8_t *d_state = nullptr;     // error, counters, partials
+  size_t state_bytes = 0;
+};
+
+extern "C" vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes) {
+  if (vg_status s = check_mk(M, K)) return s;
+  if (!bytes || (format != VG_FMT_NVFP4 && format != VG_FMT_FP8_ROWSCALE)) return VG_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo *di;
+  if (vg_status s = device_info(&dev, &di)) return s;
+  const MatDev m = make_mat(format, M, K, nullptr, nullptr, nullptr, 0.f, nullptr, nullptr);
+  const int grid = int(i64min(di->sms, m.RB * m.KC));
+  *bytes = ws_bytes(m.RB, grid);
+  return VG_OK;
+}
+
+static vg_status check_gemv_args(const void *w, const void *x, const void *y, int N, int64_t M,
+                                 int64_t K) {
+  if (vg_status s = check_mk(M, K)) return s;
+  if (N < 1 || N > 8 || !w || !x || !y) return VG_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(x) || !aligned16(y)) return VG_ERR_ALIGNMENT;
+  return VG_OK;
+}
+
+extern "C" vg_status vg_gemv_nvfp4(const void *w, const void *scales, float gscale,
+                                   const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
+                                   void *workspace, size_t workspace_bytes, vg_stream_t stream) {
+  if (vg_status s = check_gemv_args(w, x, y, N, M, K)) return s;
+  if (!scales) return VG_ERR_INVALID_ARG;
+  if (!aligned16(scales)) return VG_ERR_ALIGNMENT;
+  const MatDev m = make_mat(VG_FMT_NVFP4, M, K, w, scales, nullptr, gscale, x, y);
+  return gemv_common(m, N, workspace, workspace_bytes, stream);
+}
+
+extern "C" vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale, const uint16_t *x,
+                                          int N, int64_t M, int64_t K, uint16_t *y,
+                                          void *workspace, size_t workspace_bytes,
+                                          vg_stream_t stream) {
+  if (vg_status s = check_gemv_args(w, x, y, N, M, K)) return s;
+  if (!rowscale) return VG_ERR_INVALID_ARG;
+  const MatDev m = make_mat(VG_FMT_FP8_ROWSCALE, M, K, w, nullptr, rowscale, 0.f, x, y);
+  return gemv_common(m, N, workspace, workspace_bytes, stream);
+}
+
+extern "C" vg_status vg_gemv_workspace_check(void *workspace, size_t workspace_bytes,
+                                             int *device_error, vg_stream_t stream) {
+  if (!workspace || !device_error || workspace_bytes < kWsHead) return VG_ERR_INVALID_ARG;
+  cudaStream_t st = as_cuda(stream);
+  int err = 0;
+  VG_CUDA(cudaMemcpyAsync(&err, workspace, sizeof err, cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  *device_error = err;
+  if (err) {
+    VG_CUDA(cudaMemsetAsync(workspace, 0, workspace_bytes, st));
+    VG_CUDA(cudaStreamSynchronize(st));
+    return VG_ERR_TIMEOUT;
+  }
+  return VG_OK;
+}
+
+// -------------------------------------------------------------- verify plan
+
+extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,
+                                              const vg_plan_options *opt,
+                                              vg_verify_plan **plan_out) {
+  if (!mats || count < 1 || !plan_out || N < 1 || N > 8) return VG_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  vg_plan_options o;
+  std::memset(&o, 0, sizeof o);
+  o.ordered = 1;
+  o.hold_group = -1;
+  if (opt) o = *opt;
+  int dev;
+  DeviceInfo *di;
+  if (vg_status s = device_info(&dev, &di)) return s;
+  int coop = 0;
+  VG_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+  if (!coop) return VG_ERR_UNSUPPORTED;
+
+  std::vector<MatDev> hm(static_cast<size_t>(count));
+  std::vector<PhaseDev> hp;
+  int64_t rb_total = 0, bytes = 0;
+  int hold_phase = -1;
+  for (int i = 0; i < count; ++i) {
+    const vg_matrix_desc &d = mats[i];
+    if (vg_status s = check_gemv_args(d.w, d.x, d.y, N, d.M, d.K)) return s;
+    if (i > 0 && d.group < mats[i - 1].group) return VG_ERR_INVALID_ARG;
+    if (d.format == VG_FMT_NVFP4) {
+      if (!d.scales) return VG_ERR_INVALID_ARG;
+      if (!aligned16(d.scales)) return VG_ERR_ALIGNMENT;
+    } else if (d.format == VG_FMT_FP8_ROWSCALE) {
+      if (!d.rowscale) return VG_ERR_INVALID_ARG;
+    } else {
+      return VG_ERR_INVALID_ARG;
+    }
+    hm[i] = make_mat(d.format, d.M, d.K, d.w, d.scales, d.rowscale, d.gscale, d.x, d.y);
+    const bool new_phase = hp.empty() || (o.ordered && d.group != mats[i - 1].group);
+    if (new_phase) {
+      PhaseDev ph;
+      ph.items = 0;
+      ph.rbs = 0;
+      ph.mat_begin = i;
+      ph.mat_end = i;
+      hp.push_back(ph);
+      if (o.ordered && d.group == o.hold_group) hold_phase = int(hp.size()) - 1;
+    }
+    PhaseDev &ph = hp.back();
+    hm[i].item0 = ph.items;
+    hm[i].rb_base = rb_total;
+    ph.items += hm[i].RB * hm[i].KC;
+    ph.rbs += hm[i].RB;
+    ph.mat_end = i + 1;
+    rb_total += hm[i].RB;
+    bytes += algorithmic_bytes(hm[i]);
+  }
+  int grid = di->sms;
+  if (o.max_ctas > 0) grid = std::min(grid, int(o.max_ctas));
+  int per_sm = 0;
+  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel, kThreads, kSmemBytes));
+  if (per_sm < 1) return VG_ERR_UNSUPPORTED;
+  grid = std::min(grid, per_sm * di->sms);
+
+  vg_verify_plan *plan = new vg_verify_plan();
+  plan->dev = dev;
+  plan->N = N;
+  plan->grid = grid;
+  plan->ordered = o.ordered ? 1 : 0;
+  plan->nphases = int(hp.size());
+  plan->bytes = bytes;
+  const size_t head = 256;
+  const size_t cnt_bytes = size_t((rb_total * 4 + 255) / 256 * 256);
+  const size_t done_bytes = size_t((hp.size() * 4 + 4 + 255) / 256 * 256);
+  const size_t part_bytes = size_t(grid) * 2 * kPartialFloats * sizeof(float);
+  plan->state_bytes = head + cnt_bytes + done_bytes + part_bytes;
+  cudaError_t e = cudaMalloc(&plan->d_mats, sizeof(MatDev) * hm.size());
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_phases, sizeof(PhaseDev) * hp.size());
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_state, plan->state_bytes);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(plan->d_mats, hm.data(), sizeof(MatDev) * hm.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(plan->d_phases, hp.data(), sizeof(PhaseDev) * hp.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(plan->d_state, 0, plan->state_bytes);
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    vg_verify_plan_destroy(plan);
+    return VG_ERR_CUDA;
+  }
+  Params &p = plan->params;
+  std::memset(&p, 0, sizeof p);
+  p.mats = plan->d_mats;
+  p.phases = plan->d_phases;
+  p.nphases = plan->nphases;
+  p.N = N;
+  p.ordered = plan->ordered;
+  p.hold_phase = hold_phase;
+  p.grid = grid;
+  p.timeout_ns = o.wait_timeout_ns > 0 ? uint64_t(o.wait_timeout_ns) : 2000000000ull;
+  p.error = reinterpret_cast<int *>(plan->d_state);
+  p.cnt = reinterpret_cast<uint32_t *>(plan->d_state + head);
+  p.done = reinterpret_cast<uint32_t *>(plan->d_state + head + cnt_bytes);
+  p.ctas_done = p.done + hp.size();
+  p.partials = reinterpret_cast<float *>(plan->d_state + head + cnt_bytes + done_bytes);
+  if (!plan->ordered) {
+    p.done = nullptr;
+    p.ctas_done = nullptr;
+  }
+  *plan_out = plan;
+  return VG_OK;
+}
+
+extern "C" vg_status vg_verify_plan_create(const vg_matrix_desc *mats, int count, int N,
+                                           int ordered, vg_verify_plan **plan_out) {
+  vg_plan_options o;
+  std::memset(&o, 0, sizeof o);
+  o.ordered = ordered;
+  o.hold_group = -1;
+  return vg_verify_plan_create_ex(mats, count, N, &o, plan_out);
+}
+
+extern "C" vg_status vg_verify_pass(vg_verify_plan *plan, vg_stream_t stream) {
+  if (!plan) return VG_ERR_INVALID_ARG;
+  int dev = 0;
+  VG_CUDA(cudaGetDevice(&dev));
+  if (dev != plan->dev) return VG_ERR_INVALID_ARG;
+  void *args[] = {&plan->params};
+  VG_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(stream_kernel),
+                                      dim3(plan->grid), dim3(kThreads), args, kSmemBytes,
+                                      as_cuda(stream)));
+  return VG_OK;
+}
+
+extern "C" vg_status vg_verify_plan_check(vg_verify_plan *plan, vg_stream_t stream,
+                                          int *device_error) {
+  if (!plan || !device_error) return VG_ERR_INVALID_ARG;
+  cudaStream_t st = as_cuda(stream);
+  int err = 0;
+  VG_CUDA(cudaMemcpyAsync(&err, plan->d_state, sizeof err, cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  *device_error = err;
+  if (err) {
+    VG_CUDA(cudaMemsetAsync(plan->d_state, 0, plan->state_bytes, st));
+    VG_CUDA(cudaStreamSynchronize(st));
+    return VG_ERR_TIMEOUT;
+  }
+  return VG_OK;
+}
+
+extern "C" vg_status vg_verify_plan_bytes(const vg_verify_plan *plan, int64_t *bytes) {
+  if (!plan || !bytes) return VG_ERR_INVALID_ARG;
+  *bytes = plan->bytes;
+  return VG_OK;
+}
+
+extern "C" vg_status vg_verify_plan_grid(const vg_verify_plan *plan, int *ctas) {
+  if (!plan || !ctas) return VG_ERR_INVALID_ARG;
+  *ctas = plan->grid;
+  return VG_OK;
+}
+
+extern "C" vg_status vg_verify_plan_destroy(vg_verify_plan *plan) {
+  if (!plan) return VG_OK;
+  cudaFree(plan->d_mats);
+  cudaFree(plan->d_phases);
+  cudaFree(plan->d_state);
+  delete plan;
+  return VG_OK;
+}
