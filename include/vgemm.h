@@ -159,8 +159,9 @@ vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t K, void *w_
  * holds per-row-block arrival counters, a device error word and the FP32
  * partial sums of row blocks whose K range is split between two or more
  * thread blocks.  It must be zero-filled once when allocated; every call
- * leaves it zero-filled again.  Calls that share a workspace must not
- * overlap on the GPU. */
+ * leaves the counters and the error word at zero again (the partial-sum
+ * space may keep stale values, which are never read before being
+ * rewritten).  Calls that share a workspace must not overlap on the GPU. */
 vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes);
 
 /* y[n][m] = bf16( sum_k x[n][k] * dequant(W)[m][k] ), NVFP4 weights.
