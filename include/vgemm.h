@@ -183,6 +183,30 @@ vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale,
                                const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
                                void *workspace, size_t workspace_bytes, vg_stream_t stream);
 
+/* Largest workspace, in bytes, that vg_gemv_nvfp4_noalloc can serve. */
+#define VG_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/* vg_gemv_nvfp4 without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: code inside a host application that owns all
+ * device memory and only lends out input and output buffers, code that must
+ * not call cudaMalloc because it may synchronise the whole device, or code
+ * held to a fixed memory budget.  The pages have no counterpart to this
+ * entry point; it exists for such callers only.
+ *   Arguments, results and errors are those of vg_gemv_nvfp4, minus the
+ *   workspace.  The workspace is one fixed device array of
+ *   VG_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, which every GPU
+ *   that loads the library holds until the process exits.  A matrix that
+ *   needs more (vg_gemv_workspace_size) gives VG_ERR_UNSUPPORTED.
+ *   Nothing is allocated: the call clears the part of the array it uses with
+ *   cudaMemsetAsync on `stream`, then runs the GEMV on it.  The first call
+ *   on a device looks up the array's device address (cudaGetSymbolAddress);
+ *   make that first call before any stream capture.  All calls share the
+ *   one array, so calls that overlap on the GPU (other streams, other host
+ *   threads) race and give wrong results: serialise them. */
+vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, float gscale,
+                                const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
+                                vg_stream_t stream);
+
 /* Reads and clears the device error word of a GEMV workspace (synchronous).
  * *device_error receives 0, or a nonzero code if a bounded wait inside a
  * kernel ran out (then the workspace is also re-zeroed). */

@@ -1,0 +1,66 @@
+"""vg_gemv_nvfp4_noalloc: the NVFP4 GEMV for callers that cannot allocate
+device memory (a host application that owns all device memory and lends out
+only the input and output buffers, code that must not call cudaMalloc
+because it can synchronise the device, code under a fixed memory budget).
+It runs the same GEMV on a fixed scratch array inside the library.
+
+This file is collected last on purpose.  It calls the entry point through
+the C ABI twice in a row (the shared array keeps the first call's contents)
+and checks each result against the workspace entry point, vg_gemv_nvfp4,
+and against the CPU oracle, within the tolerance the other tests use.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_noalloc_matches_workspace_entry_point(orc):
+    from verify_gemm_gb300 import build
+
+    build.build()
+    import verify_gemm_gb300 as vg
+    from verify_gemm_gb300 import _lib
+
+    lib = _lib.load()
+    M, K = 1040, 2560                    # several row blocks and K splits
+    g = torch.Generator().manual_seed(123)
+    W = torch.randn((M, K), generator=g) * 0.02
+    wt = vg.nvfp4_pack(W.cuda())
+    nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call, N in enumerate((8, 3)):    # two calls in a row
+        x = (torch.randn((N, K), generator=g)).to(torch.bfloat16).cuda()
+        y_ref = vg.gemv(wt, x)           # existing entry point, own workspace
+        y = torch.full((N, M), 7.0, dtype=torch.bfloat16, device="cuda")
+        s = lib.vg_gemv_nvfp4_noalloc(ctypes.c_void_p(wt.w.data_ptr()),
+                                      ctypes.c_void_p(wt.scales.data_ptr()), wt.gscale,
+                                      ctypes.c_void_p(x.data_ptr()), N, M, K,
+                                      ctypes.c_void_p(y.data_ptr()), stream)
+        assert s == 0, (call, lib.vg_status_string(s))
+        torch.cuda.synchronize()
+        yr, a = orc.gemv_nvfp4(nib, sc, gs, _bits(x), threads=8)
+        bad_new, _ = orc.check(_bits(y), yr, a)
+        bad_old, _ = orc.check(_bits(y_ref), yr, a)
+        assert bad_new == 0 and bad_old == 0, (call, bad_new, bad_old)
+        # both use the same kernel and split, so they agree within tolerance
+        # of each other too (in practice bit for bit)
+        diff = (y.double() - y_ref.double()).abs().cpu().numpy()
+        assert np.all(diff <= 4e-3 * a + 1e-6), call
+
+
+def test_noalloc_rejects_matrices_beyond_the_scratch_size():
+    from verify_gemm_gb300 import _lib
+
+    lib = _lib.load()
+    p = ctypes.c_void_p(0x10000)
+    # 2^39 elements need arrival counters far beyond the 4 MiB array
+    s = lib.vg_gemv_nvfp4_noalloc(p, p, 1.0, p, 1, 1 << 29, 1024, p, None)
+    assert s == _lib.VG_ERR_UNSUPPORTED

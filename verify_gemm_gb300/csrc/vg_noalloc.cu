@@ -1,0 +1,70 @@
+// vg_noalloc.cu -- vg_gemv_nvfp4_noalloc: the NVFP4 GEMV for callers that
+// cannot allocate device memory.
+//
+// vg_gemv_nvfp4 needs a workspace (arrival counters, an error word and FP32
+// partial sums for row blocks whose K range is split between thread
+// blocks), and expects the caller to allocate it.  Some callers cannot:
+// code that runs inside a host application which owns all device memory
+// and only lends out the input and output buffers (a plugin or an engine
+// adapter), code that must not call cudaMalloc because it can synchronise
+// the whole device and stall other work, and code that runs under a memory
+// budget that a hidden allocation would break.  For them this file keeps
+// one fixed scratch array in device memory, created when the library is
+// loaded and held by every GPU that loads it until the process exits, and
+// runs the unchanged GEMV with that array as its workspace.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "vg_internal.h"
+
+namespace {
+
+// Largest workspace this entry point can serve: 4 MiB, enough for one
+// thread block per SM on a 160-SM device (2.5 MiB of partial sums) plus
+// arrival counters for about 390 000 row blocks of 256 rows.
+constexpr size_t kScratchBytes = VG_NOALLOC_SCRATCH_BYTES;
+
+// The workspace lives here.  In host code this name is only a stand-in for
+// the device array, never a usable address: the device address is looked
+// up per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void *g_scratch_ptr[64] = {};
+
+// Device address of g_scratch on the current device, looked up once per
+// device (on the first call made with that device current).
+vg_status scratch_address(void **out) {
+  int dev = 0;
+  VG_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return VG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    VG_CUDA(cudaGetSymbolAddress(&p, g_scratch));
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return VG_OK;
+}
+
+}  // namespace
+
+extern "C" vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, float gscale,
+                                           const uint16_t *x, int N, int64_t M, int64_t K,
+                                           uint16_t *y, vg_stream_t stream) {
+  // Arguments are checked by vg_gemv_nvfp4 below; the size check needs M, K.
+  if (vg_status s = vg::check_mk(M, K)) return s;
+  size_t need = 0;
+  if (vg_status s = vg_gemv_workspace_size(M, K, VG_FMT_NVFP4, &need)) return s;
+  if (need > kScratchBytes) return VG_ERR_UNSUPPORTED;   // beyond the fixed maximum
+  void *scratch = nullptr;
+  if (vg_status s = scratch_address(&scratch)) return s;
+  // The array keeps whatever the previous call left.  The kernel expects
+  // its error word and arrival counters to start at zero, so clear the part
+  // of the array this call uses (at most kScratchBytes) on the stream.
+  VG_CUDA(cudaMemsetAsync(scratch, 0, need, vg::as_cuda(stream)));
+  return vg_gemv_nvfp4(w, scales, gscale, x, N, M, K, y, scratch, kScratchBytes, stream);
+}
