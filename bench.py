@@ -44,6 +44,10 @@ def parse():
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default="stack",
+                    choices=["stack", "tiny", "proj", "gateup", "down", "head", "probe"],
+                    help="stack: the fused verify pass (headline); others: one product of "
+                         "that configuration, timed alone with an L2 flush between launches")
     return ap.parse_args()
 
 
@@ -327,11 +331,135 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+SINGLE = {
+    "tiny": ("tiny NVFP4 GEMV 256x512, seed 0", ["w"]),
+    "proj": ("single projection NVFP4 5120x5120, outlier x, seed 1", ["w"]),
+    "gateup": ("fused gate+up NVFP4 34816x5120 (two 17408x5120 halves), seed 2",
+               ["gate", "up"]),
+    "down": ("row-scaled FP8 down 5120x17408, seed 3", ["down"]),
+    "head": ("NVFP4 head 151936x5120, seed 3", ["head"]),
+}
+
+
+def run_single(args, local):
+    """One configuration's product, timed alone: L2 flushed (a 512 MB write)
+    between launches, CUDA events around each launch only."""
+    import torch
+
+    import verify_gemm_gb300 as vg
+    from verify_gemm_gb300 import build as vbuild
+    from verify_gemm_gb300.inputs import WORKLOADS, draw_workload
+
+    vbuild.build()
+    torch.cuda.set_device(local)
+    key = {"down": "down_head", "head": "down_head"}.get(args.workload, args.workload)
+    title, names = SINGLE[args.workload]
+    Ws, xs = draw_workload(key, args.N, device="cuda")
+    mats = WORKLOADS[key].mats
+    entries = []
+    for m, W in zip(mats, Ws):
+        if m.name not in names:
+            continue
+        wt = vg.nvfp4_pack(W) if m.fmt == "nvfp4" else vg.fp8_pack(W)
+        y = torch.empty((args.N, m.M), dtype=torch.bfloat16, device="cuda")
+        entries.append((wt, xs[m.K], y, 0))
+    del Ws
+    nbytes = sum(e[0].nbytes for e in entries)
+    if len(entries) == 1:
+        wt, x, y, _ = entries[0]
+        ws = vg.workspace_for(wt)
+
+        def run():
+            vg.gemv(wt, x, y, ws)
+    else:
+        plan = vg.VerifyPlan(entries, args.N, ordered=True)
+        run = plan.run
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        run()
+    torch.cuda.synchronize()
+    per = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        per.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in per]
+    med = statistics.median(ms)
+    peak, kind = peaks()
+    line = {"metric": METRIC, "value": round(nbytes / (med / 1e3) / 1e9, 1), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(med, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4/fp8-e4m3 weights x bf16 -> f32",
+            "data": "synthetic",
+            "config": {"workload": title, "N": args.N, "bytes": nbytes,
+                       "l2": "flushed by a 512 MB write before every launch",
+                       "us_p10_p90": [round(1e3 * sorted(ms)[len(ms) // 10], 2),
+                                      round(1e3 * sorted(ms)[(9 * len(ms)) // 10], 2)]},
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / (med / 1e3) / 1e9, 1),
+                         "peak": peak, "unit": "GB/s",
+                         "frac": round(nbytes / (med / 1e3) / 1e9 / peak, 4), "traffic": None,
+                         "peak_kind": kind},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
+def run_probe(args, local):
+    """Read-only HBM ceiling: vector loads and per-warp bulk-copy rings over a
+    4 GiB buffer (>> L2), median of `steps` launches each."""
+    import ctypes
+
+    import torch
+
+    from verify_gemm_gb300 import _lib
+    from verify_gemm_gb300 import build as vbuild
+
+    vbuild.build()
+    torch.cuda.set_device(local)
+    lib = _lib.load()
+    nbytes = 4 << 30
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(8192, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = {}
+    configs = [(1, 12288, 1), (0, 0, 0), (1, 2048, 6), (1, 4096, 3), (1, 2048, 4),
+               (1, 1024, 12), (1, 2048, 2), (1, 4096, 2), (1, 8192, 1), (1, 12288, 1),
+               (0, 0, 0), (1, 2048, 6)]
+    for mode, chunk, slots in configs:
+        ms = []
+        for i in range(args.warmup + args.steps):
+            a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+            a.record(stream)
+            s = lib.vg_hbm_read_probe(ctypes.c_void_p(buf.data_ptr()), nbytes, mode, chunk, slots,
+                                      ctypes.c_void_p(sink.data_ptr()), sink.numel(),
+                                      ctypes.c_void_p(stream.cuda_stream))
+            _lib.check(s, "vg_hbm_read_probe")
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        key = "ldg128" if mode == 0 else f"bulk {chunk}B x{slots} slots/warp"
+        out.setdefault(key, []).append(round(nbytes / (statistics.median(ms) / 1e3) / 1e9, 1))
+    peak, kind = peaks()
+    print(json.dumps({"metric": "read-only HBM probe GB/s", "unit": "GB/s", "bytes": nbytes,
+                      "results": out, "copy_peak": peak, "peak_kind": kind}), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload == "probe":
+        run_probe(args, int(os.environ.get("LOCAL_RANK", "0")))
+        return
     world, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload != "stack":
+        run_single(args, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

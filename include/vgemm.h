@@ -34,15 +34,18 @@
  *  - Limits: 1 <= N <= 8, M >= 1, K >= 16, K % 16 == 0, M * K < 2^40.
  *
  * Device weight layout (the "packed" form; canonical forms are below):
- *  NVFP4 codes are stored in 16-row tiles.  Each tile is a run of 64-column
- *  units of 512 bytes, arranged so that every lane of a warp reads one
- *  16-byte vector per unit holding 16 consecutive K positions of two rows
- *  (one scale block of each), with the bits of each code placed for a
- *  cheap in-register decode to BF16.  Block scales live in a separate
- *  buffer, 256 bytes per tile per 256 columns, re-encoded losslessly so
- *  that E4M3 subnormal scales decode like normal ones.  Row-scaled FP8
- *  codes use 1024-byte units of the same shape; their FP32 row scales are
- *  a plain [M] array.  Rows past M and columns past K are zero padding.
+ *  NVFP4 codes are stored in 16-row tiles cut into 64-column units of 512
+ *  bytes, arranged so that every lane of a warp reads one 16-byte vector
+ *  per unit holding 16 consecutive K positions of two rows (one scale block
+ *  of each), with the bits of each code placed for a cheap in-register
+ *  decode to BF16.  Units are ordered by row block (16 tiles), then chunk
+ *  (8 units), then tile, so that one chunk of a whole row block -- the
+ *  kernel's unit of work -- is one contiguous run of bytes.  Block scales
+ *  live in a separate buffer in the same order, 512 bytes per tile per
+ *  chunk, re-encoded losslessly so that E4M3 subnormal scales decode like
+ *  normal ones.  Row-scaled FP8 codes use 1024-byte units (4 per chunk) in
+ *  the same order; their FP32 row scales are a plain [M] array.  Rows past
+ *  M and columns past K are zero padding inside the last tile and unit.
  *  The packed buffers are opaque: use the pack / unpack / from_canonical
  *  calls to move between them and the canonical layout.
  *
@@ -212,6 +215,19 @@ vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, float gscale,
  * kernel ran out (then the workspace is also re-zeroed). */
 vg_status vg_gemv_workspace_check(void *workspace, size_t workspace_bytes,
                                   int *device_error, vg_stream_t stream);
+
+/* ------------------------------------------------------ HBM read probe */
+
+/* Read-only bandwidth probe (the "physics-based" ceiling that crit's Eval
+ * measures, crit README, Eval section; the engine card's Measured section
+ * sets the verify pass against the card's read rate).  Reads `bytes` of the
+ * device buffer `buf` once and folds them into `sink` (device, >= one word
+ * per thread block: the SM count for mode 1, SMs x resident blocks for
+ * mode 0).  mode 0: 16-byte vector loads; mode 1: per-warp rings of
+ * `slots` bulk copies of `chunk` bytes (chunk a multiple of 256,
+ * chunk * slots <= 12288).  Time it with events on `stream`. */
+vg_status vg_hbm_read_probe(const void *buf, size_t bytes, int mode, int chunk, int slots,
+                            uint32_t *sink, int sink_words, vg_stream_t stream);
 
 /* -------------------------------------------------- fused verify pass */
 

@@ -63,7 +63,7 @@ def test_size_queries(lib):
     assert wb.value + 4 * 5120 == 89_149_440
     # ragged shapes round up to 16-row tiles and 64-column units
     assert lib.vg_nvfp4_sizes(17, 80, ctypes.byref(wb), ctypes.byref(sb)) == 0
-    assert wb.value == 2 * 2 * 512 and sb.value == 2 * 1 * 256
+    assert wb.value == 2 * 2 * 512 and sb.value == 2 * 1 * 512
     assert lib.vg_fp8_sizes(1, 16, ctypes.byref(wb)) == 0 and wb.value == 1024
 
 

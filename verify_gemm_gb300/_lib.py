@@ -60,6 +60,7 @@ SIGNATURES = {
     "vg_gemv_fp8_rowscale": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_workspace_check": (st, [P, sz, ctypes.POINTER(i32), P]),
     "vg_gemv_nvfp4_noalloc": (st, [P, P, f32, P, i32, i64, i64, P, P]),
+    "vg_hbm_read_probe": (st, [P, sz, i32, i32, i32, P, i32, P]),
     "vg_verify_plan_create": (st, [ctypes.POINTER(vg_matrix_desc), i32, i32, i32,
                                    ctypes.POINTER(P)]),
     "vg_verify_plan_create_ex": (st, [ctypes.POINTER(vg_matrix_desc), i32, i32,

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libvgemm.so")
-SOURCES = ["vg_api.cu", "vg_pack.cu", "vg_gemv.cu", "vg_noalloc.cu"]
+SOURCES = ["vg_api.cu", "vg_pack.cu", "vg_gemv.cu", "vg_noalloc.cu", "vg_probe.cu"]
 HEADERS = ["vg_device.cuh", "vg_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-prec-div=true",

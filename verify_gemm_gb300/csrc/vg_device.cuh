@@ -19,26 +19,57 @@ constexpr int kTileRows = 16;
 constexpr int kUnitK = 64;
 constexpr int kNvUnitBytes = 512;
 constexpr int kF8UnitBytes = 1024;
-// NVFP4 block scales: per tile, per chunk of 4 units (256 columns), 32 lanes
-// x 8 bytes: [unit 0..3][row g, row g+8].
-constexpr int kNvChunkUnits = 4;
-constexpr int kNvScaleChunkBytes = 256;
-constexpr int kF8ChunkUnits = 2;
+// A chunk is 8 NVFP4 units (512 columns, 4096 bytes per tile) or 4 FP8
+// units (256 columns, 4096 bytes).  NVFP4 block scales: per tile per chunk,
+// 32 lanes x 16 bytes: [unit 0..7][row g, row g+8].
+constexpr int kNvChunkUnits = 8;
+constexpr int kNvScaleLaneBytes = 2 * kNvChunkUnits;                    // 16
+constexpr int kNvScaleChunkBytes = 32 * kNvScaleLaneBytes;              // 512
+constexpr int kF8ChunkUnits = 4;
 
-// A row block is 16 row tiles (256 rows); one pipeline stage holds one
-// chunk of every tile of a row block.
+// A row block is 16 row tiles (256 rows); a work item is one chunk of every
+// tile of a row block.  Each of the 16 consumer warps owns one tile of the
+// row block and streams its own part of every item through a private ring
+// of kSlots shared-memory slots (one slot = one tile's chunk: 4 NVFP4 units
+// + their 256 scale bytes, or 2 FP8 units).
+#ifndef VG_WARPS
+#define VG_WARPS 16
+#endif
+#ifndef VG_SLOTS
+#define VG_SLOTS 3
+#endif
 constexpr int kBlockTiles = 16;
-constexpr int kConsumerWarps = 8;            // 2 row tiles per warp
-constexpr int kTilesPerWarp = kBlockTiles / kConsumerWarps;
-constexpr int kStageNvCodeBytes = kBlockTiles * kNvChunkUnits * kNvUnitBytes;   // 32768
-constexpr int kStageBytes = kStageNvCodeBytes + kBlockTiles * kNvScaleChunkBytes;  // 36864
-constexpr int kStages = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
+constexpr int kWarps = VG_WARPS;
+static_assert(kWarps == kBlockTiles, "one tile of the row block per warp");
+constexpr int kSlots = VG_SLOTS;
+constexpr int kSlotCodeBytes = kNvChunkUnits * kNvUnitBytes;          // 4096
+constexpr int kSlotBytes = kSlotCodeBytes + kNvScaleChunkBytes;        // 4608
+constexpr int kThreads = kWarps * 32;
 
-static_assert(kF8ChunkUnits * kF8UnitBytes == kNvChunkUnits * kNvUnitBytes,
-              "an FP8 chunk fills the NVFP4 code slot of a tile");
+static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
+              "an FP8 chunk fills the code part of a slot");
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Item-contiguous order of the packed buffers.  Codes are grouped by row
+// block (16 tiles), then by chunk (cu units), then by tile, then by unit, so
+// that one work item -- one chunk of every tile of a row block -- is one
+// contiguous run of bytes and consecutive chunks of a row block follow each
+// other.  Only the last row block may have fewer than 16 tiles and only the
+// last chunk fewer than cu units; nothing is padded.
+__host__ __device__ inline int64_t code_offset(int64_t mt, int64_t u, int64_t MT, int64_t KU,
+                                               int64_t cu, int64_t ub) {
+  const int64_t rb = mt / 16, tile = mt % 16, c = u / cu, uu = u % cu;
+  const int64_t tiles = (MT - rb * 16) < 16 ? (MT - rb * 16) : 16;
+  const int64_t nu = (KU - c * cu) < cu ? (KU - c * cu) : cu;
+  return rb * 16 * KU * ub + c * tiles * cu * ub + tile * nu * ub + uu * ub;
+}
+// Byte offset of the scale chunk c of tile mt (same grouping).
+__host__ __device__ inline int64_t scale_offset(int64_t mt, int64_t c, int64_t MT, int64_t KC) {
+  const int64_t rb = mt / 16, tile = mt % 16;
+  const int64_t tiles = (MT - rb * 16) < 16 ? (MT - rb * 16) : 16;
+  return (rb * 16 * KC + c * tiles + tile) * kNvScaleChunkBytes;
+}
 
 // ------------------------------------------------------ decode constants
 // NVFP4 code bit positions inside a packed 32-bit word.  A word holds the 8
@@ -103,9 +134,12 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
+// BF16x2 product a*b as a fused multiply-add with a -0 addend (native
+// HFMA2 on BF16).  Every product formed here is exact in BF16, and adding
+// -0 keeps both the value and the sign of a zero product.
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0x80008000u));
   return d;
 }
 
@@ -203,19 +237,33 @@ __device__ __forceinline__ uint4 ldg128(const void *p) {
   return v;
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ----------------------------------------------------- in-register decode
 // Four BF16x2 A-fragment registers of one NVFP4 word, each multiplied by
-// the packed scale of its row (fg for rows g, fg8 for rows g+8).
-__device__ __forceinline__ void nv_decode(uint32_t w, uint32_t fg, uint32_t fg8, uint32_t &a0,
-                                          uint32_t &a1, uint32_t &a2, uint32_t &a3) {
+// the packed scale of its row (fg for rows g, fg8 for rows g+8).  The left
+// shifts by 3 and 6 are written as multiplies by m8 = 8 and m64 = 64 held in
+// registers, so that they run on the FMA pipe next to the integer logic.
+__device__ __forceinline__ uint32_t umul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void nv_decode(uint32_t w, uint32_t fg, uint32_t fg8, uint32_t m8,
+                                          uint32_t m64, uint32_t &a0, uint32_t &a1,
+                                          uint32_t &a2, uint32_t &a3) {
   const uint32_t r0 = w & kNvMask;
-  const uint32_t r1 = (w << 3) & kNvMask;
-  const uint32_t r2 = (w << 6) & kNvMask;
-  const uint32_t r3 = (((w >> 7) & kNvR3Pick) * kNvR3Spread) & kNvMask;
+  const uint32_t r1 = umul(w, m8) & kNvMask;
+  const uint32_t r2 = umul(w, m64) & kNvMask;
+  const uint32_t r3 = umul((w >> 7) & kNvR3Pick, kNvR3Spread) & kNvMask;
   a0 = bmul2(r0, fg);
   a1 = bmul2(r1, fg8);
   a2 = bmul2(r2, fg);

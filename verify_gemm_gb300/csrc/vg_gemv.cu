@@ -76,13 +76,16 @@ struct Params {
   uint32_t *ctas_done;
   float *partials;          // [grid][2][16 tiles][32 lanes][4]
   int *error;
+  uint32_t m8, m64;         // 8 and 64: shift multipliers kept in registers
   MatDev mat0;
   PhaseDev phase0;
 };
 
 constexpr int kPartialFloats = kBlockTiles * 32 * 4;   // one slot
-constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStages * 8 + 64;
-constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3;
+constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;
+constexpr int kSmemBytes = kRingBytes + kWarps * kSlots * 8 + 64;
+constexpr int kErrFullWait = 1, kErrDepWait = 3;
+constexpr int kConsumers = kWarps * 32;
 
 __host__ __device__ inline int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -95,108 +98,249 @@ __device__ inline int64_t owner(int64_t T, int64_t G, int64_t i) { return ((i + 
 
 __device__ inline void set_error(int *error, int code) { atomicCAS(error, 0, code); }
 
-// Per-CTA walk over the (matrix, row block, chunk) items of one phase.
-struct Cursor {
+// The items one thread block processes, in order, across all phases: for
+// each phase with items for this block, its contiguous range [i0, i1).  The
+// position inside the current matrix (row block rb, chunk c) advances
+// incrementally; the only divisions happen when a phase starts.
+struct Seq {
   const MatDev *mats;
-  int mi, mend;
-  MatDev m;
-  __device__ void start(const MatDev *all, const PhaseDev &ph) {
-    mats = all;
-    mi = ph.mat_begin;
-    mend = ph.mat_end;
-    m = mats[mi];
+  const PhaseDev *phases;
+  int nphases, ph, mi, mend;
+  int64_t b, grid, G, i, i0, i1, items;
+  int64_t rb, c, KC, RB;
+  bool valid;
+
+  __device__ void init(const MatDev *m, const PhaseDev *p, int np, int64_t blk, int64_t g) {
+    mats = m;
+    phases = p;
+    nphases = np;
+    b = blk;
+    grid = g;
+    ph = -1;
+    next_phase();
   }
-  __device__ void seek(int64_t item) {
-    while (item >= m.item0 + m.RB * m.KC && mi + 1 < mend) m = mats[++mi];
+  __device__ void next_phase() {
+    for (++ph; ph < nphases; ++ph) {
+      items = phases[ph].items;
+      G = i64min(grid, items);
+      if (b < G) {
+        i0 = item_begin(items, G, b);
+        i1 = item_begin(items, G, b + 1);
+        i = i0;
+        mi = phases[ph].mat_begin;
+        mend = phases[ph].mat_end;
+        while (mi + 1 < mend && i >= mats[mi].item0 + mats[mi].RB * mats[mi].KC) ++mi;
+        KC = mats[mi].KC;
+        RB = mats[mi].RB;
+        const int64_t rel = i - mats[mi].item0;
+        rb = rel / KC;
+        c = rel - rb * KC;
+        valid = true;
+        return;
+      }
+    }
+    valid = false;
+  }
+  __device__ __forceinline__ void advance() {
+    if (++i == i1) {
+      next_phase();
+      return;
+    }
+    if (++c == KC) {
+      c = 0;
+      if (++rb == RB) {
+        rb = 0;
+        ++mi;
+        KC = mats[mi].KC;
+        RB = mats[mi].RB;
+      }
+    }
   }
 };
 
+// Issue the bulk copies of this warp's tile of the item at `q` into ring
+// slot `slot_addr` (lane 0 only).  A tile past the matrix arrives with no
+// bytes.  Offsets follow the item-contiguous packed order.
+__device__ __forceinline__ void issue_tile(const Seq &q, int warp, uint32_t slot_addr,
+                                           uint32_t bar, uint64_t policy) {
+  const MatDev &m = q.mats[q.mi];
+  const int64_t tiles = i64min(kBlockTiles, m.MT - q.rb * kBlockTiles);
+  if (warp >= tiles) {
+    mbar_arrive_expect_tx(bar, 0);
+    return;
+  }
+  const bool nv = m.fmt == VG_FMT_NVFP4;
+  const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
+  const int64_t ub = nv ? kNvUnitBytes : kF8UnitBytes;
+  const int64_t nu = i64min(cu, m.KU - q.c * cu);
+  const uint32_t code_bytes = uint32_t(nu * ub);
+  const int64_t off = q.rb * kBlockTiles * m.KU * ub + q.c * tiles * cu * ub + warp * nu * ub;
+  mbar_arrive_expect_tx(bar, code_bytes + (nv ? kNvScaleChunkBytes : 0));
+  bulk_g2s(slot_addr, m.w + off, code_bytes, bar, policy);
+  if (nv) {
+    const int64_t soff = (q.rb * kBlockTiles * m.KC + q.c * tiles + warp) * kNvScaleChunkBytes;
+    bulk_g2s(slot_addr + kSlotCodeBytes, m.sc + soff, kNvScaleChunkBytes, bar, policy);
+  }
+}
+
+// One NVFP4 unit of one tile: 4 MMAs (k16 steps) into two accumulators.
+__device__ __forceinline__ void nv_unit(const uint4 wv, uint32_t fg, uint32_t fg8, const uint4 xa,
+                                        const uint4 xb, uint32_t m8, uint32_t m64,
+                                        float (&acc0)[4], float (&acc1)[4]) {
+  uint32_t a0, a1, a2, a3;
+  nv_decode(wv.x, fg, fg8, m8, m64, a0, a1, a2, a3);
+  mma_bf16(acc0, a0, a1, a2, a3, xa.x, xa.y);
+  nv_decode(wv.y, fg, fg8, m8, m64, a0, a1, a2, a3);
+  mma_bf16(acc1, a0, a1, a2, a3, xa.z, xa.w);
+  nv_decode(wv.z, fg, fg8, m8, m64, a0, a1, a2, a3);
+  mma_bf16(acc0, a0, a1, a2, a3, xb.x, xb.y);
+  nv_decode(wv.w, fg, fg8, m8, m64, a0, a1, a2, a3);
+  mma_bf16(acc1, a0, a1, a2, a3, xb.z, xb.w);
+}
+
+__device__ __forceinline__ void f8_unit(const uint4 w0, const uint4 w1, const uint4 xa,
+                                        const uint4 xb, float (&acc0)[4], float (&acc1)[4]) {
+  uint32_t a0, a1, a2, a3;
+  f8_decode(w0.x, a0, a1);
+  f8_decode(w0.y, a2, a3);
+  mma_bf16(acc0, a0, a1, a2, a3, xa.x, xa.y);
+  f8_decode(w0.z, a0, a1);
+  f8_decode(w0.w, a2, a3);
+  mma_bf16(acc1, a0, a1, a2, a3, xa.z, xa.w);
+  f8_decode(w1.x, a0, a1);
+  f8_decode(w1.y, a2, a3);
+  mma_bf16(acc0, a0, a1, a2, a3, xb.x, xb.y);
+  f8_decode(w1.z, a0, a1);
+  f8_decode(w1.w, a2, a3);
+  mma_bf16(acc1, a0, a1, a2, a3, xb.z, xb.w);
+}
+
+// x fragment of one unit for lane (g, t): the 16 columns at xp as two
+// 16-byte loads, or zeros when `on` is false (column g >= N or K padding).
+__device__ __forceinline__ void load_x(const uint16_t *xp, bool on, uint4 &xa, uint4 &xb) {
+  if (on) {
+    xa = ldg128(xp);
+    xb = ldg128(xp + 8);
+  } else {
+    xa = make_uint4(0, 0, 0, 0);
+    xb = xa;
+  }
+}
+
+// A whole NVFP4 chunk (8 units) of this lane's tile: scale pairs from one
+// 16-byte load, codes and x for two units at a time, the next pair loaded
+// before the current one is multiplied.
+__device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, const uint16_t *xp,
+                                              bool on, uint32_t m8, uint32_t m64,
+                                              float (&acc0)[4], float (&acc1)[4]) {
+  const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
+  const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+  uint4 w0 = lds128(slot + lane * 16), w1 = lds128(slot + kNvUnitBytes + lane * 16);
+  uint4 x0a, x0b, x1a, x1b;
+  load_x(xp, on, x0a, x0b);
+  load_x(xp + kUnitK, on, x1a, x1b);
+#pragma unroll
+  for (int h = 0; h < kNvChunkUnits / 2; ++h) {
+    uint4 nw0, nw1, nx0a, nx0b, nx1a, nx1b;
+    if (h + 1 < kNvChunkUnits / 2) {
+      nw0 = lds128(slot + (2 * h + 2) * kNvUnitBytes + lane * 16);
+      nw1 = lds128(slot + (2 * h + 3) * kNvUnitBytes + lane * 16);
+      load_x(xp + (2 * h + 2) * kUnitK, on, nx0a, nx0b);
+      load_x(xp + (2 * h + 3) * kUnitK, on, nx1a, nx1b);
+    }
+    // unit 2h uses scale bytes 0,1 of word h; unit 2h+1 bytes 2,3
+    nv_unit(w0, nv_scale_pair(scw[h], 0), nv_scale_pair(scw[h], 1), x0a, x0b, m8, m64, acc0,
+            acc1);
+    nv_unit(w1, nv_scale_pair(scw[h], 2), nv_scale_pair(scw[h], 3), x1a, x1b, m8, m64, acc0,
+            acc1);
+    if (h + 1 < kNvChunkUnits / 2) {
+      w0 = nw0;
+      w1 = nw1;
+      x0a = nx0a;
+      x0b = nx0b;
+      x1a = nx1a;
+      x1b = nx1b;
+    }
+  }
+}
+
+// A partial NVFP4 chunk (the K tail): nu units, columns checked against K.
+__device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uint16_t *xp,
+                                              bool on, int nu, int64_t kleft, uint32_t m8,
+                                              uint32_t m64, float (&acc0)[4],
+                                              float (&acc1)[4]) {
+  const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
+  for (int u = 0; u < nu; ++u) {
+    const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
+    uint4 xa, xb;
+    load_x(xp + u * kUnitK, on && u * kUnitK < kleft, xa, xb);
+    const int q = u >> 1;
+    const uint32_t word = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
+    const uint32_t b = uint32_t(u & 1) * 2u;
+    nv_unit(wv, nv_scale_pair(word, b), nv_scale_pair(word, b + 1), xa, xb, m8, m64, acc0, acc1);
+  }
+}
+
+// An FP8 chunk: nu (<= 4) units of 1024 bytes, two at a time.
+__device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t *xp, bool on,
+                                         int nu, int64_t kleft, float (&acc0)[4],
+                                         float (&acc1)[4]) {
+#pragma unroll
+  for (int u = 0; u < kF8ChunkUnits; ++u) {
+    if (u < nu) {
+      const uint4 w0 = lds128(slot + u * kF8UnitBytes + lane * 32);
+      const uint4 w1 = lds128(slot + u * kF8UnitBytes + lane * 32 + 16);
+      uint4 xa, xb;
+      load_x(xp + u * kUnitK, on && u * kUnitK < kleft, xa, xb);
+      f8_unit(w0, w1, xa, xb, acc0, acc1);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-  volatile int *sflag = reinterpret_cast<volatile int *>(bars + 2 * kStages);
-  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
+  volatile int *sflag = reinterpret_cast<volatile int *>(bars + kWarps * kSlots);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t b = blockIdx.x;
+  const int g = lane >> 2, t = lane & 3;
+  const int N = p.N;
   const MatDev *mats = p.mats ? p.mats : &p.mat0;
   const PhaseDev *phases = p.mats ? p.phases : &p.phase0;
+  const uint32_t ring = smem_addr(smem + warp * kSlots * kSlotBytes);
+  const uint32_t bar0 = smem_addr(bars + warp * kSlots);
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kConsumerWarps);
-    }
+  if (lane == 0) {
+    for (int s = 0; s < kSlots; ++s) mbar_init(bar0 + 8 * s, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid == 0) {
     sflag[0] = 0;
     sflag[1] = 0;
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    // ================================================================ producer
-    const uint64_t policy = policy_evict_first();
-    int64_t it = 0;
-    bool aborted = false;
-    for (int ph = 0; ph < p.nphases && !aborted; ++ph) {
-      const PhaseDev P = phases[ph];
-      const int64_t G = i64min(p.grid, P.items);
-      if (b >= G) continue;
-      Cursor cur;
-      cur.start(mats, P);
-      const int64_t i1 = item_begin(P.items, G, b + 1);
-      for (int64_t i = item_begin(P.items, G, b); i < i1; ++i, ++it) {
-        cur.seek(i);
-        const MatDev &m = cur.m;
-        const int s = int(it % kStages);
-        const uint32_t par = uint32_t(it / kStages) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, par ^ 1u, globaltimer() + p.timeout_ns)) {
-          if (lane == 0) set_error(p.error, kErrEmptyWait);
-          aborted = true;
-          break;
-        }
-        const int64_t rel = i - m.item0, rb = rel / m.KC, c = rel % m.KC;
-        const int64_t tiles = i64min(kBlockTiles, m.MT - rb * kBlockTiles);
-        const bool nv = m.fmt == VG_FMT_NVFP4;
-        const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
-        const int64_t nu = i64min(cu, m.KU - c * cu);
-        const uint32_t code_bytes = uint32_t(nu * (nv ? kNvUnitBytes : kF8UnitBytes));
-        const uint32_t bytes = uint32_t(tiles) * (code_bytes + (nv ? kNvScaleChunkBytes : 0));
-        const uint32_t stage = smem_addr(smem + s * kStageBytes);
-        const uint32_t full = full0 + 8 * s;
-        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
-        __syncwarp();
-        const int r = lane & 15;
-        if (r < tiles) {
-          const int64_t mt = rb * kBlockTiles + r;
-          if (lane < 16) {
-            const uint8_t *src = m.w + (mt * m.KU + c * cu) * (nv ? kNvUnitBytes : kF8UnitBytes);
-            bulk_g2s(stage + r * (kNvChunkUnits * kNvUnitBytes), src, code_bytes, full, policy);
-          } else if (nv) {
-            const uint8_t *src = m.sc + (mt * m.KC + c) * kNvScaleChunkBytes;
-            bulk_g2s(stage + kStageNvCodeBytes + r * kNvScaleChunkBytes, src,
-                     kNvScaleChunkBytes, full, policy);
-          }
-        }
-      }
-    }
-    // Never leave the block while a bulk copy may still be writing shared
-    // memory: wait (bounded) for the last stages issued.
-    for (int64_t k = i64max(0, it - kStages); k < it; ++k) {
-      const int s = int(k % kStages);
-      mbar_wait(full0 + 8 * s, uint32_t(k / kStages) & 1u, globaltimer() + p.timeout_ns);
-    }
-  } else {
-    // =============================================================== consumers
-    const int g = lane >> 2, t = lane & 3;
-    const int N = p.N;
-    int64_t it = 0;
-    bool aborted = false;
-    float acc[kTilesPerWarp][4];
-    for (int ph = 0; ph < p.nphases; ++ph) {
-      const PhaseDev P = phases[ph];
-      const int64_t G = i64min(p.grid, P.items);
-      if (b >= G) continue;
-      // ordered verify: group ph's products wait for group ph-1
+  const uint64_t policy = policy_evict_first();
+  Seq cons, pref;
+  cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
+  pref = cons;
+  // Prologue: fill the ring.
+  int64_t issued = 0;
+  for (int q = 0; q < kSlots && pref.valid; ++q, ++issued) {
+    if (lane == 0) issue_tile(pref, warp, ring + q * kSlotBytes, bar0 + 8 * q, policy);
+    pref.advance();
+  }
+
+  bool aborted = false;
+  int64_t n = 0;                 // items consumed
+  int s = 0;                     // ring slot of item n
+  uint32_t par = 0;              // parity of that slot's current phase
+  int cur_ph = -1;
+  int64_t piece_start = 0, piece_c0 = 0;
+  float acc0[4], acc1[4];
+  while (cons.valid) {
+    const int ph = cons.ph;
+    // ---------------------------------------- ordered: wait for group ph-1
+    if (ph != cur_ph) {
       if (p.ordered && ph > 0) {
         if (tid == 0) {
           int ok = 1;
@@ -216,168 +360,143 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           }
           sflag[0] = ok ? 0 : 1;
         }
-        named_bar(1, kConsumerWarps * 32);
+        named_bar(1, kConsumers);
         if (sflag[0]) aborted = true;
-        named_bar(1, kConsumerWarps * 32);
+        named_bar(1, kConsumers);
       }
-      Cursor cur;
-      cur.start(mats, P);
-      const int64_t i0 = item_begin(P.items, G, b), i1 = item_begin(P.items, G, b + 1);
-      int64_t piece_start = i0;
-      for (int64_t i = i0; i < i1; ++i, ++it) {
-        cur.seek(i);
-        const MatDev &m = cur.m;
-        const int64_t rel = i - m.item0, rb = rel / m.KC, c = rel % m.KC;
-        if (c == 0 || i == i0) {
-          piece_start = i;
+      cur_ph = ph;
+    }
+    const MatDev &m = mats[cons.mi];
+    const int64_t rb = cons.rb, c = cons.c;
+    if (c == 0 || cons.i == cons.i0) {
+      piece_start = cons.i;
+      piece_c0 = c;
 #pragma unroll
-          for (int q = 0; q < kTilesPerWarp; ++q)
-            acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-        }
-        const int s = int(it % kStages);
-        const uint32_t par = uint32_t(it / kStages) & 1u;
-        if (!aborted && !mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)) {
-          if (lane == 0) set_error(p.error, kErrFullWait);
-          aborted = true;
-        }
-        if (!aborted) {
-          const uint32_t stage = smem_addr(smem + s * kStageBytes);
-          const bool nv = m.fmt == VG_FMT_NVFP4;
-          const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
-          const int nu = int(i64min(cu, m.KU - c * cu));
-          const int64_t tiles = i64min(kBlockTiles, m.MT - rb * kBlockTiles);
-          const int tile0 = warp * kTilesPerWarp;
-          uint2 scw[kTilesPerWarp];
-          if (nv) {
-#pragma unroll
-            for (int q = 0; q < kTilesPerWarp; ++q)
-              scw[q] = lds64(stage + kStageNvCodeBytes + (tile0 + q) * kNvScaleChunkBytes + lane * 8);
-          }
-          const uint16_t *xrow = m.x + int64_t(g) * m.K;
-          for (int uu = 0; uu < nu; ++uu) {
-            const int64_t kg = (c * cu + uu) * kUnitK + 16 * t;
-            uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
-            if (g < N && kg < m.K) {
-              xa = ldg128(xrow + kg);
-              xb = ldg128(xrow + kg + 8);
-            }
-            const uint32_t bx[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-            for (int q = 0; q < kTilesPerWarp; ++q) {
-              if (tile0 + q >= tiles) continue;
-              const uint32_t base = stage + (tile0 + q) * (kNvChunkUnits * kNvUnitBytes);
-              if (nv) {
-                const uint4 wv = lds128(base + uu * kNvUnitBytes + lane * 16);
-                const uint32_t sw = uu < 2 ? scw[q].x : scw[q].y;
-                const uint32_t sb = uint32_t(uu & 1) * 2u;
-                const uint32_t fg = nv_scale_pair(sw, sb), fg8 = nv_scale_pair(sw, sb + 1);
-                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  uint32_t a0, a1, a2, a3;
-                  nv_decode(wd[j], fg, fg8, a0, a1, a2, a3);
-                  mma_bf16(acc[q], a0, a1, a2, a3, bx[2 * j], bx[2 * j + 1]);
-                }
-              } else {
-                const uint4 w0 = lds128(base + uu * kF8UnitBytes + lane * 32);
-                const uint4 w1 = lds128(base + uu * kF8UnitBytes + lane * 32 + 16);
-                const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  uint32_t a0, a1, a2, a3;
-                  f8_decode(wd[2 * j], a0, a1);
-                  f8_decode(wd[2 * j + 1], a2, a3);
-                  mma_bf16(acc[q], a0, a1, a2, a3, bx[2 * j], bx[2 * j + 1]);
-                }
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+    }
+    const uint32_t slot = ring + s * kSlotBytes;
+    const int64_t mt = rb * kBlockTiles + warp;
+    if (!aborted && !mbar_wait(bar0 + 8 * s, par, globaltimer() + p.timeout_ns)) {
+      if (lane == 0) set_error(p.error, kErrFullWait);
+      aborted = true;
+    }
+    if (!aborted && mt < m.MT) {
+      const bool nv = m.fmt == VG_FMT_NVFP4;
+      const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
+      // lane's x columns of this chunk: x[g][c*cu*64 + 16t ...]
+      const int64_t kc = c * cu * kUnitK;
+      const uint16_t *xp = m.x + int64_t(g) * m.K + kc + 16 * t;
+      const int64_t kleft = m.K - kc - 16 * t;       // columns left for this lane
+      const bool on = g < N;
+      if (nv) {
+        // warp-uniform test (mma.sync needs the whole warp): the chunk's whole
+        // column range lies inside K
+        if ((c * cu + cu) * kUnitK <= m.K)
+          nv_chunk_full(slot, lane, xp, on, p.m8, p.m64, acc0, acc1);
+        else
+          nv_chunk_tail(slot, lane, xp, on, int(i64min(cu, m.KU - c * cu)), kleft, p.m8,
+                        p.m64, acc0, acc1);
+      } else {
+        f8_chunk(slot, lane, xp, on, int(i64min(cu, m.KU - c * cu)), kleft, acc0, acc1);
+      }
+    }
+    // Refill this slot with the item kSlots ahead (after every lane has
+    // finished reading it).
+    __syncwarp();
+    if (pref.valid) {
+      if (lane == 0) {
+        fence_proxy_async();
+        issue_tile(pref, warp, slot, bar0 + 8 * s, policy);
+      }
+      pref.advance();
+      ++issued;
+    }
+    ++n;
+    if (++s == kSlots) {
+      s = 0;
+      par ^= 1u;
+    }
 
-        // ------------------------------------------- end of a row-block piece
-        if (c != m.KC - 1 && i != i1 - 1) continue;
-        const bool full_piece = (piece_start - m.item0) % m.KC == 0 && c == m.KC - 1;
-        const int64_t mt0 = rb * kBlockTiles + warp * kTilesPerWarp;
-        bool write_out = true;
-        if (!full_piece) {
-          // partial sums: stash, count arrivals, the last arrival reduces
-          const int slot = int(2 * b + (piece_start == i0 ? 0 : 1));
-          float *part = p.partials + int64_t(slot) * kPartialFloats;
+    // ------------------------------------------------ end of a row-block piece
+    const bool piece_end = c == m.KC - 1 || cons.i == cons.i1 - 1;
+    if (piece_end) {
+      const int64_t T = cons.items, G = cons.G, i0 = cons.i0;
+      const bool full_piece = piece_c0 == 0 && c == m.KC - 1;
+      float acc[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = acc0[e] + acc1[e];
+      bool write_out = true;
+      if (!full_piece) {
+        const int slotp = int(2 * blockIdx.x + (piece_start == i0 ? 0 : 1));
+        float *part = p.partials + int64_t(slotp) * kPartialFloats;
+        if (!aborted) {
+          *reinterpret_cast<float4 *>(part + (warp * 32 + lane) * 4) =
+              make_float4(acc[0], acc[1], acc[2], acc[3]);
+          __threadfence();
+        }
+        named_bar(1, kConsumers);
+        const int64_t first = m.item0 + rb * m.KC, last = first + m.KC - 1;
+        const int64_t bf = owner(T, G, first), bl = owner(T, G, last);
+        if (tid == 0) {
+          int is_last = 0;
           if (!aborted) {
-#pragma unroll
-            for (int q = 0; q < kTilesPerWarp; ++q)
-              *reinterpret_cast<float4 *>(part + ((warp * kTilesPerWarp + q) * 32 + lane) * 4) =
-                  make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-            __threadfence();
+            uint32_t *cnt = p.cnt + m.rb_base + rb;
+            const uint32_t old = atomicAdd(cnt, 1u);
+            is_last = old == uint32_t(bl - bf);
+            if (is_last) *cnt = 0u;
           }
-          named_bar(1, kConsumerWarps * 32);
-          const int64_t first = m.item0 + rb * m.KC, last = first + m.KC - 1;
-          const int64_t bf = owner(P.items, G, first), bl = owner(P.items, G, last);
-          if (tid == 0) {
-            int is_last = 0;
-            if (!aborted) {
-              uint32_t *cnt = p.cnt + m.rb_base + rb;
-              const uint32_t old = atomicAdd(cnt, 1u);
-              is_last = old == uint32_t(bl - bf);
-              if (is_last) *cnt = 0u;
-            }
-            sflag[1] = is_last;
+          sflag[1] = is_last;
+        }
+        named_bar(1, kConsumers);
+        write_out = sflag[1] != 0;
+        named_bar(1, kConsumers);
+        if (write_out) {
+          __threadfence();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+          for (int64_t bb = bf; bb <= bl; ++bb) {
+            const int64_t ss = 2 * bb + (item_begin(T, G, bb) >= first ? 0 : 1);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                p.partials + ss * kPartialFloats + (warp * 32 + lane) * 4));
+            acc[0] += v.x;
+            acc[1] += v.y;
+            acc[2] += v.z;
+            acc[3] += v.w;
           }
-          named_bar(1, kConsumerWarps * 32);
-          write_out = sflag[1] != 0;
-          named_bar(1, kConsumerWarps * 32);
-          if (write_out) {
-            __threadfence();
+        }
+      }
+      if (write_out) {
+        if (!aborted && mt < m.MT) {
 #pragma unroll
-            for (int q = 0; q < kTilesPerWarp; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-            for (int64_t bb = bf; bb <= bl; ++bb) {
-              const int64_t sslot = 2 * bb + (item_begin(P.items, G, bb) >= first ? 0 : 1);
-              const float *src = p.partials + sslot * kPartialFloats;
+          for (int h = 0; h < 2; ++h) {
+            const int64_t row = mt * kTileRows + g + 8 * h;
+            if (row >= m.M) continue;
+            const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
 #pragma unroll
-              for (int q = 0; q < kTilesPerWarp; ++q) {
-                const float4 v =
-                    __ldcg(reinterpret_cast<const float4 *>(src + ((warp * kTilesPerWarp + q) * 32 + lane) * 4));
-                acc[q][0] += v.x;
-                acc[q][1] += v.y;
-                acc[q][2] += v.z;
-                acc[q][3] += v.w;
+            for (int e = 0; e < 2; ++e) {
+              const int nn = 2 * t + e;
+              if (nn < N) {
+                const __nv_bfloat16 v = __float2bfloat16_rn(acc[2 * h + e] * mult);
+                m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
               }
             }
           }
         }
-        if (write_out) {
-          if (!aborted) {
-#pragma unroll
-            for (int q = 0; q < kTilesPerWarp; ++q) {
-              const int64_t mt = mt0 + q;
-              if (mt >= m.MT) continue;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int64_t row = mt * kTileRows + g + 8 * h;
-                if (row >= m.M) continue;
-                const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int n = 2 * t + e;
-                  if (n < N) {
-                    const __nv_bfloat16 v = __float2bfloat16_rn(acc[q][2 * h + e] * mult);
-                    m.y[int64_t(n) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
-                  }
-                }
-              }
-            }
-          }
-          if (p.done) {
-            __threadfence();
-            named_bar(1, kConsumerWarps * 32);
-            if (tid == 0 && !aborted && ph != p.hold_phase) atomicAdd(p.done + ph, 1u);
-          }
+        if (p.done) {
+          __threadfence();
+          named_bar(1, kConsumers);
+          if (tid == 0 && !aborted && ph != p.hold_phase) atomicAdd(p.done + ph, 1u);
         }
       }
     }
+    cons.advance();
   }
+
+  // Never leave the block while a bulk copy may still be writing shared
+  // memory: wait (bounded) for every slot issued but not consumed.
+  for (int64_t k = n; k < issued; ++k)
+    mbar_wait(bar0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u,
+              globaltimer() + p.timeout_ns);
 
   // The last block out resets the per-phase completion counters.
   __syncthreads();
@@ -474,6 +593,8 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   p.hold_phase = -1;
   p.grid = grid;
   p.timeout_ns = 2000000000ull;
+  p.m8 = 8;
+  p.m64 = 64;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p.error = reinterpret_cast<int *>(ws);
   p.cnt = reinterpret_cast<uint32_t *>(ws + kWsHead);
@@ -660,6 +781,8 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   p.hold_phase = hold_phase;
   p.grid = grid;
   p.timeout_ns = o.wait_timeout_ns > 0 ? uint64_t(o.wait_timeout_ns) : 2000000000ull;
+  p.m8 = 8;
+  p.m64 = 64;
   p.error = reinterpret_cast<int *>(plan->d_state);
   p.cnt = reinterpret_cast<uint32_t *>(plan->d_state + head);
   p.done = reinterpret_cast<uint32_t *>(plan->d_state + head + cnt_bytes);

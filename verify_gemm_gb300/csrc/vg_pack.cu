@@ -143,10 +143,11 @@ __global__ void nv_pack_kernel(const float *__restrict__ W, Geom G, float gs,
         words[kk >> 2] |= nv_place(c, ri, kk & 3);
       }
     }
-    sc_out[(mt * G.KC + u / kNvChunkUnits) * kNvScaleChunkBytes + lane * 8 +
+    sc_out[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC) + lane * kNvScaleLaneBytes +
            (u % kNvChunkUnits) * 2 + ri] = uint8_t(scale_code_from_e4m3(code));
   }
-  *reinterpret_cast<uint4 *>(w_out + (mt * G.KU + u) * kNvUnitBytes + lane * 16) =
+  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes) +
+                             lane * 16) =
       make_uint4(words[0], words[1], words[2], words[3]);
 }
 
@@ -159,7 +160,8 @@ __global__ void nv_unpack_kernel(const uint8_t *__restrict__ w, const uint8_t *_
   const int g = lane >> 2, t = lane & 3;
   const int64_t k0 = u * kUnitK + 16 * t;
   if (k0 >= G.K) return;
-  const uint4 v = *reinterpret_cast<const uint4 *>(w + (mt * G.KU + u) * kNvUnitBytes + lane * 16);
+  const uint4 v = *reinterpret_cast<const uint4 *>(
+      w + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes) + lane * 16);
   const uint32_t words[4] = {v.x, v.y, v.z, v.w};
   for (int ri = 0; ri < 2; ++ri) {
     const int64_t row = mt * kTileRows + g + 8 * ri;
@@ -174,7 +176,7 @@ __global__ void nv_unpack_kernel(const uint8_t *__restrict__ w, const uint8_t *_
         hi |= c << (4 * (kk - 8));
     }
     *reinterpret_cast<uint2 *>(nib + row * (G.K / 2) + k0 / 2) = make_uint2(lo, hi);
-    const uint8_t d = sc[(mt * G.KC + u / kNvChunkUnits) * kNvScaleChunkBytes + lane * 8 +
+    const uint8_t d = sc[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC) + lane * kNvScaleLaneBytes +
                          (u % kNvChunkUnits) * 2 + ri];
     scc[row * (G.K / 16) + k0 / 16] = uint8_t(e4m3_from_scale_code(d));
   }
@@ -217,10 +219,11 @@ __global__ void nv_from_canonical_kernel(const uint8_t *__restrict__ nib,
         }
       }
     }
-    sc_out[(mt * G.KC + u / kNvChunkUnits) * kNvScaleChunkBytes + lane * 8 +
+    sc_out[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC) + lane * kNvScaleLaneBytes +
            (u % kNvChunkUnits) * 2 + ri] = uint8_t(scale_code_from_e4m3(code));
   }
-  *reinterpret_cast<uint4 *>(w_out + (mt * G.KU + u) * kNvUnitBytes + lane * 16) =
+  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes) +
+                             lane * 16) =
       make_uint4(words[0], words[1], words[2], words[3]);
 }
 
@@ -248,7 +251,8 @@ __global__ void f8_pack_kernel(const float *__restrict__ W, const float *__restr
       out[f8_byte(ri, kk >> 2, kk & 3)] = uint8_t(c);
     }
   }
-  uint4 *dst = reinterpret_cast<uint4 *>(w_out + (mt * G.KU + u) * kF8UnitBytes + lane * 32);
+  uint4 *dst = reinterpret_cast<uint4 *>(
+      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes) + lane * 32);
   dst[0] = *reinterpret_cast<const uint4 *>(out);
   dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
 }
@@ -262,7 +266,8 @@ __global__ void f8_unpack_kernel(const uint8_t *__restrict__ w, Geom G, uint8_t 
   const int64_t k0 = u * kUnitK + 16 * t;
   if (k0 >= G.K) return;
   uint8_t in[32];
-  const uint4 *src = reinterpret_cast<const uint4 *>(w + (mt * G.KU + u) * kF8UnitBytes + lane * 32);
+  const uint4 *src = reinterpret_cast<const uint4 *>(
+      w + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes) + lane * 32);
   *reinterpret_cast<uint4 *>(in) = src[0];
   *reinterpret_cast<uint4 *>(in + 16) = src[1];
   for (int ri = 0; ri < 2; ++ri) {
@@ -303,7 +308,8 @@ __global__ void f8_from_canonical_kernel(const uint8_t *__restrict__ q, Geom G,
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) out[f8_byte(ri, kk >> 2, kk & 3)] = in[kk];
   }
-  uint4 *dst = reinterpret_cast<uint4 *>(w_out + (mt * G.KU + u) * kF8UnitBytes + lane * 32);
+  uint4 *dst = reinterpret_cast<uint4 *>(
+      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes) + lane * 32);
   dst[0] = *reinterpret_cast<const uint4 *>(out);
   dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
 }
