@@ -51,7 +51,9 @@ struct MatDev {
   uint16_t *y;
   float mult;        // epilogue multiplier (NVFP4: 256 * gscale)
   int fmt;
-  int64_t M, K, MT, KU, KC, RB;
+  int M, K, MT, KU, KC, RB;
+  int cu, ub;        // units per chunk, bytes per unit
+  int64_t rb_bytes;  // code bytes of a full row block (16 tiles x KU units)
   int64_t item0;     // first item of this matrix within its phase
   int64_t rb_base;   // first arrival counter of this matrix
 };
@@ -83,9 +85,11 @@ struct Params {
 
 constexpr int kPartialFloats = kBlockTiles * 32 * 4;   // one slot
 constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;
-constexpr int kSmemBytes = kRingBytes + kWarps * kSlots * 8 + 64;
-constexpr int kErrFullWait = 1, kErrDepWait = 3;
+constexpr int kBarBytes = 2 * kWarps * kSlots * 8;
+constexpr int kSmemBytes = kRingBytes + kBarBytes + 64;
 constexpr int kConsumers = kWarps * 32;
+constexpr int kKernelThreads = kConsumers + 32;        // + one producer warp
+constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3;
 
 __host__ __device__ inline int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -98,6 +102,12 @@ __device__ inline int64_t owner(int64_t T, int64_t G, int64_t i) { return ((i + 
 
 __device__ inline void set_error(int *error, int code) { atomicCAS(error, 0, code); }
 
+// Bounded wait with the clock read only after a first miss.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t timeout) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity, globaltimer() + timeout);
+}
+
 // The items one thread block processes, in order, across all phases: for
 // each phase with items for this block, its contiguous range [i0, i1).  The
 // position inside the current matrix (row block rb, chunk c) advances
@@ -106,8 +116,8 @@ struct Seq {
   const MatDev *mats;
   const PhaseDev *phases;
   int nphases, ph, mi, mend;
+  int rb, c, KC, RB;
   int64_t b, grid, G, i, i0, i1, items;
-  int64_t rb, c, KC, RB;
   bool valid;
 
   __device__ void init(const MatDev *m, const PhaseDev *p, int np, int64_t blk, int64_t g) {
@@ -129,12 +139,12 @@ struct Seq {
         i = i0;
         mi = phases[ph].mat_begin;
         mend = phases[ph].mat_end;
-        while (mi + 1 < mend && i >= mats[mi].item0 + mats[mi].RB * mats[mi].KC) ++mi;
+        while (mi + 1 < mend && i >= mats[mi].item0 + int64_t(mats[mi].RB) * mats[mi].KC) ++mi;
         KC = mats[mi].KC;
         RB = mats[mi].RB;
         const int64_t rel = i - mats[mi].item0;
-        rb = rel / KC;
-        c = rel - rb * KC;
+        rb = int(rel / KC);
+        c = int(rel - int64_t(rb) * KC);
         valid = true;
         return;
       }
@@ -157,31 +167,6 @@ struct Seq {
     }
   }
 };
-
-// Issue the bulk copies of this warp's tile of the item at `q` into ring
-// slot `slot_addr` (lane 0 only).  A tile past the matrix arrives with no
-// bytes.  Offsets follow the item-contiguous packed order.
-__device__ __forceinline__ void issue_tile(const Seq &q, int warp, uint32_t slot_addr,
-                                           uint32_t bar, uint64_t policy) {
-  const MatDev &m = q.mats[q.mi];
-  const int64_t tiles = i64min(kBlockTiles, m.MT - q.rb * kBlockTiles);
-  if (warp >= tiles) {
-    mbar_arrive_expect_tx(bar, 0);
-    return;
-  }
-  const bool nv = m.fmt == VG_FMT_NVFP4;
-  const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
-  const int64_t ub = nv ? kNvUnitBytes : kF8UnitBytes;
-  const int64_t nu = i64min(cu, m.KU - q.c * cu);
-  const uint32_t code_bytes = uint32_t(nu * ub);
-  const int64_t off = q.rb * kBlockTiles * m.KU * ub + q.c * tiles * cu * ub + warp * nu * ub;
-  mbar_arrive_expect_tx(bar, code_bytes + (nv ? kNvScaleChunkBytes : 0));
-  bulk_g2s(slot_addr, m.w + off, code_bytes, bar, policy);
-  if (nv) {
-    const int64_t soff = (q.rb * kBlockTiles * m.KC + q.c * tiles + warp) * kNvScaleChunkBytes;
-    bulk_g2s(slot_addr + kSlotCodeBytes, m.sc + soff, kNvScaleChunkBytes, bar, policy);
-  }
-}
 
 // One NVFP4 unit of one tile: 4 MMAs (k16 steps) into two accumulators.
 __device__ __forceinline__ void nv_unit(const uint4 wv, uint32_t fg, uint32_t fg8, const uint4 xa,
@@ -266,7 +251,7 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, const uin
 
 // A partial NVFP4 chunk (the K tail): nu units, columns checked against K.
 __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uint16_t *xp,
-                                              bool on, int nu, int64_t kleft, uint32_t m8,
+                                              bool on, int nu, int kleft, uint32_t m8,
                                               uint32_t m64, float (&acc0)[4],
                                               float (&acc1)[4]) {
   const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
@@ -281,9 +266,9 @@ __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uin
   }
 }
 
-// An FP8 chunk: nu (<= 4) units of 1024 bytes, two at a time.
+// An FP8 chunk: nu (<= 4) units of 1024 bytes.
 __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t *xp, bool on,
-                                         int nu, int64_t kleft, float (&acc0)[4],
+                                         int nu, int kleft, float (&acc0)[4],
                                          float (&acc1)[4]) {
 #pragma unroll
   for (int u = 0; u < kF8ChunkUnits; ++u) {
@@ -297,206 +282,254 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
+// Producer lane `tile` (0..15): refill consumer warp `tile`'s ring, one item
+// at a time, as soon as that warp has released the slot.
+__device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases, int tile,
+                         uint32_t ring, uint32_t full0, uint32_t empty0) {
+  const uint64_t policy = policy_evict_first();
+  Seq q;
+  q.init(mats, phases, p.nphases, blockIdx.x, p.grid);
+  int s = 0;
+  uint32_t par = 0;
+  int64_t issued = 0;
+  while (q.valid) {
+    if (!mbar_wait_for(empty0 + 8 * s, par ^ 1u, p.timeout_ns)) {
+      set_error(p.error, kErrEmptyWait);
+      break;
+    }
+    const MatDev &m = mats[q.mi];
+    const uint32_t full = full0 + 8 * s;
+    const int tiles = min(kBlockTiles, m.MT - q.rb * kBlockTiles);
+    if (tile >= tiles) {
+      mbar_arrive_expect_tx(full, 0);
+    } else {
+      const int nu = min(m.cu, m.KU - q.c * m.cu);
+      const uint32_t code_bytes = uint32_t(nu * m.ub);
+      const int64_t off = int64_t(q.rb) * m.rb_bytes + int64_t(q.c) * tiles * m.cu * m.ub +
+                          int64_t(tile) * nu * m.ub;
+      const uint32_t slot = ring + s * kSlotBytes;
+      if (m.fmt == VG_FMT_NVFP4) {
+        mbar_arrive_expect_tx(full, code_bytes + kNvScaleChunkBytes);
+        bulk_g2s(slot, m.w + off, code_bytes, full, policy);
+        const int64_t soff =
+            (int64_t(q.rb) * kBlockTiles * m.KC + int64_t(q.c) * tiles + tile) * kNvScaleChunkBytes;
+        bulk_g2s(slot + kSlotCodeBytes, m.sc + soff, kNvScaleChunkBytes, full, policy);
+      } else {
+        mbar_arrive_expect_tx(full, code_bytes);
+        bulk_g2s(slot, m.w + off, code_bytes, full, policy);
+      }
+    }
+    q.advance();
+    ++issued;
+    if (++s == kSlots) {
+      s = 0;
+      par ^= 1u;
+    }
+  }
+  // Never leave while a bulk copy may still be writing shared memory.
+  for (int64_t k = i64max(0, issued - kSlots); k < issued; ++k)
+    mbar_wait_for(full0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u, p.timeout_ns);
+}
+
+__global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
-  volatile int *sflag = reinterpret_cast<volatile int *>(bars + kWarps * kSlots);
+  volatile int *sflag = reinterpret_cast<volatile int *>(smem + kRingBytes + kBarBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int N = p.N;
   const MatDev *mats = p.mats ? p.mats : &p.mat0;
   const PhaseDev *phases = p.mats ? p.phases : &p.phase0;
-  const uint32_t ring = smem_addr(smem + warp * kSlots * kSlotBytes);
-  const uint32_t bar0 = smem_addr(bars + warp * kSlots);
 
-  if (lane == 0) {
-    for (int s = 0; s < kSlots; ++s) mbar_init(bar0 + 8 * s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (tid < kWarps * kSlots) {
+    mbar_init(smem_addr(bars + tid), 1);                       // full
+    mbar_init(smem_addr(bars + kWarps * kSlots + tid), 1);     // empty
   }
   if (tid == 0) {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sflag[0] = 0;
     sflag[1] = 0;
   }
   __syncthreads();
 
-  const uint64_t policy = policy_evict_first();
-  Seq cons, pref;
-  cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
-  pref = cons;
-  // Prologue: fill the ring.
-  int64_t issued = 0;
-  for (int q = 0; q < kSlots && pref.valid; ++q, ++issued) {
-    if (lane == 0) issue_tile(pref, warp, ring + q * kSlotBytes, bar0 + 8 * q, policy);
-    pref.advance();
-  }
-
-  bool aborted = false;
-  int64_t n = 0;                 // items consumed
-  int s = 0;                     // ring slot of item n
-  uint32_t par = 0;              // parity of that slot's current phase
-  int cur_ph = -1;
-  int64_t piece_start = 0, piece_c0 = 0;
-  float acc0[4], acc1[4];
-  while (cons.valid) {
-    const int ph = cons.ph;
-    // ---------------------------------------- ordered: wait for group ph-1
-    if (ph != cur_ph) {
-      if (p.ordered && ph > 0) {
-        if (tid == 0) {
-          int ok = 1;
-          if (!aborted) {
-            const volatile uint32_t *d = p.done + (ph - 1);
-            const uint32_t target = uint32_t(phases[ph - 1].rbs);
-            const uint64_t deadline = globaltimer() + p.timeout_ns;
-            while (*d < target) {
-              if (globaltimer() > deadline) {
-                ok = 0;
-                set_error(p.error, kErrDepWait);
-                break;
+  if (warp == kWarps) {
+    // ================================================================ producer
+    if (lane < kBlockTiles)
+      producer(p, mats, phases, lane, smem_addr(smem + lane * kSlots * kSlotBytes),
+               smem_addr(bars + lane * kSlots), smem_addr(bars + kWarps * kSlots + lane * kSlots));
+  } else {
+    // =============================================================== consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int N = p.N;
+    const bool on = g < N;
+    const uint32_t ring = smem_addr(smem + warp * kSlots * kSlotBytes);
+    const uint32_t full0 = smem_addr(bars + warp * kSlots);
+    const uint32_t empty0 = smem_addr(bars + kWarps * kSlots + warp * kSlots);
+    Seq cons;
+    cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
+    bool aborted = false;
+    int s = 0;                     // ring slot of the current item
+    uint32_t par = 0;              // parity of that slot's current phase
+    int cur_ph = -1, cur_mi = -1;
+    int64_t piece_start = 0;
+    int piece_c0 = 0;
+    float acc0[4], acc1[4];
+    // matrix fields cached while the matrix does not change
+    const uint16_t *xbase = nullptr;
+    int K = 0, KU = 0, MT = 0, fmt = 0;
+    while (cons.valid) {
+      const int ph = cons.ph;
+      // -------------------------------------- ordered: wait for group ph-1
+      if (ph != cur_ph) {
+        if (p.ordered && ph > 0) {
+          if (tid == 0) {
+            int ok = 1;
+            if (!aborted) {
+              const volatile uint32_t *d = p.done + (ph - 1);
+              const uint32_t target = uint32_t(phases[ph - 1].rbs);
+              const uint64_t deadline = globaltimer() + p.timeout_ns;
+              while (*d < target) {
+                if (globaltimer() > deadline) {
+                  ok = 0;
+                  set_error(p.error, kErrDepWait);
+                  break;
+                }
+                __nanosleep(32);
               }
-              __nanosleep(64);
+              __threadfence();
             }
-            __threadfence();
+            sflag[0] = ok ? 0 : 1;
           }
-          sflag[0] = ok ? 0 : 1;
-        }
-        named_bar(1, kConsumers);
-        if (sflag[0]) aborted = true;
-        named_bar(1, kConsumers);
-      }
-      cur_ph = ph;
-    }
-    const MatDev &m = mats[cons.mi];
-    const int64_t rb = cons.rb, c = cons.c;
-    if (c == 0 || cons.i == cons.i0) {
-      piece_start = cons.i;
-      piece_c0 = c;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
-    }
-    const uint32_t slot = ring + s * kSlotBytes;
-    const int64_t mt = rb * kBlockTiles + warp;
-    if (!aborted && !mbar_wait(bar0 + 8 * s, par, globaltimer() + p.timeout_ns)) {
-      if (lane == 0) set_error(p.error, kErrFullWait);
-      aborted = true;
-    }
-    if (!aborted && mt < m.MT) {
-      const bool nv = m.fmt == VG_FMT_NVFP4;
-      const int64_t cu = nv ? kNvChunkUnits : kF8ChunkUnits;
-      // lane's x columns of this chunk: x[g][c*cu*64 + 16t ...]
-      const int64_t kc = c * cu * kUnitK;
-      const uint16_t *xp = m.x + int64_t(g) * m.K + kc + 16 * t;
-      const int64_t kleft = m.K - kc - 16 * t;       // columns left for this lane
-      const bool on = g < N;
-      if (nv) {
-        // warp-uniform test (mma.sync needs the whole warp): the chunk's whole
-        // column range lies inside K
-        if ((c * cu + cu) * kUnitK <= m.K)
-          nv_chunk_full(slot, lane, xp, on, p.m8, p.m64, acc0, acc1);
-        else
-          nv_chunk_tail(slot, lane, xp, on, int(i64min(cu, m.KU - c * cu)), kleft, p.m8,
-                        p.m64, acc0, acc1);
-      } else {
-        f8_chunk(slot, lane, xp, on, int(i64min(cu, m.KU - c * cu)), kleft, acc0, acc1);
-      }
-    }
-    // Refill this slot with the item kSlots ahead (after every lane has
-    // finished reading it).
-    __syncwarp();
-    if (pref.valid) {
-      if (lane == 0) {
-        fence_proxy_async();
-        issue_tile(pref, warp, slot, bar0 + 8 * s, policy);
-      }
-      pref.advance();
-      ++issued;
-    }
-    ++n;
-    if (++s == kSlots) {
-      s = 0;
-      par ^= 1u;
-    }
-
-    // ------------------------------------------------ end of a row-block piece
-    const bool piece_end = c == m.KC - 1 || cons.i == cons.i1 - 1;
-    if (piece_end) {
-      const int64_t T = cons.items, G = cons.G, i0 = cons.i0;
-      const bool full_piece = piece_c0 == 0 && c == m.KC - 1;
-      float acc[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] = acc0[e] + acc1[e];
-      bool write_out = true;
-      if (!full_piece) {
-        const int slotp = int(2 * blockIdx.x + (piece_start == i0 ? 0 : 1));
-        float *part = p.partials + int64_t(slotp) * kPartialFloats;
-        if (!aborted) {
-          *reinterpret_cast<float4 *>(part + (warp * 32 + lane) * 4) =
-              make_float4(acc[0], acc[1], acc[2], acc[3]);
-          __threadfence();
-        }
-        named_bar(1, kConsumers);
-        const int64_t first = m.item0 + rb * m.KC, last = first + m.KC - 1;
-        const int64_t bf = owner(T, G, first), bl = owner(T, G, last);
-        if (tid == 0) {
-          int is_last = 0;
-          if (!aborted) {
-            uint32_t *cnt = p.cnt + m.rb_base + rb;
-            const uint32_t old = atomicAdd(cnt, 1u);
-            is_last = old == uint32_t(bl - bf);
-            if (is_last) *cnt = 0u;
-          }
-          sflag[1] = is_last;
-        }
-        named_bar(1, kConsumers);
-        write_out = sflag[1] != 0;
-        named_bar(1, kConsumers);
-        if (write_out) {
-          __threadfence();
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[e] = 0.f;
-          for (int64_t bb = bf; bb <= bl; ++bb) {
-            const int64_t ss = 2 * bb + (item_begin(T, G, bb) >= first ? 0 : 1);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                p.partials + ss * kPartialFloats + (warp * 32 + lane) * 4));
-            acc[0] += v.x;
-            acc[1] += v.y;
-            acc[2] += v.z;
-            acc[3] += v.w;
-          }
-        }
-      }
-      if (write_out) {
-        if (!aborted && mt < m.MT) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t row = mt * kTileRows + g + 8 * h;
-            if (row >= m.M) continue;
-            const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int nn = 2 * t + e;
-              if (nn < N) {
-                const __nv_bfloat16 v = __float2bfloat16_rn(acc[2 * h + e] * mult);
-                m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
-              }
-            }
-          }
-        }
-        if (p.done) {
-          __threadfence();
           named_bar(1, kConsumers);
-          if (tid == 0 && !aborted && ph != p.hold_phase) atomicAdd(p.done + ph, 1u);
+          if (sflag[0]) aborted = true;
+          named_bar(1, kConsumers);
+        }
+        cur_ph = ph;
+      }
+      if (cons.mi != cur_mi) {
+        const MatDev &mm = mats[cons.mi];
+        cur_mi = cons.mi;
+        K = mm.K;
+        KU = mm.KU;
+        MT = mm.MT;
+        fmt = mm.fmt;
+        xbase = mm.x + int64_t(g) * K + 16 * t;
+      }
+      const int rb = cons.rb, c = cons.c;
+      if (c == 0 || cons.i == cons.i0) {
+        piece_start = cons.i;
+        piece_c0 = c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+      }
+      const uint32_t slot = ring + s * kSlotBytes;
+      const int mt = rb * kBlockTiles + warp;
+      if (!aborted && !mbar_wait_for(full0 + 8 * s, par, p.timeout_ns)) {
+        if (lane == 0) set_error(p.error, kErrFullWait);
+        aborted = true;
+      }
+      if (!aborted && mt < MT) {
+        if (fmt == VG_FMT_NVFP4) {
+          const int kc = c * (kNvChunkUnits * kUnitK);
+          // warp-uniform test (mma.sync needs the whole warp): the chunk's
+          // whole column range lies inside K
+          if (kc + kNvChunkUnits * kUnitK <= K)
+            nv_chunk_full(slot, lane, xbase + kc, on, p.m8, p.m64, acc0, acc1);
+          else
+            nv_chunk_tail(slot, lane, xbase + kc, on, min(kNvChunkUnits, KU - c * kNvChunkUnits),
+                          K - kc - 16 * t, p.m8, p.m64, acc0, acc1);
+        } else {
+          const int kc = c * (kF8ChunkUnits * kUnitK);
+          f8_chunk(slot, lane, xbase + kc, on, min(kF8ChunkUnits, KU - c * kF8ChunkUnits),
+                   K - kc - 16 * t, acc0, acc1);
         }
       }
-    }
-    cons.advance();
-  }
+      // release the slot to the producer (every lane has read it)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (++s == kSlots) {
+        s = 0;
+        par ^= 1u;
+      }
 
-  // Never leave the block while a bulk copy may still be writing shared
-  // memory: wait (bounded) for every slot issued but not consumed.
-  for (int64_t k = n; k < issued; ++k)
-    mbar_wait(bar0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u,
-              globaltimer() + p.timeout_ns);
+      // ---------------------------------------------- end of a row-block piece
+      const bool piece_end = c == cons.KC - 1 || cons.i == cons.i1 - 1;
+      if (piece_end) {
+        const MatDev &m = mats[cons.mi];
+        const int64_t T = cons.items, G = cons.G, i0 = cons.i0;
+        const bool full_piece = piece_c0 == 0 && c == m.KC - 1;
+        float acc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = acc0[e] + acc1[e];
+        bool write_out = true;
+        if (!full_piece) {
+          // partial sums: stash, count arrivals, the last arrival reduces
+          const int slotp = int(2 * blockIdx.x + (piece_start == i0 ? 0 : 1));
+          float *part = p.partials + int64_t(slotp) * kPartialFloats;
+          if (!aborted)
+            *reinterpret_cast<float4 *>(part + (warp * 32 + lane) * 4) =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+          named_bar(1, kConsumers);
+          const int64_t first = m.item0 + int64_t(rb) * m.KC, last = first + m.KC - 1;
+          const int64_t bf = owner(T, G, first), bl = owner(T, G, last);
+          if (tid == 0) {
+            int is_last = 0;
+            if (!aborted) {
+              __threadfence();       // publish this block's partials (cumulative)
+              uint32_t *cnt = p.cnt + m.rb_base + rb;
+              const uint32_t old = atomicAdd(cnt, 1u);
+              is_last = old == uint32_t(bl - bf);
+              if (is_last) {
+                *cnt = 0u;
+                __threadfence();     // acquire the other blocks' partials
+              }
+            }
+            sflag[1] = is_last;
+          }
+          named_bar(1, kConsumers);
+          write_out = sflag[1] != 0;
+          named_bar(1, kConsumers);
+          if (write_out) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+            for (int64_t bb = bf; bb <= bl; ++bb) {
+              const int64_t ss = 2 * bb + (item_begin(T, G, bb) >= first ? 0 : 1);
+              const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                  p.partials + ss * kPartialFloats + (warp * 32 + lane) * 4));
+              acc[0] += v.x;
+              acc[1] += v.y;
+              acc[2] += v.z;
+              acc[3] += v.w;
+            }
+          }
+        }
+        if (write_out) {
+          if (!aborted && mt < m.MT) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = mt * kTileRows + g + 8 * h;
+              if (row >= m.M) continue;
+              const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int nn = 2 * t + e;
+                if (nn < N) {
+                  const __nv_bfloat16 v = __float2bfloat16_rn(acc[2 * h + e] * mult);
+                  m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
+                }
+              }
+            }
+          }
+          if (p.done) {
+            named_bar(1, kConsumers);
+            if (tid == 0 && !aborted && ph != p.hold_phase) {
+              __threadfence();       // publish the row block's y (cumulative)
+              atomicAdd(p.done + ph, 1u);
+            }
+          }
+        }
+      }
+      cons.advance();
+    }
+  }
 
   // The last block out resets the per-phase completion counters.
   __syncthreads();
@@ -556,17 +589,21 @@ MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, co
   m.y = y;
   m.fmt = fmt;
   m.mult = fmt == VG_FMT_NVFP4 ? kNvEpilogueScale * gscale : 1.0f;
-  m.M = M;
-  m.K = K;
-  m.MT = ceil_div(M, kTileRows);
-  m.KU = ceil_div(K, kUnitK);
-  m.KC = ceil_div(m.KU, fmt == VG_FMT_NVFP4 ? kNvChunkUnits : kF8ChunkUnits);
-  m.RB = ceil_div(m.MT, kBlockTiles);
+  m.M = int(M);
+  m.K = int(K);
+  m.MT = int(ceil_div(M, kTileRows));
+  m.KU = int(ceil_div(K, kUnitK));
+  m.cu = fmt == VG_FMT_NVFP4 ? kNvChunkUnits : kF8ChunkUnits;
+  m.ub = fmt == VG_FMT_NVFP4 ? kNvUnitBytes : kF8UnitBytes;
+  m.KC = int(ceil_div(m.KU, m.cu));
+  m.RB = int(ceil_div(m.MT, kBlockTiles));
+  m.rb_bytes = int64_t(kBlockTiles) * m.KU * m.ub;
   return m;
 }
 
 int64_t algorithmic_bytes(const MatDev &m) {
-  return m.fmt == VG_FMT_NVFP4 ? m.M * m.K / 2 + m.M * m.K / 16 + 4 : m.M * m.K + 4 * m.M;
+  const int64_t E = int64_t(m.M) * m.K;
+  return m.fmt == VG_FMT_NVFP4 ? E / 2 + E / 16 + 4 : E + 4 * int64_t(m.M);
 }
 
 // Single-GEMV workspace: [error word | counters | partial slots].
@@ -581,7 +618,7 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   int dev;
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
-  const int64_t T = m0.RB * m0.KC;
+  const int64_t T = int64_t(m0.RB) * m0.KC;
   const int grid = int(i64min(di->sms, T));
   if (!workspace || workspace_bytes < ws_bytes(m0.RB, grid)) return VG_ERR_WORKSPACE;
   if (!aligned16(workspace)) return VG_ERR_ALIGNMENT;
@@ -604,7 +641,7 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   p.phase0.rbs = m0.RB;
   p.phase0.mat_begin = 0;
   p.phase0.mat_end = 1;
-  stream_kernel<<<grid, kThreads, kSmemBytes, as_cuda(stream)>>>(p);
+  stream_kernel<<<grid, kKernelThreads, kSmemBytes, as_cuda(stream)>>>(p);
   VG_LAUNCH_CHECK();
   return VG_OK;
 }
@@ -635,7 +672,7 @@ extern "C" vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, si
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
   const MatDev m = make_mat(format, M, K, nullptr, nullptr, nullptr, 0.f, nullptr, nullptr);
-  const int grid = int(i64min(di->sms, m.RB * m.KC));
+  const int grid = int(i64min(di->sms, int64_t(m.RB) * m.KC));
   *bytes = ws_bytes(m.RB, grid);
   return VG_OK;
 }
@@ -733,7 +770,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
     PhaseDev &ph = hp.back();
     hm[i].item0 = ph.items;
     hm[i].rb_base = rb_total;
-    ph.items += hm[i].RB * hm[i].KC;
+    ph.items += int64_t(hm[i].RB) * hm[i].KC;
     ph.rbs += hm[i].RB;
     ph.mat_end = i + 1;
     rb_total += hm[i].RB;
@@ -742,7 +779,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   int grid = di->sms;
   if (o.max_ctas > 0) grid = std::min(grid, int(o.max_ctas));
   int per_sm = 0;
-  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel, kThreads, kSmemBytes));
+  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel, kKernelThreads, kSmemBytes));
   if (per_sm < 1) return VG_ERR_UNSUPPORTED;
   grid = std::min(grid, per_sm * di->sms);
 
@@ -812,7 +849,7 @@ extern "C" vg_status vg_verify_pass(vg_verify_plan *plan, vg_stream_t stream) {
   if (dev != plan->dev) return VG_ERR_INVALID_ARG;
   void *args[] = {&plan->params};
   VG_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(stream_kernel),
-                                      dim3(plan->grid), dim3(kThreads), args, kSmemBytes,
+                                      dim3(plan->grid), dim3(kKernelThreads), args, kSmemBytes,
                                       as_cuda(stream)));
   return VG_OK;
 }

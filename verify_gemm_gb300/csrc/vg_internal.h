@@ -22,7 +22,8 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;
 
 inline vg_status check_mk(int64_t M, int64_t K) {
   if (M < 1 || K < 16 || K % 16 != 0) return VG_ERR_INVALID_ARG;
-  if (M > kMaxElems / K) return VG_ERR_UNSUPPORTED;
+  if (M > kMaxElems / K || M >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return VG_ERR_UNSUPPORTED;
   return VG_OK;
 }
 
