@@ -427,9 +427,8 @@ def run_probe(args, local):
     sink = torch.zeros(8192, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
     out = {}
-    configs = [(1, 12288, 1), (0, 0, 0), (1, 2048, 6), (1, 4096, 3), (1, 2048, 4),
-               (1, 1024, 12), (1, 2048, 2), (1, 4096, 2), (1, 8192, 1), (1, 12288, 1),
-               (0, 0, 0), (1, 2048, 6)]
+    configs = [(1, 12288, 1), (0, 0, 0), (1, 4096, 2), (2, 4096, 3), (2, 4096, 2),
+               (2, 8192, 1), (3, 4096, 2), (3, 2048, 4), (3, 8192, 1), (2, 12288, 1)]
     for mode, chunk, slots in configs:
         ms = []
         for i in range(args.warmup + args.steps):
@@ -443,7 +442,9 @@ def run_probe(args, local):
             torch.cuda.synchronize()
             if i >= args.warmup:
                 ms.append(a.elapsed_time(b))
-        key = "ldg128" if mode == 0 else f"bulk {chunk}B x{slots} slots/warp"
+        key = "ldg128" if mode == 0 else \
+            f"bulk {chunk}B x{slots} slots/warp, " + \
+            {1: "interleaved", 2: "per-block ranges", 3: "per-block ranges + 1/8 side copy"}[mode]
         out.setdefault(key, []).append(round(nbytes / (statistics.median(ms) / 1e3) / 1e9, 1))
     peak, kind = peaks()
     print(json.dumps({"metric": "read-only HBM probe GB/s", "unit": "GB/s", "bytes": nbytes,

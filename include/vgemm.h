@@ -158,16 +158,22 @@ vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t K, void *w_
 /* ------------------------------------------------------------ the GEMV */
 
 /* Workspace bytes that vg_gemv_nvfp4 / vg_gemv_fp8_rowscale need for an
- * M x K matrix on the current device (format: VG_FMT_*).  The workspace
- * holds per-row-block arrival counters, a device error word and the FP32
- * partial sums of row blocks whose K range is split between two or more
- * thread blocks.  It must be zero-filled once when allocated; every call
- * leaves the counters and the error word at zero again (the partial-sum
- * space may keep stale values, which are never read before being
- * rewritten).  Calls that share a workspace must not overlap on the GPU. */
+ * M x K matrix on the current device (format: VG_FMT_*): 256 header bytes
+ * (a device error word, a count of finished thread blocks, a pass counter)
+ * and one 16 KiB slot per thread block for the FP32 partial sums of row
+ * blocks whose K range is split between thread blocks.  Each partial sum
+ * carries a tag of the pass that wrote it, so stale slots are never mistaken
+ * for current ones.  The workspace must be zero-filled once when allocated;
+ * afterwards every call leaves it consistent for the next one (error word
+ * and block count at zero, pass counter advanced), so it is never cleared
+ * again unless vg_gemv_workspace_check reports an error.  Calls that share
+ * a workspace must not overlap on the GPU. */
 vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes);
 
 /* y[n][m] = bf16( sum_k x[n][k] * dequant(W)[m][k] ), NVFP4 weights.
+ * One cooperative launch of up to one thread block per SM (all resident at
+ * once: the block that sums a split row block waits, bounded, for the
+ * others' partial sums).
  *   w, scales   device, packed by vg_nvfp4_pack / vg_nvfp4_from_canonical.
  *   gscale      FP32 tensor scale (from the pack).
  *   x           device BF16 [N][K], row-major, 16-byte aligned.
@@ -200,8 +206,9 @@ vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale,
  *   VG_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, which every GPU
  *   that loads the library holds until the process exits.  A matrix that
  *   needs more (vg_gemv_workspace_size) gives VG_ERR_UNSUPPORTED.
- *   Nothing is allocated: the call clears the part of the array it uses with
- *   cudaMemsetAsync on `stream`, then runs the GEMV on it.  The first call
+ *   Nothing is allocated: the call clears the array's error word (4 bytes,
+ *   cudaMemsetAsync on `stream`), then runs the GEMV on it; the rest of the
+ *   array stays consistent from call to call.  The first call
  *   on a device looks up the array's device address (cudaGetSymbolAddress);
  *   make that first call before any stream capture.  All calls share the
  *   one array, so calls that overlap on the GPU (other streams, other host
@@ -223,9 +230,13 @@ vg_status vg_gemv_workspace_check(void *workspace, size_t workspace_bytes,
  * sets the verify pass against the card's read rate).  Reads `bytes` of the
  * device buffer `buf` once and folds them into `sink` (device, >= one word
  * per thread block: the SM count for mode 1, SMs x resident blocks for
- * mode 0).  mode 0: 16-byte vector loads; mode 1: per-warp rings of
- * `slots` bulk copies of `chunk` bytes (chunk a multiple of 256,
- * chunk * slots <= 12288).  Time it with events on `stream`. */
+ * mode 0).  mode 0: 16-byte vector loads; modes 1 and 2: per-warp rings
+ * of `slots` bulk copies of `chunk` bytes (chunk a multiple of 256,
+ * chunk * slots <= 12288); mode 1 interleaves chunks over the whole device,
+ * mode 2 gives each block one contiguous range (the GEMV's order), mode 3
+ * is mode 2 plus a chunk/8-byte side copy per slot from a second region
+ * (codes plus block scales; then (chunk + chunk/8) * slots <= 12288).
+ * Time it with events on `stream`. */
 vg_status vg_hbm_read_probe(const void *buf, size_t bytes, int mode, int chunk, int slots,
                             uint32_t *sink, int sink_words, vg_stream_t stream);
 
@@ -265,7 +276,10 @@ typedef struct vg_plan_options {
  * columns; Measured section: 19.26 GB read per pass).  Allocates the
  * plan's descriptor table, counters and partial-sum space once.
  * Descriptors (pointers included) are copied; buffer contents may change
- * between passes. */
+ * between passes.  Every group's x is read through the read-only data
+ * path: an x must not alias any matrix's y within the same plan (group
+ * order sequences the work; it does not forward one group's y as the
+ * next group's x). */
 vg_status vg_verify_plan_create(const vg_matrix_desc *mats, int count, int N,
                                 int ordered, vg_verify_plan **plan_out);
 vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,

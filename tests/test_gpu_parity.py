@@ -150,8 +150,35 @@ def test_gemv_nvfp4_parity(vg, orc, M, K, Ns):
         yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
         assert_close(orc, y, yref, a, f"nvfp4 {M}x{K} N={N}")
     assert vg.workspace_error(ws) == 0
-    rb = -(-(-(-M // 16)) // 16)                 # row blocks of 256 rows
-    assert not ws[256:256 + 4 * rb].any(), "arrival counters must be left at zero"
+    err, finished, epoch = ws[:12].cpu().numpy().view(np.uint32)
+    assert finished == 0, "the finished-block count must be left at zero"
+    assert epoch == len(Ns), "each call advances the pass counter once"
+
+
+def test_gemv_pass_counter_wrap(vg, orc):
+    """Split row blocks (32 items on 32 blocks, every row block summed from 8
+    blocks' tagged partials) stay exact when the pass counter that tags them
+    reaches its end: the pass then restarts the counter at 0 and clears every
+    slot, and the next pass's tags are fresh again."""
+    M, K, N = 1024, 4096, 8
+    W = rand_w(77, M, K)
+    wt = vg.nvfp4_pack(W.cuda())
+    nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+    x = rand_x(78, N, K).cuda()
+    ws = vg.workspace_for(wt)
+    y0 = vg.gemv(wt, x, workspace=ws)
+    yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x.cpu()), threads=THREADS)
+    assert_close(orc, y0, yref, a, "before the wrap")
+    last = np.array([0xFFFFFFFE], dtype=np.uint32).view(np.uint8)
+    ws[8:12] = torch.from_numpy(last).cuda()
+    y1 = vg.gemv(wt, x, workspace=ws)          # tags 0xFFFFFFFF, then wrap
+    torch.cuda.synchronize()
+    assert int(ws[8:12].cpu().numpy().view(np.uint32)[0]) == 0
+    assert not ws[256:].any(), "the wrap clears every partial-sum slot"
+    y2 = vg.gemv(wt, x, workspace=ws)          # tags 1 again
+    assert int(ws[8:12].cpu().numpy().view(np.uint32)[0]) == 1
+    assert vg.workspace_error(ws) == 0
+    assert torch.equal(y0, y1) and torch.equal(y0, y2)
 
 
 @pytest.mark.parametrize("M,K,Ns", GEMV_SHAPES)

@@ -38,6 +38,12 @@ constexpr int kF8ChunkUnits = 4;
 #ifndef VG_SLOTS
 #define VG_SLOTS 3
 #endif
+#ifndef VG_R3_MULHI
+#define VG_R3_MULHI 0
+#endif
+#ifndef VG_SHIFT_ALU
+#define VG_SHIFT_ALU 0
+#endif
 constexpr int kBlockTiles = 16;
 constexpr int kWarps = VG_WARPS;
 static_assert(kWarps == kBlockTiles, "one tile of the row block per warp");
@@ -208,6 +214,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -243,6 +254,38 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// GPU-scope accesses for the cross-block protocol.
+__device__ __forceinline__ void red_add_release(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_relaxed(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.relaxed.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Two 64-bit words, each a single-copy-atomic access at GPU scope (a vector
+// access is a set of independent scalar accesses, one per element).  Used
+// for partial sums that carry their own validity tag in the upper half, so
+// that no fence is needed between the data and a flag.
+__device__ __forceinline__ void st_relaxed_v2u64(uint64_t *p, uint64_t a, uint64_t b) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void ld_relaxed_v2u64(const uint64_t *p, uint64_t &a, uint64_t &b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -261,9 +304,20 @@ __device__ __forceinline__ void nv_decode(uint32_t w, uint32_t fg, uint32_t fg8,
                                           uint32_t m64, uint32_t &a0, uint32_t &a1,
                                           uint32_t &a2, uint32_t &a3) {
   const uint32_t r0 = w & kNvMask;
+#if VG_SHIFT_ALU
+  const uint32_t r1 = (w << 3) & kNvMask;
+  const uint32_t r2 = (w << 6) & kNvMask;
+#else
   const uint32_t r1 = umul(w, m8) & kNvMask;
   const uint32_t r2 = umul(w, m64) & kNvMask;
+#endif
+#if VG_R3_MULHI
+  uint32_t w7;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(w7) : "r"(w), "r"(m64 << 19));
+  const uint32_t r3 = umul(w7 & kNvR3Pick, kNvR3Spread) & kNvMask;
+#else
   const uint32_t r3 = umul((w >> 7) & kNvR3Pick, kNvR3Spread) & kNvMask;
+#endif
   a0 = bmul2(r0, fg);
   a1 = bmul2(r1, fg8);
   a2 = bmul2(r2, fg);

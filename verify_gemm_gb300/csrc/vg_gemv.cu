@@ -10,20 +10,24 @@
 // rate), so the kernel is built to stream bytes at HBM speed.
 //
 // Design (sm_103a):
-//  * Persistent thread blocks, one per SM: 8 consumer warps + 1 producer
-//    warp.  The producer streams one pipeline stage per work item with 1-D
-//    bulk copies (cp.async.bulk) into a 4-deep shared-memory ring guarded by
-//    mbarriers; the weights never pass through registers of the producer.
-//  * A work item is one chunk (256 columns NVFP4, 128 FP8) of a row block of
-//    16 tiles (256 rows); each consumer warp owns 2 tiles and decodes its
+//  * Persistent thread blocks, one per SM: 16 consumer warps + 1 producer
+//    warp.  Producer lane t keeps consumer warp t's private 3-slot ring of
+//    shared memory full with 1-D bulk copies (cp.async.bulk, L2 evict-first),
+//    guarded by full/empty mbarriers; the weights never pass through
+//    registers of the producer.
+//  * A work item is one chunk (512 columns NVFP4, 256 FP8) of a row block of
+//    16 tiles (256 rows); consumer warp t owns tile t of it.  It decodes the
 //    codes in registers to BF16 A fragments (bit placement + one BF16x2
 //    multiply by the block scale, exact) and runs mma.m16n8k16 with x as the
 //    B fragment (x read through L1, shared by all warps), accumulating FP32.
 //  * Items are split between thread blocks stream-K style (contiguous item
 //    ranges of equal length), so every SM streams the same number of bytes.
-//    A row block whose K range is split between blocks is summed from FP32
-//    partials by the last block to arrive, in block order (deterministic,
-//    no spinning); the counter it used is reset for the next call.
+//    A row block whose K range is split between blocks is summed by the
+//    block holding its first item (it reaches that piece last) from the
+//    others' FP32 partial sums, in block order (deterministic).  Each
+//    partial sum travels with a tag of the pass and phase in the same 64-bit
+//    word, so a contributor publishes it with plain stores and moves on: no
+//    fence, counter or barrier on its path.
 //  * Verify pass: matrices are grouped; in ordered mode the consumers of
 //    group g wait (bounded) until group g-1 has completed every row block,
 //    while the producer keeps prefetching group g's weights.  All waits are
@@ -54,13 +58,14 @@ struct MatDev {
   int M, K, MT, KU, KC, RB;
   int cu, ub;        // units per chunk, bytes per unit
   int64_t rb_bytes;  // code bytes of a full row block (16 tiles x KU units)
-  int64_t item0;     // first item of this matrix within its phase
-  int64_t rb_base;   // first arrival counter of this matrix
+  int item0;         // first item of this matrix within its phase
 };
 
+// Item counts fit 32 bits: a matrix has fewer than 2^40 / (256 x 512) items
+// and a plan's phase is checked on the host.
 struct PhaseDev {
-  int64_t items;
-  int64_t rbs;
+  int items;
+  int rbs;
   int mat_begin, mat_end;
 };
 
@@ -73,34 +78,44 @@ struct Params {
   int hold_phase;
   int grid;
   uint64_t timeout_ns;
-  uint32_t *cnt;
+  int *error;               // first failed wait's code, else 0
+  uint32_t *ctas_done;      // blocks finished in this pass (left at 0)
+  uint32_t *epoch;          // pass counter: tags partial sums
   uint32_t *done;           // per-phase completed row blocks (ordered only)
-  uint32_t *ctas_done;
-  float *partials;          // [grid][2][16 tiles][32 lanes][4]
-  int *error;
+  uint64_t *partials;       // [grid][kPartialWords]: tagged FP32 partial sums
   uint32_t m8, m64;         // 8 and 64: shift multipliers kept in registers
   MatDev mat0;
   PhaseDev phase0;
 };
 
-constexpr int kPartialFloats = kBlockTiles * 32 * 4;   // one slot
+// One block's partial-sum slot: 4 FP32 sums per consumer thread, each in a
+// 64-bit word whose upper half is the tag of the pass and phase that wrote it.
+constexpr int kPartialWords = kBlockTiles * 32 * 4;
 constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;
 constexpr int kBarBytes = 2 * kWarps * kSlots * 8;
 constexpr int kSmemBytes = kRingBytes + kBarBytes + 64;
 constexpr int kConsumers = kWarps * 32;
 constexpr int kKernelThreads = kConsumers + 32;        // + one producer warp
-constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3;
+constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3, kErrPartialWait = 4;
+// Header words of a workspace (GEMV) or plan state: error, finished blocks,
+// pass epoch; then, 256 bytes in, the per-phase counters (plans) and the
+// partial-sum slots.
+constexpr size_t kWsHead = 256;
 
 __host__ __device__ inline int64_t i64min(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline int64_t i64max(int64_t a, int64_t b) { return a > b ? a : b; }
 
-__host__ __device__ inline int64_t item_begin(int64_t T, int64_t G, int64_t b) {
-  return T * b / G;
+__host__ __device__ inline int item_begin(int T, int G, int b) {
+  return int(int64_t(T) * b / G);
 }
 // Block that owns item i of a phase of T items split over G blocks.
-__device__ inline int64_t owner(int64_t T, int64_t G, int64_t i) { return ((i + 1) * G - 1) / T; }
+__device__ inline int owner(int T, int G, int i) { return int((int64_t(i + 1) * G - 1) / T); }
 
 __device__ inline void set_error(int *error, int code) { atomicCAS(error, 0, code); }
+
+// x of a column >= N is read from here (zeros), so that x loads never need a
+// per-unit condition.  Covers one chunk of a lane's columns.
+__device__ __align__(16) uint16_t g_zero_x[kNvChunkUnits * kUnitK + 16];
 
 // Bounded wait with the clock read only after a first miss.
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t timeout) {
@@ -117,10 +132,10 @@ struct Seq {
   const PhaseDev *phases;
   int nphases, ph, mi, mend;
   int rb, c, KC, RB;
-  int64_t b, grid, G, i, i0, i1, items;
+  int b, grid, G, i, i0, i1, items;
   bool valid;
 
-  __device__ void init(const MatDev *m, const PhaseDev *p, int np, int64_t blk, int64_t g) {
+  __device__ void init(const MatDev *m, const PhaseDev *p, int np, int blk, int g) {
     mats = m;
     phases = p;
     nphases = np;
@@ -132,19 +147,19 @@ struct Seq {
   __device__ void next_phase() {
     for (++ph; ph < nphases; ++ph) {
       items = phases[ph].items;
-      G = i64min(grid, items);
+      G = min(grid, items);
       if (b < G) {
         i0 = item_begin(items, G, b);
         i1 = item_begin(items, G, b + 1);
         i = i0;
         mi = phases[ph].mat_begin;
         mend = phases[ph].mat_end;
-        while (mi + 1 < mend && i >= mats[mi].item0 + int64_t(mats[mi].RB) * mats[mi].KC) ++mi;
+        while (mi + 1 < mend && i >= mats[mi].item0 + mats[mi].RB * mats[mi].KC) ++mi;
         KC = mats[mi].KC;
         RB = mats[mi].RB;
-        const int64_t rel = i - mats[mi].item0;
-        rb = int(rel / KC);
-        c = int(rel - int64_t(rb) * KC);
+        const int rel = i - mats[mi].item0;
+        rb = rel / KC;
+        c = rel - rb * KC;
         valid = true;
         return;
       }
@@ -168,36 +183,43 @@ struct Seq {
   }
 };
 
-// One NVFP4 unit of one tile: 4 MMAs (k16 steps) into two accumulators.
+// MMA steps j = 0..3 of a unit accumulate into acc[j % kAcc]: with kAcc
+// accumulators the dependent MMA chains are kAcc times shorter.
+#ifndef VG_NACC
+#define VG_NACC 2
+#endif
+constexpr int kAcc = VG_NACC;
+
+// One NVFP4 unit of one tile: 4 MMAs (k16 steps).
 __device__ __forceinline__ void nv_unit(const uint4 wv, uint32_t fg, uint32_t fg8, const uint4 xa,
                                         const uint4 xb, uint32_t m8, uint32_t m64,
-                                        float (&acc0)[4], float (&acc1)[4]) {
+                                        float (&acc)[kAcc][4]) {
   uint32_t a0, a1, a2, a3;
   nv_decode(wv.x, fg, fg8, m8, m64, a0, a1, a2, a3);
-  mma_bf16(acc0, a0, a1, a2, a3, xa.x, xa.y);
+  mma_bf16(acc[0], a0, a1, a2, a3, xa.x, xa.y);
   nv_decode(wv.y, fg, fg8, m8, m64, a0, a1, a2, a3);
-  mma_bf16(acc1, a0, a1, a2, a3, xa.z, xa.w);
+  mma_bf16(acc[1 % kAcc], a0, a1, a2, a3, xa.z, xa.w);
   nv_decode(wv.z, fg, fg8, m8, m64, a0, a1, a2, a3);
-  mma_bf16(acc0, a0, a1, a2, a3, xb.x, xb.y);
+  mma_bf16(acc[2 % kAcc], a0, a1, a2, a3, xb.x, xb.y);
   nv_decode(wv.w, fg, fg8, m8, m64, a0, a1, a2, a3);
-  mma_bf16(acc1, a0, a1, a2, a3, xb.z, xb.w);
+  mma_bf16(acc[3 % kAcc], a0, a1, a2, a3, xb.z, xb.w);
 }
 
 __device__ __forceinline__ void f8_unit(const uint4 w0, const uint4 w1, const uint4 xa,
-                                        const uint4 xb, float (&acc0)[4], float (&acc1)[4]) {
+                                        const uint4 xb, float (&acc)[kAcc][4]) {
   uint32_t a0, a1, a2, a3;
   f8_decode(w0.x, a0, a1);
   f8_decode(w0.y, a2, a3);
-  mma_bf16(acc0, a0, a1, a2, a3, xa.x, xa.y);
+  mma_bf16(acc[0], a0, a1, a2, a3, xa.x, xa.y);
   f8_decode(w0.z, a0, a1);
   f8_decode(w0.w, a2, a3);
-  mma_bf16(acc1, a0, a1, a2, a3, xa.z, xa.w);
+  mma_bf16(acc[1 % kAcc], a0, a1, a2, a3, xa.z, xa.w);
   f8_decode(w1.x, a0, a1);
   f8_decode(w1.y, a2, a3);
-  mma_bf16(acc0, a0, a1, a2, a3, xb.x, xb.y);
+  mma_bf16(acc[2 % kAcc], a0, a1, a2, a3, xb.x, xb.y);
   f8_decode(w1.z, a0, a1);
   f8_decode(w1.w, a2, a3);
-  mma_bf16(acc1, a0, a1, a2, a3, xb.z, xb.w);
+  mma_bf16(acc[3 % kAcc], a0, a1, a2, a3, xb.z, xb.w);
 }
 
 // x fragment of one unit for lane (g, t): the 16 columns at xp as two
@@ -214,30 +236,29 @@ __device__ __forceinline__ void load_x(const uint16_t *xp, bool on, uint4 &xa, u
 
 // A whole NVFP4 chunk (8 units) of this lane's tile: scale pairs from one
 // 16-byte load, codes and x for two units at a time, the next pair loaded
-// before the current one is multiplied.
+// before the current one is multiplied.  xp points at the lane's x columns,
+// or at zeros for a column >= N.
 __device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, const uint16_t *xp,
-                                              bool on, uint32_t m8, uint32_t m64,
-                                              float (&acc0)[4], float (&acc1)[4]) {
+                                              uint32_t m8, uint32_t m64, float (&acc)[kAcc][4]) {
   const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
   const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
   uint4 w0 = lds128(slot + lane * 16), w1 = lds128(slot + kNvUnitBytes + lane * 16);
-  uint4 x0a, x0b, x1a, x1b;
-  load_x(xp, on, x0a, x0b);
-  load_x(xp + kUnitK, on, x1a, x1b);
+  uint4 x0a = ldg128(xp), x0b = ldg128(xp + 8);
+  uint4 x1a = ldg128(xp + kUnitK), x1b = ldg128(xp + kUnitK + 8);
 #pragma unroll
   for (int h = 0; h < kNvChunkUnits / 2; ++h) {
     uint4 nw0, nw1, nx0a, nx0b, nx1a, nx1b;
     if (h + 1 < kNvChunkUnits / 2) {
       nw0 = lds128(slot + (2 * h + 2) * kNvUnitBytes + lane * 16);
       nw1 = lds128(slot + (2 * h + 3) * kNvUnitBytes + lane * 16);
-      load_x(xp + (2 * h + 2) * kUnitK, on, nx0a, nx0b);
-      load_x(xp + (2 * h + 3) * kUnitK, on, nx1a, nx1b);
+      nx0a = ldg128(xp + (2 * h + 2) * kUnitK);
+      nx0b = ldg128(xp + (2 * h + 2) * kUnitK + 8);
+      nx1a = ldg128(xp + (2 * h + 3) * kUnitK);
+      nx1b = ldg128(xp + (2 * h + 3) * kUnitK + 8);
     }
     // unit 2h uses scale bytes 0,1 of word h; unit 2h+1 bytes 2,3
-    nv_unit(w0, nv_scale_pair(scw[h], 0), nv_scale_pair(scw[h], 1), x0a, x0b, m8, m64, acc0,
-            acc1);
-    nv_unit(w1, nv_scale_pair(scw[h], 2), nv_scale_pair(scw[h], 3), x1a, x1b, m8, m64, acc0,
-            acc1);
+    nv_unit(w0, nv_scale_pair(scw[h], 0), nv_scale_pair(scw[h], 1), x0a, x0b, m8, m64, acc);
+    nv_unit(w1, nv_scale_pair(scw[h], 2), nv_scale_pair(scw[h], 3), x1a, x1b, m8, m64, acc);
     if (h + 1 < kNvChunkUnits / 2) {
       w0 = nw0;
       w1 = nw1;
@@ -252,8 +273,7 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, const uin
 // A partial NVFP4 chunk (the K tail): nu units, columns checked against K.
 __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uint16_t *xp,
                                               bool on, int nu, int kleft, uint32_t m8,
-                                              uint32_t m64, float (&acc0)[4],
-                                              float (&acc1)[4]) {
+                                              uint32_t m64, float (&acc)[kAcc][4]) {
   const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
   for (int u = 0; u < nu; ++u) {
     const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
@@ -262,28 +282,38 @@ __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uin
     const int q = u >> 1;
     const uint32_t word = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
     const uint32_t b = uint32_t(u & 1) * 2u;
-    nv_unit(wv, nv_scale_pair(word, b), nv_scale_pair(word, b + 1), xa, xb, m8, m64, acc0, acc1);
+    nv_unit(wv, nv_scale_pair(word, b), nv_scale_pair(word, b + 1), xa, xb, m8, m64, acc);
   }
 }
 
-// An FP8 chunk: nu (<= 4) units of 1024 bytes.
+// An FP8 chunk: nu (<= 4) units of 1024 bytes.  `full`: all 4 units lie
+// inside K, so x loads need no per-unit condition.
 __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t *xp, bool on,
-                                         int nu, int kleft, float (&acc0)[4],
-                                         float (&acc1)[4]) {
+                                         bool full, int nu, int kleft, float (&acc)[kAcc][4]) {
 #pragma unroll
   for (int u = 0; u < kF8ChunkUnits; ++u) {
-    if (u < nu) {
+    if (full || u < nu) {
       const uint4 w0 = lds128(slot + u * kF8UnitBytes + lane * 32);
       const uint4 w1 = lds128(slot + u * kF8UnitBytes + lane * 32 + 16);
       uint4 xa, xb;
-      load_x(xp + u * kUnitK, on && u * kUnitK < kleft, xa, xb);
-      f8_unit(w0, w1, xa, xb, acc0, acc1);
+      if (full) {
+        xa = ldg128(xp + u * kUnitK);
+        xb = ldg128(xp + u * kUnitK + 8);
+      } else {
+        load_x(xp + u * kUnitK, on && u * kUnitK < kleft, xa, xb);
+      }
+      f8_unit(w0, w1, xa, xb, acc);
     }
   }
 }
 
 // Producer lane `tile` (0..15): refill consumer warp `tile`'s ring, one item
-// at a time, as soon as that warp has released the slot.
+// at a time, as soon as that warp has released the slot.  Lanes below N also
+// bring the item's x row into L2, during the block's first pass over the
+// matrix's chunks only (after that x is in L2 already).  The lanes of the
+// producer warp progress independently: each pass of the loop a lane polls
+// its own slot once and issues only if it is free, so a slow consumer warp
+// never holds back the refills of the others.
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases, int tile,
                          uint32_t ring, uint32_t full0, uint32_t empty0) {
   const uint64_t policy = policy_evict_first();
@@ -292,11 +322,22 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   int s = 0;
   uint32_t par = 0;
   int64_t issued = 0;
+  uint64_t deadline = 0;
+  bool waiting = false;
+  int x_mi = -1, x_ph = -1, x_left = 0;   // x prefetches left for this matrix
   while (q.valid) {
-    if (!mbar_wait_for(empty0 + 8 * s, par ^ 1u, p.timeout_ns)) {
-      set_error(p.error, kErrEmptyWait);
-      break;
+    if (!mbar_try_wait(empty0 + 8 * s, par ^ 1u)) {
+      const uint64_t now = globaltimer();
+      if (!waiting) {
+        waiting = true;
+        deadline = now + p.timeout_ns;
+      } else if (now > deadline) {
+        set_error(p.error, kErrEmptyWait);
+        break;
+      }
+      continue;
     }
+    waiting = false;
     const MatDev &m = mats[q.mi];
     const uint32_t full = full0 + 8 * s;
     const int tiles = min(kBlockTiles, m.MT - q.rb * kBlockTiles);
@@ -319,6 +360,18 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
         bulk_g2s(slot, m.w + off, code_bytes, full, policy);
       }
     }
+    // lane n < N also brings row n of this item's x slice into L2, so that
+    // the consumers' x loads hit L2 rather than DRAM
+    if (q.mi != x_mi || q.ph != x_ph) {
+      x_mi = q.mi;
+      x_ph = q.ph;
+      x_left = m.KC;
+    }
+    if (tile < p.N && x_left-- > 0) {
+      const int64_t k0 = int64_t(q.c) * m.cu * kUnitK;
+      const int64_t cols = i64min(int64_t(m.cu) * kUnitK, m.K - k0);
+      bulk_prefetch_l2(m.x + int64_t(tile) * m.K + k0, uint32_t(cols * 2));
+    }
     q.advance();
     ++issued;
     if (++s == kSlots) {
@@ -329,6 +382,107 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   // Never leave while a bulk copy may still be writing shared memory.
   for (int64_t k = i64max(0, issued - kSlots); k < issued; ++k)
     mbar_wait_for(full0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u, p.timeout_ns);
+}
+
+// The reducer of a split row block adds the partial sums of the other
+// contributors, blocks b0..bl, in block order.  Each thread reads only its
+// own four words of every slot; a word counts once its tag matches `tag`, so
+// no fence is needed on either side.  Loads for two contributors are in
+// flight at once (more would crowd the streaming loop's registers).
+// Returns false if the wait ran out or another block has already failed.
+__device__ __noinline__ bool collect(const Params &p, int b0, int bl, uint32_t tag, int at,
+                                     float (&accs)[4]) {
+  uint64_t deadline = 0;
+  for (int bb = b0; bb <= bl; bb += 2) {
+    uint64_t v[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (bb + j <= bl) {
+        const uint64_t *src = p.partials + int64_t(bb + j) * kPartialWords + at;
+        ld_relaxed_v2u64(src, v[j][0], v[j][1]);
+        ld_relaxed_v2u64(src + 64, v[j][2], v[j][3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (bb + j <= bl) {
+        while (uint32_t(v[j][0] >> 32) != tag || uint32_t(v[j][1] >> 32) != tag ||
+               uint32_t(v[j][2] >> 32) != tag || uint32_t(v[j][3] >> 32) != tag) {
+          const uint64_t now = globaltimer();
+          if (deadline == 0) {
+            deadline = now + p.timeout_ns;
+          } else if (now > deadline) {
+            set_error(p.error, kErrPartialWait);
+            return false;
+          }
+          if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
+          const uint64_t *src = p.partials + int64_t(bb + j) * kPartialWords + at;
+          ld_relaxed_v2u64(src, v[j][0], v[j][1]);
+          ld_relaxed_v2u64(src + 64, v[j][2], v[j][3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accs[e] += __uint_as_float(uint32_t(v[j][e]));
+      }
+    }
+  }
+  return true;
+}
+
+// End of a row-block piece.  A block that covered the whole row block writes
+// y.  Otherwise the row block is split: the block holding its first item
+// (the reducer) adds the other contributors' partial sums to its own and
+// writes y; every other contributor publishes its partial sums in its slot,
+// tagged, and moves on without waiting.  In ordered mode the completed row
+// block is counted for its phase.  Kept out of line: it runs once per piece,
+// and its registers must not crowd the streaming loop.  Returns false if the
+// wait for partial sums failed.
+__device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, int T, int G,
+                                          int piece_start, bool full_piece, int rb, int ph,
+                                          uint32_t tag, bool aborted, float a0, float a1,
+                                          float a2, float a3) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int mt = rb * kBlockTiles + warp;
+  const int at = ((warp * 2) * 32 + lane) * 2;    // this thread's words in a slot
+  float accs[4] = {a0, a1, a2, a3};
+  bool ok = true;
+  if (!full_piece) {
+    const int first = m.item0 + rb * m.KC;
+    if (piece_start != first) {
+      if (!aborted) {
+        uint64_t *dst = p.partials + int64_t(blockIdx.x) * kPartialWords + at;
+        const uint64_t hi = uint64_t(tag) << 32;
+        st_relaxed_v2u64(dst, hi | __float_as_uint(accs[0]), hi | __float_as_uint(accs[1]));
+        st_relaxed_v2u64(dst + 64, hi | __float_as_uint(accs[2]), hi | __float_as_uint(accs[3]));
+      }
+      return true;
+    }
+    if (!aborted) ok = collect(p, int(blockIdx.x) + 1, owner(T, G, first + m.KC - 1), tag, at, accs);
+    // mma.sync needs whole warps: a failure anywhere in the warp stops it all
+    ok = __all_sync(0xFFFFFFFFu, ok);
+  }
+  if (ok && !aborted && mt < m.MT) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = mt * kTileRows + g + 8 * h;
+      if (row >= m.M) continue;
+      const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int nn = 2 * t + e;
+        if (nn < p.N) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(accs[2 * h + e] * mult);
+          m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
+        }
+      }
+    }
+  }
+  if (p.done) {
+    named_bar(1, kConsumers);
+    // releases the row block's y (written before the barrier)
+    if (tid == 0 && ok && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
+  }
+  return ok;
 }
 
 __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_constant__ Params p) {
@@ -346,15 +500,18 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   if (tid == 0) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sflag[0] = 0;
-    sflag[1] = 0;
+    sflag[1] = int(ld_relaxed(p.epoch));
+    sflag[2] = 0;
   }
   __syncthreads();
+  const uint32_t epoch = uint32_t(sflag[1]);
 
   if (warp == kWarps) {
     // ================================================================ producer
     if (lane < kBlockTiles)
       producer(p, mats, phases, lane, smem_addr(smem + lane * kSlots * kSlotBytes),
                smem_addr(bars + lane * kSlots), smem_addr(bars + kWarps * kSlots + lane * kSlots));
+
   } else {
     // =============================================================== consumers
     const int g = lane >> 2, t = lane & 3;
@@ -369,9 +526,10 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     int s = 0;                     // ring slot of the current item
     uint32_t par = 0;              // parity of that slot's current phase
     int cur_ph = -1, cur_mi = -1;
-    int64_t piece_start = 0;
+    uint32_t tag = 0;              // tag of this pass and phase
+    int piece_start = 0;
     int piece_c0 = 0;
-    float acc0[4], acc1[4];
+    float acc[kAcc][4];
     // matrix fields cached while the matrix does not change
     const uint16_t *xbase = nullptr;
     int K = 0, KU = 0, MT = 0, fmt = 0;
@@ -383,18 +541,23 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
           if (tid == 0) {
             int ok = 1;
             if (!aborted) {
-              const volatile uint32_t *d = p.done + (ph - 1);
+              const uint32_t *d = p.done + (ph - 1);
               const uint32_t target = uint32_t(phases[ph - 1].rbs);
-              const uint64_t deadline = globaltimer() + p.timeout_ns;
-              while (*d < target) {
-                if (globaltimer() > deadline) {
-                  ok = 0;
-                  set_error(p.error, kErrDepWait);
-                  break;
+              if (ld_acquire(d) < target) {
+                const uint64_t deadline = globaltimer() + p.timeout_ns;
+                while (ld_acquire(d) < target) {
+                  if (globaltimer() > deadline) {
+                    ok = 0;
+                    set_error(p.error, kErrDepWait);
+                    break;
+                  }
+                  if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) {
+                    ok = 0;   // another block has failed: results are void
+                    break;
+                  }
+                  __nanosleep(32);
                 }
-                __nanosleep(32);
               }
-              __threadfence();
             }
             sflag[0] = ok ? 0 : 1;
           }
@@ -403,6 +566,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
           named_bar(1, kConsumers);
         }
         cur_ph = ph;
+        tag = epoch * uint32_t(p.nphases) + uint32_t(ph) + 1u;
       }
       if (cons.mi != cur_mi) {
         const MatDev &mm = mats[cons.mi];
@@ -418,13 +582,20 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         piece_start = cons.i;
         piece_c0 = c;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc0[e] = acc1[e] = 0.f;
+        for (int a = 0; a < kAcc; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
       }
       const uint32_t slot = ring + s * kSlotBytes;
       const int mt = rb * kBlockTiles + warp;
-      if (!aborted && !mbar_wait_for(full0 + 8 * s, par, p.timeout_ns)) {
-        if (lane == 0) set_error(p.error, kErrFullWait);
-        aborted = true;
+      if (!aborted) {
+        // every lane polls; a lane whose wait ran out stops the whole warp,
+        // since mma.sync needs all of it
+        const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
+        if (!__all_sync(0xFFFFFFFFu, ready)) {
+          if (lane == 0) set_error(p.error, kErrFullWait);
+          aborted = true;
+        }
       }
       if (!aborted && mt < MT) {
         if (fmt == VG_FMT_NVFP4) {
@@ -432,14 +603,15 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
           // warp-uniform test (mma.sync needs the whole warp): the chunk's
           // whole column range lies inside K
           if (kc + kNvChunkUnits * kUnitK <= K)
-            nv_chunk_full(slot, lane, xbase + kc, on, p.m8, p.m64, acc0, acc1);
+            nv_chunk_full(slot, lane, on ? xbase + kc : g_zero_x, p.m8, p.m64, acc);
           else
             nv_chunk_tail(slot, lane, xbase + kc, on, min(kNvChunkUnits, KU - c * kNvChunkUnits),
-                          K - kc - 16 * t, p.m8, p.m64, acc0, acc1);
+                          K - kc - 16 * t, p.m8, p.m64, acc);
         } else {
           const int kc = c * (kF8ChunkUnits * kUnitK);
-          f8_chunk(slot, lane, xbase + kc, on, min(kF8ChunkUnits, KU - c * kF8ChunkUnits),
-                   K - kc - 16 * t, acc0, acc1);
+          const bool full = kc + kF8ChunkUnits * kUnitK <= K;
+          f8_chunk(slot, lane, full && !on ? g_zero_x : xbase + kc, on, full,
+                   min(kF8ChunkUnits, KU - c * kF8ChunkUnits), K - kc - 16 * t, acc);
         }
       }
       // release the slot to the producer (every lane has read it)
@@ -453,93 +625,44 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
       // ---------------------------------------------- end of a row-block piece
       const bool piece_end = c == cons.KC - 1 || cons.i == cons.i1 - 1;
       if (piece_end) {
-        const MatDev &m = mats[cons.mi];
-        const int64_t T = cons.items, G = cons.G, i0 = cons.i0;
-        const bool full_piece = piece_c0 == 0 && c == m.KC - 1;
-        float acc[4];
+        float accs[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = acc0[e] + acc1[e];
-        bool write_out = true;
-        if (!full_piece) {
-          // partial sums: stash, count arrivals, the last arrival reduces
-          const int slotp = int(2 * blockIdx.x + (piece_start == i0 ? 0 : 1));
-          float *part = p.partials + int64_t(slotp) * kPartialFloats;
-          if (!aborted)
-            *reinterpret_cast<float4 *>(part + (warp * 32 + lane) * 4) =
-                make_float4(acc[0], acc[1], acc[2], acc[3]);
-          named_bar(1, kConsumers);
-          const int64_t first = m.item0 + int64_t(rb) * m.KC, last = first + m.KC - 1;
-          const int64_t bf = owner(T, G, first), bl = owner(T, G, last);
-          if (tid == 0) {
-            int is_last = 0;
-            if (!aborted) {
-              __threadfence();       // publish this block's partials (cumulative)
-              uint32_t *cnt = p.cnt + m.rb_base + rb;
-              const uint32_t old = atomicAdd(cnt, 1u);
-              is_last = old == uint32_t(bl - bf);
-              if (is_last) {
-                *cnt = 0u;
-                __threadfence();     // acquire the other blocks' partials
-              }
-            }
-            sflag[1] = is_last;
-          }
-          named_bar(1, kConsumers);
-          write_out = sflag[1] != 0;
-          named_bar(1, kConsumers);
-          if (write_out) {
+        for (int e = 0; e < 4; ++e) {
+          accs[e] = acc[0][e];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = 0.f;
-            for (int64_t bb = bf; bb <= bl; ++bb) {
-              const int64_t ss = 2 * bb + (item_begin(T, G, bb) >= first ? 0 : 1);
-              const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                  p.partials + ss * kPartialFloats + (warp * 32 + lane) * 4));
-              acc[0] += v.x;
-              acc[1] += v.y;
-              acc[2] += v.z;
-              acc[3] += v.w;
-            }
-          }
+          for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
         }
-        if (write_out) {
-          if (!aborted && mt < m.MT) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int row = mt * kTileRows + g + 8 * h;
-              if (row >= m.M) continue;
-              const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int nn = 2 * t + e;
-                if (nn < N) {
-                  const __nv_bfloat16 v = __float2bfloat16_rn(acc[2 * h + e] * mult);
-                  m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
-                }
-              }
-            }
-          }
-          if (p.done) {
-            named_bar(1, kConsumers);
-            if (tid == 0 && !aborted && ph != p.hold_phase) {
-              __threadfence();       // publish the row block's y (cumulative)
-              atomicAdd(p.done + ph, 1u);
-            }
-          }
-        }
+        if (!finish_piece(p, mats[cons.mi], cons.items, cons.G, piece_start,
+                          piece_c0 == 0 && c == cons.KC - 1, rb, ph, tag, aborted, accs[0],
+                          accs[1], accs[2], accs[3]))
+          aborted = true;
       }
       cons.advance();
     }
   }
 
-  // The last block out resets the per-phase completion counters.
+  // The last block out resets the per-phase completion counters and
+  // advances the pass epoch, so that the next pass's partial sums carry new
+  // tags.  Before the tags would overflow 32 bits the epoch restarts at 0
+  // and every slot is cleared (tag 0 never matches).
   __syncthreads();
-  if (p.done && tid == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(p.ctas_done, 1u);
-    if (old == uint32_t(p.grid - 1)) {
-      for (int ph = 0; ph < p.nphases; ++ph) p.done[ph] = 0u;
+  if (tid == 0) sflag[2] = atom_add_relaxed(p.ctas_done, 1u) == uint32_t(p.grid - 1) ? 1 : 0;
+  __syncthreads();
+  if (sflag[2]) {
+    if (tid == 0) {
+      fence_acq_rel_gpu();    // every other block has finished with the state
+      if (p.done)
+        for (int ph = 0; ph < p.nphases; ++ph) p.done[ph] = 0u;
+      const bool wrap = (uint64_t(epoch) + 2u) * uint64_t(p.nphases) > 0xFFFFFFFFull;
+      *p.epoch = wrap ? 0u : epoch + 1u;
       *p.ctas_done = 0u;
-      __threadfence();
+      sflag[0] = wrap ? 1 : 0;
+    }
+    __syncthreads();
+    if (sflag[0]) {
+      uint4 *dst = reinterpret_cast<uint4 *>(p.partials);
+      const int64_t n = int64_t(p.grid) * kPartialWords / 2;
+      for (int64_t k = tid; k < n; k += kKernelThreads) dst[k] = make_uint4(0, 0, 0, 0);
     }
   }
 }
@@ -606,11 +729,33 @@ int64_t algorithmic_bytes(const MatDev &m) {
   return m.fmt == VG_FMT_NVFP4 ? E / 2 + E / 16 + 4 : E + 4 * int64_t(m.M);
 }
 
-// Single-GEMV workspace: [error word | counters | partial slots].
-constexpr size_t kWsHead = 256;
-size_t ws_counters_bytes(int64_t RB) { return size_t((RB * 4 + 255) / 256 * 256); }
-size_t ws_bytes(int64_t RB, int grid) {
-  return kWsHead + ws_counters_bytes(RB) + size_t(grid) * 2 * kPartialFloats * sizeof(float);
+// Single-GEMV workspace: [header words | partial slots].
+size_t ws_bytes(int grid) { return kWsHead + size_t(grid) * kPartialWords * sizeof(uint64_t); }
+
+void set_head(Params &p, uint8_t *head) {
+  p.error = reinterpret_cast<int *>(head);
+  p.ctas_done = reinterpret_cast<uint32_t *>(head + 4);
+  p.epoch = reinterpret_cast<uint32_t *>(head + 8);
+}
+
+// Every block of a pass must be resident at once (a reducer waits for the
+// other contributors), which a cooperative launch guarantees.
+vg_status launch(const Params &p, vg_stream_t stream) {
+  void *args[] = {const_cast<Params *>(&p)};
+  VG_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&stream_kernel), dim3(p.grid),
+                                      dim3(kKernelThreads), args, kSmemBytes, as_cuda(stream)));
+  return VG_OK;
+}
+
+// Blocks per pass: one per SM (fewer when there are fewer items), capped by
+// what can be resident at once.
+vg_status max_grid(const DeviceInfo &d, int *grid) {
+  int per_sm = 0;
+  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel, kKernelThreads,
+                                                        kSmemBytes));
+  if (per_sm < 1) return VG_ERR_UNSUPPORTED;
+  *grid = std::min(d.sms, per_sm * d.sms);
+  return VG_OK;
 }
 
 vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace_bytes,
@@ -619,8 +764,10 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
   const int64_t T = int64_t(m0.RB) * m0.KC;
-  const int grid = int(i64min(di->sms, T));
-  if (!workspace || workspace_bytes < ws_bytes(m0.RB, grid)) return VG_ERR_WORKSPACE;
+  int grid = 0;
+  if (vg_status s = max_grid(*di, &grid)) return s;
+  grid = int(i64min(grid, T));
+  if (!workspace || workspace_bytes < ws_bytes(grid)) return VG_ERR_WORKSPACE;
   if (!aligned16(workspace)) return VG_ERR_ALIGNMENT;
   Params p;
   std::memset(&p, 0, sizeof p);
@@ -633,17 +780,14 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   p.m8 = 8;
   p.m64 = 64;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  p.error = reinterpret_cast<int *>(ws);
-  p.cnt = reinterpret_cast<uint32_t *>(ws + kWsHead);
-  p.partials = reinterpret_cast<float *>(ws + kWsHead + ws_counters_bytes(m0.RB));
+  set_head(p, ws);
+  p.partials = reinterpret_cast<uint64_t *>(ws + kWsHead);
   p.mat0 = m0;
-  p.phase0.items = T;
+  p.phase0.items = int(T);
   p.phase0.rbs = m0.RB;
   p.phase0.mat_begin = 0;
   p.phase0.mat_end = 1;
-  stream_kernel<<<grid, kKernelThreads, kSmemBytes, as_cuda(stream)>>>(p);
-  VG_LAUNCH_CHECK();
-  return VG_OK;
+  return launch(p, stream);
 }
 
 }  // namespace
@@ -672,8 +816,9 @@ extern "C" vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, si
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
   const MatDev m = make_mat(format, M, K, nullptr, nullptr, nullptr, 0.f, nullptr, nullptr);
-  const int grid = int(i64min(di->sms, int64_t(m.RB) * m.KC));
-  *bytes = ws_bytes(m.RB, grid);
+  int grid = 0;
+  if (vg_status s = max_grid(*di, &grid)) return s;
+  *bytes = ws_bytes(int(i64min(grid, int64_t(m.RB) * m.KC)));
   return VG_OK;
 }
 
@@ -742,7 +887,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
 
   std::vector<MatDev> hm(static_cast<size_t>(count));
   std::vector<PhaseDev> hp;
-  int64_t rb_total = 0, bytes = 0;
+  int64_t bytes = 0;
   int hold_phase = -1;
   for (int i = 0; i < count; ++i) {
     const vg_matrix_desc &d = mats[i];
@@ -769,19 +914,16 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
     }
     PhaseDev &ph = hp.back();
     hm[i].item0 = ph.items;
-    hm[i].rb_base = rb_total;
-    ph.items += int64_t(hm[i].RB) * hm[i].KC;
+    // a phase's items are counted in 32 bits on the device
+    if (int64_t(ph.items) + int64_t(hm[i].RB) * hm[i].KC > int64_t(1) << 30) return VG_ERR_UNSUPPORTED;
+    ph.items += hm[i].RB * hm[i].KC;
     ph.rbs += hm[i].RB;
     ph.mat_end = i + 1;
-    rb_total += hm[i].RB;
     bytes += algorithmic_bytes(hm[i]);
   }
-  int grid = di->sms;
+  int grid = 0;
+  if (vg_status s = max_grid(*di, &grid)) return s;
   if (o.max_ctas > 0) grid = std::min(grid, int(o.max_ctas));
-  int per_sm = 0;
-  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel, kKernelThreads, kSmemBytes));
-  if (per_sm < 1) return VG_ERR_UNSUPPORTED;
-  grid = std::min(grid, per_sm * di->sms);
 
   vg_verify_plan *plan = new vg_verify_plan();
   plan->dev = dev;
@@ -790,11 +932,9 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   plan->ordered = o.ordered ? 1 : 0;
   plan->nphases = int(hp.size());
   plan->bytes = bytes;
-  const size_t head = 256;
-  const size_t cnt_bytes = size_t((rb_total * 4 + 255) / 256 * 256);
-  const size_t done_bytes = size_t((hp.size() * 4 + 4 + 255) / 256 * 256);
-  const size_t part_bytes = size_t(grid) * 2 * kPartialFloats * sizeof(float);
-  plan->state_bytes = head + cnt_bytes + done_bytes + part_bytes;
+  const size_t done_bytes = size_t((hp.size() * 4 + 255) / 256 * 256);
+  const size_t part_bytes = size_t(grid) * kPartialWords * sizeof(uint64_t);
+  plan->state_bytes = kWsHead + done_bytes + part_bytes;
   cudaError_t e = cudaMalloc(&plan->d_mats, sizeof(MatDev) * hm.size());
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_phases, sizeof(PhaseDev) * hp.size());
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_state, plan->state_bytes);
@@ -820,15 +960,9 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   p.timeout_ns = o.wait_timeout_ns > 0 ? uint64_t(o.wait_timeout_ns) : 2000000000ull;
   p.m8 = 8;
   p.m64 = 64;
-  p.error = reinterpret_cast<int *>(plan->d_state);
-  p.cnt = reinterpret_cast<uint32_t *>(plan->d_state + head);
-  p.done = reinterpret_cast<uint32_t *>(plan->d_state + head + cnt_bytes);
-  p.ctas_done = p.done + hp.size();
-  p.partials = reinterpret_cast<float *>(plan->d_state + head + cnt_bytes + done_bytes);
-  if (!plan->ordered) {
-    p.done = nullptr;
-    p.ctas_done = nullptr;
-  }
+  set_head(p, plan->d_state);
+  p.done = plan->ordered ? reinterpret_cast<uint32_t *>(plan->d_state + kWsHead) : nullptr;
+  p.partials = reinterpret_cast<uint64_t *>(plan->d_state + kWsHead + done_bytes);
   *plan_out = plan;
   return VG_OK;
 }
@@ -847,11 +981,7 @@ extern "C" vg_status vg_verify_pass(vg_verify_plan *plan, vg_stream_t stream) {
   int dev = 0;
   VG_CUDA(cudaGetDevice(&dev));
   if (dev != plan->dev) return VG_ERR_INVALID_ARG;
-  void *args[] = {&plan->params};
-  VG_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(stream_kernel),
-                                      dim3(plan->grid), dim3(kKernelThreads), args, kSmemBytes,
-                                      as_cuda(stream)));
-  return VG_OK;
+  return launch(plan->params, stream);
 }
 
 extern "C" vg_status vg_verify_plan_check(vg_verify_plan *plan, vg_stream_t stream,

@@ -1,9 +1,9 @@
 // vg_noalloc.cu -- vg_gemv_nvfp4_noalloc: the NVFP4 GEMV for callers that
 // cannot allocate device memory.
 //
-// vg_gemv_nvfp4 needs a workspace (arrival counters, an error word and FP32
-// partial sums for row blocks whose K range is split between thread
-// blocks), and expects the caller to allocate it.  Some callers cannot:
+// vg_gemv_nvfp4 needs a workspace (a few header words and FP32 partial
+// sums for row blocks whose K range is split between thread blocks), and
+// expects the caller to allocate it.  Some callers cannot:
 // code that runs inside a host application which owns all device memory
 // and only lends out the input and output buffers (a plugin or an engine
 // adapter), code that must not call cudaMalloc because it can synchronise
@@ -22,8 +22,8 @@
 namespace {
 
 // Largest workspace this entry point can serve: 4 MiB, enough for one
-// thread block per SM on a 160-SM device (2.5 MiB of partial sums) plus
-// arrival counters for about 390 000 row blocks of 256 rows.
+// thread block per SM (16 KiB of partial sums each) on devices of up to 255
+// SMs, whatever the matrix size.
 constexpr size_t kScratchBytes = VG_NOALLOC_SCRATCH_BYTES;
 
 // The workspace lives here.  In host code this name is only a stand-in for
@@ -62,9 +62,11 @@ extern "C" vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, fl
   if (need > kScratchBytes) return VG_ERR_UNSUPPORTED;   // beyond the fixed maximum
   void *scratch = nullptr;
   if (vg_status s = scratch_address(&scratch)) return s;
-  // The array keeps whatever the previous call left.  The kernel expects
-  // its error word and arrival counters to start at zero, so clear the part
-  // of the array this call uses (at most kScratchBytes) on the stream.
-  VG_CUDA(cudaMemsetAsync(scratch, 0, need, vg::as_cuda(stream)));
+  // The array starts zeroed and every call leaves it consistent for the
+  // next one (finished-block count back at zero, pass epoch advanced), except
+  // for the error word: a failed call leaves it set, and a set error word
+  // makes the kernel's waits give up early.  No caller of this entry point
+  // can read it, so clear it (4 bytes) before each call.
+  VG_CUDA(cudaMemsetAsync(scratch, 0, sizeof(int), vg::as_cuda(stream)));
   return vg_gemv_nvfp4(w, scales, gscale, x, N, M, K, y, scratch, kScratchBytes, stream);
 }

@@ -43,12 +43,15 @@ __global__ void __launch_bounds__(kProbeThreads) probe_ldg(const uint4 *__restri
   if ((threadIdx.x & 31) == 0) atomicXor(sink + blockIdx.x, acc);
 }
 
-// Each warp owns kProbeRingBytes / kProbeWarps bytes of slots; chunks are
-// assigned to (block, warp) round-robin so that all warps of the device read
-// neighbouring chunks at the same time.
+// Each warp owns kProbeRingBytes / kProbeWarps bytes of slots.  Pattern 0:
+// chunks are assigned to (block, warp) round-robin over the whole device, so
+// all warps read neighbouring chunks at the same time.  Pattern 1: each block
+// streams its own contiguous range (warps take neighbouring chunks of it),
+// the order the GEMV's split of work produces.
 __global__ void __launch_bounds__(kProbeThreads, 1) probe_bulk(const uint8_t *__restrict__ p,
                                                                int64_t nchunks, int chunk,
-                                                               int slots, uint32_t *sink,
+                                                               int slots, int pattern,
+                                                               uint32_t *sink,
                                                                uint64_t timeout_ns) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kProbeRingBytes);
@@ -59,26 +62,43 @@ __global__ void __launch_bounds__(kProbeThreads, 1) probe_bulk(const uint8_t *__
     for (int s = 0; s < slots; ++s) mbar_init(bar0 + 8 * s, 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
-  const int64_t workers = int64_t(gridDim.x) * kProbeWarps;
-  const int64_t me = int64_t(warp) * gridDim.x + blockIdx.x;
+  // pattern 2: like pattern 1, plus a second copy of chunk/8 bytes per slot
+  // from the upper eighth of the buffer (the block scales next to the codes)
+  const int side = pattern == 2 ? chunk / 8 : 0;
+  const uint8_t *sp = p + (nchunks * int64_t(chunk)) / 9 * 8;
+  if (pattern == 2) nchunks = nchunks / 9 * 8;
+  int64_t workers = int64_t(gridDim.x) * kProbeWarps;
+  int64_t next = int64_t(warp) * gridDim.x + blockIdx.x;
+  if (pattern >= 1) {
+    const int64_t per = nchunks / gridDim.x / kProbeWarps * kProbeWarps;
+    workers = kProbeWarps;
+    next = blockIdx.x * per + warp;
+    nchunks = blockIdx.x * per + per;
+  }
   const uint64_t policy = policy_evict_first();
-  int64_t next = me, issued = 0, done = 0;
+  int64_t issued = 0, done = 0;
   uint32_t acc = 0;
+  const int stride = chunk + side;
   for (int s = 0; s < slots && next < nchunks; ++s, next += workers, ++issued)
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar0 + 8 * s, uint32_t(chunk));
-      bulk_g2s(ring + s * chunk, p + next * chunk, uint32_t(chunk), bar0 + 8 * s, policy);
+      mbar_arrive_expect_tx(bar0 + 8 * s, uint32_t(chunk + side));
+      bulk_g2s(ring + s * stride, p + next * chunk, uint32_t(chunk), bar0 + 8 * s, policy);
+      if (side)
+        bulk_g2s(ring + s * stride + chunk, sp + next * side, uint32_t(side), bar0 + 8 * s, policy);
     }
   while (done < issued) {
     const int s = int(done % slots);
     if (!mbar_wait(bar0 + 8 * s, uint32_t(done / slots) & 1u, globaltimer() + timeout_ns)) break;
-    acc ^= lds64(ring + s * chunk + lane * 8).x;
+    acc ^= lds64(ring + s * stride + lane * 8).x;
     __syncwarp();
     if (next < nchunks) {
       if (lane == 0) {
         fence_proxy_async();
-        mbar_arrive_expect_tx(bar0 + 8 * s, uint32_t(chunk));
-        bulk_g2s(ring + s * chunk, p + next * chunk, uint32_t(chunk), bar0 + 8 * s, policy);
+        mbar_arrive_expect_tx(bar0 + 8 * s, uint32_t(chunk + side));
+        bulk_g2s(ring + s * stride, p + next * chunk, uint32_t(chunk), bar0 + 8 * s, policy);
+        if (side)
+          bulk_g2s(ring + s * stride + chunk, sp + next * side, uint32_t(side), bar0 + 8 * s,
+                   policy);
       }
       next += workers;
       ++issued;
@@ -100,7 +120,7 @@ using namespace vg;
 extern "C" vg_status vg_hbm_read_probe(const void *buf, size_t bytes, int mode, int chunk,
                                        int slots, uint32_t *sink, int sink_words,
                                        vg_stream_t stream) {
-  if (!buf || !sink || bytes < 4096 || (mode != 0 && mode != 1)) return VG_ERR_INVALID_ARG;
+  if (!buf || !sink || bytes < 4096 || mode < 0 || mode > 3) return VG_ERR_INVALID_ARG;
   if (!aligned16(buf) || !aligned16(sink)) return VG_ERR_ALIGNMENT;
   int dev = 0, sms = 0;
   VG_CUDA(cudaGetDevice(&dev));
@@ -115,14 +135,14 @@ extern "C" vg_status vg_hbm_read_probe(const void *buf, size_t bytes, int mode, 
                                               int64_t(bytes / 16), sink);
   } else {
     if (chunk < 256 || chunk % 256 || slots < 1 || slots > 16 ||
-        int64_t(chunk) * slots > kProbeRingBytes / kProbeWarps)
+        int64_t(chunk + (mode == 3 ? chunk / 8 : 0)) * slots > kProbeRingBytes / kProbeWarps)
       return VG_ERR_INVALID_ARG;
     if (sink_words < sms) return VG_ERR_INVALID_ARG;
     const int smem = kProbeRingBytes + kProbeWarps * 16 * 8;
     VG_CUDA(cudaFuncSetAttribute(probe_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     probe_bulk<<<sms, kProbeThreads, smem, st>>>(static_cast<const uint8_t *>(buf),
                                                  int64_t(bytes / size_t(chunk)), chunk, slots,
-                                                 sink, 2000000000ull);
+                                                 mode - 1, sink, 2000000000ull);
   }
   VG_LAUNCH_CHECK();
   return VG_OK;
