@@ -30,19 +30,18 @@ constexpr int kF8ChunkUnits = 4;
 // A row block is 16 row tiles (256 rows); a work item is one chunk of every
 // tile of a row block.  Each of the 16 consumer warps owns one tile of the
 // row block and streams its own part of every item through a private ring
-// of kSlots shared-memory slots (one slot = one tile's chunk: 4 NVFP4 units
-// + their 256 scale bytes, or 2 FP8 units).
+// of kSlots shared-memory slots (one slot = one tile's chunk: 8 NVFP4 units
+// + their 512 scale bytes, or 4 FP8 units).  The item's x slice (N rows of
+// the chunk's columns) goes once per block through a shared ring of kXSlots
+// slots.
 #ifndef VG_WARPS
 #define VG_WARPS 16
 #endif
 #ifndef VG_SLOTS
-#define VG_SLOTS 3
+#define VG_SLOTS 2
 #endif
-#ifndef VG_R3_MULHI
-#define VG_R3_MULHI 0
-#endif
-#ifndef VG_SHIFT_ALU
-#define VG_SHIFT_ALU 0
+#ifndef VG_XSLOTS
+#define VG_XSLOTS 4
 #endif
 constexpr int kBlockTiles = 16;
 constexpr int kWarps = VG_WARPS;
@@ -51,6 +50,11 @@ constexpr int kSlots = VG_SLOTS;
 constexpr int kSlotCodeBytes = kNvChunkUnits * kNvUnitBytes;          // 4096
 constexpr int kSlotBytes = kSlotCodeBytes + kNvScaleChunkBytes;        // 4608
 constexpr int kThreads = kWarps * 32;
+constexpr int kXSlots = VG_XSLOTS;
+// One x row of a chunk (512 BF16 columns) plus 16 bytes of padding, so that
+// the 8 rows read by a quarter warp fall in different banks.
+constexpr int kXRowBytes = kNvChunkUnits * kUnitK * 2 + 16;             // 1040
+constexpr int kXSlotBytes = 8 * kXRowBytes;                            // 8 rows
 
 static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
               "an FP8 chunk fills the code part of a slot");
@@ -184,6 +188,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       : "memory");
 }
 
+// Non-blocking test of a phase (never suspends the thread): for polling
+// loops whose lanes diverge, where a suspended lane would hold back others.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -222,6 +238,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
@@ -304,20 +325,9 @@ __device__ __forceinline__ void nv_decode(uint32_t w, uint32_t fg, uint32_t fg8,
                                           uint32_t m64, uint32_t &a0, uint32_t &a1,
                                           uint32_t &a2, uint32_t &a3) {
   const uint32_t r0 = w & kNvMask;
-#if VG_SHIFT_ALU
-  const uint32_t r1 = (w << 3) & kNvMask;
-  const uint32_t r2 = (w << 6) & kNvMask;
-#else
   const uint32_t r1 = umul(w, m8) & kNvMask;
   const uint32_t r2 = umul(w, m64) & kNvMask;
-#endif
-#if VG_R3_MULHI
-  uint32_t w7;
-  asm("mul.hi.u32 %0, %1, %2;" : "=r"(w7) : "r"(w), "r"(m64 << 19));
-  const uint32_t r3 = umul(w7 & kNvR3Pick, kNvR3Spread) & kNvMask;
-#else
   const uint32_t r3 = umul((w >> 7) & kNvR3Pick, kNvR3Spread) & kNvMask;
-#endif
   a0 = bmul2(r0, fg);
   a1 = bmul2(r1, fg8);
   a2 = bmul2(r2, fg);

@@ -91,11 +91,23 @@ struct Params {
 // One block's partial-sum slot: 4 FP32 sums per consumer thread, each in a
 // 64-bit word whose upper half is the tag of the pass and phase that wrote it.
 constexpr int kPartialWords = kBlockTiles * 32 * 4;
+// Shared memory: the consumer warps' rings, the x ring, one zero x row (read
+// for columns >= N), the mbarriers (full and empty per ring slot, then full
+// and empty per x slot) and a few flags.
 constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;
-constexpr int kBarBytes = 2 * kWarps * kSlots * 8;
-constexpr int kSmemBytes = kRingBytes + kBarBytes + 64;
+constexpr int kXRingBytes = kXSlots * kXSlotBytes;
+// The zero row starts 16 bytes past a 128-byte line, like x row 1 of a slot,
+// so that lanes reading it and lanes reading row 0 use different banks.
+constexpr int kZeroRowOff = kRingBytes + kXRingBytes + 16;
+constexpr int kBarOff = kZeroRowOff + kXRowBytes;
+constexpr int kNumBars = 2 * kWarps * kSlots + 2 * kXSlots;
+constexpr int kBarBytes = kNumBars * 8;
+constexpr int kSmemBytes = kBarOff + kBarBytes + 64;
+static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(kRingBytes % 128 == 0 && kXSlotBytes % 128 == 0, "x slots start 128-byte aligned");
+static_assert(kSmemBytes <= 227 * 1024, "fits one block per SM");
 constexpr int kConsumers = kWarps * 32;
-constexpr int kKernelThreads = kConsumers + 32;        // + one producer warp
+constexpr int kKernelThreads = kConsumers + 64;        // + weight and x producer warps
 constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3, kErrPartialWait = 4;
 // Header words of a workspace (GEMV) or plan state: error, finished blocks,
 // pass epoch; then, 256 bytes in, the per-phase counters (plans) and the
@@ -113,9 +125,6 @@ __device__ inline int owner(int T, int G, int i) { return int((int64_t(i + 1) * 
 
 __device__ inline void set_error(int *error, int code) { atomicCAS(error, 0, code); }
 
-// x of a column >= N is read from here (zeros), so that x loads never need a
-// per-unit condition.  Covers one chunk of a lane's columns.
-__device__ __align__(16) uint16_t g_zero_x[kNvChunkUnits * kUnitK + 16];
 
 // Bounded wait with the clock read only after a first miss.
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t timeout) {
@@ -222,12 +231,13 @@ __device__ __forceinline__ void f8_unit(const uint4 w0, const uint4 w1, const ui
   mma_bf16(acc[3 % kAcc], a0, a1, a2, a3, xb.z, xb.w);
 }
 
-// x fragment of one unit for lane (g, t): the 16 columns at xp as two
-// 16-byte loads, or zeros when `on` is false (column g >= N or K padding).
-__device__ __forceinline__ void load_x(const uint16_t *xp, bool on, uint4 &xa, uint4 &xb) {
+// x fragment of one unit for lane (g, t): its 16 columns from the shared x
+// slot (two 16-byte loads at xs), or zeros when `on` is false (column g >= N
+// or columns past K, whose slot bytes are stale).
+__device__ __forceinline__ void load_x(uint32_t xs, bool on, uint4 &xa, uint4 &xb) {
   if (on) {
-    xa = ldg128(xp);
-    xb = ldg128(xp + 8);
+    xa = lds128(xs);
+    xb = lds128(xs + 16);
   } else {
     xa = make_uint4(0, 0, 0, 0);
     xb = xa;
@@ -236,25 +246,27 @@ __device__ __forceinline__ void load_x(const uint16_t *xp, bool on, uint4 &xa, u
 
 // A whole NVFP4 chunk (8 units) of this lane's tile: scale pairs from one
 // 16-byte load, codes and x for two units at a time, the next pair loaded
-// before the current one is multiplied.  xp points at the lane's x columns,
-// or at zeros for a column >= N.
-__device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, const uint16_t *xp,
-                                              uint32_t m8, uint32_t m64, float (&acc)[kAcc][4]) {
+// before the current one is multiplied.  xs is the shared-memory address of
+// the lane's x columns in the item's x slot, or of a zero row for a column
+// >= N.
+__device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, uint32_t xs, uint32_t m8,
+                                              uint32_t m64, float (&acc)[kAcc][4]) {
+  constexpr int kXUnit = kUnitK * 2;   // bytes of one unit's columns in an x row
   const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
   const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
   uint4 w0 = lds128(slot + lane * 16), w1 = lds128(slot + kNvUnitBytes + lane * 16);
-  uint4 x0a = ldg128(xp), x0b = ldg128(xp + 8);
-  uint4 x1a = ldg128(xp + kUnitK), x1b = ldg128(xp + kUnitK + 8);
+  uint4 x0a = lds128(xs), x0b = lds128(xs + 16);
+  uint4 x1a = lds128(xs + kXUnit), x1b = lds128(xs + kXUnit + 16);
 #pragma unroll
   for (int h = 0; h < kNvChunkUnits / 2; ++h) {
     uint4 nw0, nw1, nx0a, nx0b, nx1a, nx1b;
     if (h + 1 < kNvChunkUnits / 2) {
       nw0 = lds128(slot + (2 * h + 2) * kNvUnitBytes + lane * 16);
       nw1 = lds128(slot + (2 * h + 3) * kNvUnitBytes + lane * 16);
-      nx0a = ldg128(xp + (2 * h + 2) * kUnitK);
-      nx0b = ldg128(xp + (2 * h + 2) * kUnitK + 8);
-      nx1a = ldg128(xp + (2 * h + 3) * kUnitK);
-      nx1b = ldg128(xp + (2 * h + 3) * kUnitK + 8);
+      nx0a = lds128(xs + (2 * h + 2) * kXUnit);
+      nx0b = lds128(xs + (2 * h + 2) * kXUnit + 16);
+      nx1a = lds128(xs + (2 * h + 3) * kXUnit);
+      nx1b = lds128(xs + (2 * h + 3) * kXUnit + 16);
     }
     // unit 2h uses scale bytes 0,1 of word h; unit 2h+1 bytes 2,3
     nv_unit(w0, nv_scale_pair(scw[h], 0), nv_scale_pair(scw[h], 1), x0a, x0b, m8, m64, acc);
@@ -271,14 +283,14 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, const uin
 }
 
 // A partial NVFP4 chunk (the K tail): nu units, columns checked against K.
-__device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uint16_t *xp,
-                                              bool on, int nu, int kleft, uint32_t m8,
-                                              uint32_t m64, float (&acc)[kAcc][4]) {
+__device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, uint32_t xs, bool on,
+                                              int nu, int kleft, uint32_t m8, uint32_t m64,
+                                              float (&acc)[kAcc][4]) {
   const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
   for (int u = 0; u < nu; ++u) {
     const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
     uint4 xa, xb;
-    load_x(xp + u * kUnitK, on && u * kUnitK < kleft, xa, xb);
+    load_x(xs + u * kUnitK * 2, on && u * kUnitK < kleft, xa, xb);
     const int q = u >> 1;
     const uint32_t word = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
     const uint32_t b = uint32_t(u & 1) * 2u;
@@ -287,9 +299,10 @@ __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, const uin
 }
 
 // An FP8 chunk: nu (<= 4) units of 1024 bytes.  `full`: all 4 units lie
-// inside K, so x loads need no per-unit condition.
-__device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t *xp, bool on,
-                                         bool full, int nu, int kleft, float (&acc)[kAcc][4]) {
+// inside K, so x loads need no per-unit condition (xs then points at a zero
+// row for a column >= N).
+__device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, bool on, bool full,
+                                         int nu, int kleft, float (&acc)[kAcc][4]) {
 #pragma unroll
   for (int u = 0; u < kF8ChunkUnits; ++u) {
     if (full || u < nu) {
@@ -297,10 +310,10 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t
       const uint4 w1 = lds128(slot + u * kF8UnitBytes + lane * 32 + 16);
       uint4 xa, xb;
       if (full) {
-        xa = ldg128(xp + u * kUnitK);
-        xb = ldg128(xp + u * kUnitK + 8);
+        xa = lds128(xs + u * kUnitK * 2);
+        xb = lds128(xs + u * kUnitK * 2 + 16);
       } else {
-        load_x(xp + u * kUnitK, on && u * kUnitK < kleft, xa, xb);
+        load_x(xs + u * kUnitK * 2, on && u * kUnitK < kleft, xa, xb);
       }
       f8_unit(w0, w1, xa, xb, acc);
     }
@@ -308,9 +321,7 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, const uint16_t
 }
 
 // Producer lane `tile` (0..15): refill consumer warp `tile`'s ring, one item
-// at a time, as soon as that warp has released the slot.  Lanes below N also
-// bring the item's x row into L2, during the block's first pass over the
-// matrix's chunks only (after that x is in L2 already).  The lanes of the
+// at a time, as soon as that warp has released the slot.  The lanes of the
 // producer warp progress independently: each pass of the loop a lane polls
 // its own slot once and issues only if it is free, so a slow consumer warp
 // never holds back the refills of the others.
@@ -324,9 +335,8 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   int64_t issued = 0;
   uint64_t deadline = 0;
   bool waiting = false;
-  int x_mi = -1, x_ph = -1, x_left = 0;   // x prefetches left for this matrix
   while (q.valid) {
-    if (!mbar_try_wait(empty0 + 8 * s, par ^ 1u)) {
+    if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
       const uint64_t now = globaltimer();
       if (!waiting) {
         waiting = true;
@@ -360,18 +370,6 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
         bulk_g2s(slot, m.w + off, code_bytes, full, policy);
       }
     }
-    // lane n < N also brings row n of this item's x slice into L2, so that
-    // the consumers' x loads hit L2 rather than DRAM
-    if (q.mi != x_mi || q.ph != x_ph) {
-      x_mi = q.mi;
-      x_ph = q.ph;
-      x_left = m.KC;
-    }
-    if (tile < p.N && x_left-- > 0) {
-      const int64_t k0 = int64_t(q.c) * m.cu * kUnitK;
-      const int64_t cols = i64min(int64_t(m.cu) * kUnitK, m.K - k0);
-      bulk_prefetch_l2(m.x + int64_t(tile) * m.K + k0, uint32_t(cols * 2));
-    }
     q.advance();
     ++issued;
     if (++s == kSlots) {
@@ -382,6 +380,48 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   // Never leave while a bulk copy may still be writing shared memory.
   for (int64_t k = i64max(0, issued - kSlots); k < issued; ++k)
     mbar_wait_for(full0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u, p.timeout_ns);
+}
+
+// The x producer (one lane of its own warp): copy each item's x slice, rows 0..N-1 of the chunk's
+// columns, into the block's shared x ring once all 16 consumer warps have
+// released the slot.  x is read by every block, so it is kept in L2
+// (evict-last).  Columns past K are not copied; the consumers mask them.
+__device__ void x_producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
+                           uint32_t xring, uint32_t xfull0, uint32_t xempty0) {
+  const uint64_t policy = policy_evict_last();
+  Seq q;
+  q.init(mats, phases, p.nphases, blockIdx.x, p.grid);
+  int s = 0;
+  uint32_t par = 0;
+  int64_t issued = 0;
+  while (q.valid) {
+    if (!mbar_test_wait(xempty0 + 8 * s, par ^ 1u)) {
+      const uint64_t deadline = globaltimer() + p.timeout_ns;
+      bool ok = false;
+      while (!(ok = mbar_test_wait(xempty0 + 8 * s, par ^ 1u)) && globaltimer() <= deadline) {
+      }
+      if (!ok) {
+        set_error(p.error, kErrEmptyWait);
+        break;
+      }
+    }
+    const MatDev &m = mats[q.mi];
+    const int k0 = q.c * m.cu * kUnitK;
+    const uint32_t bytes = uint32_t(min(m.cu * kUnitK, m.K - k0) * 2);
+    const uint32_t full = xfull0 + 8 * s;
+    mbar_arrive_expect_tx(full, bytes * uint32_t(p.N));
+    for (int n = 0; n < p.N; ++n)
+      bulk_g2s(xring + s * kXSlotBytes + n * kXRowBytes, m.x + int64_t(n) * m.K + k0, bytes, full,
+               policy);
+    q.advance();
+    ++issued;
+    if (++s == kXSlots) {
+      s = 0;
+      par ^= 1u;
+    }
+  }
+  for (int64_t k = i64max(0, issued - kXSlots); k < issued; ++k)
+    mbar_wait_for(xfull0 + 8 * int(k % kXSlots), uint32_t(k / kXSlots) & 1u, p.timeout_ns);
 }
 
 // The reducer of a split row block adds the partial sums of the other
@@ -487,17 +527,21 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
 
 __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
-  volatile int *sflag = reinterpret_cast<volatile int *>(smem + kRingBytes + kBarBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
+  volatile int *sflag = reinterpret_cast<volatile int *>(smem + kBarOff + kBarBytes);
+  uint64_t *xbars = bars + 2 * kWarps * kSlots;       // x full [kXSlots], x empty [kXSlots]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const MatDev *mats = p.mats ? p.mats : &p.mat0;
   const PhaseDev *phases = p.mats ? p.phases : &p.phase0;
 
-  if (tid < kWarps * kSlots) {
-    mbar_init(smem_addr(bars + tid), 1);                       // full
-    mbar_init(smem_addr(bars + kWarps * kSlots + tid), 1);     // empty
-  }
+  if (tid * 16 < kXRowBytes)
+    *reinterpret_cast<uint4 *>(smem + kZeroRowOff + tid * 16) = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
+    for (int i = 0; i < 2 * kWarps * kSlots; ++i) mbar_init(smem_addr(bars + i), 1);
+    for (int i = 0; i < kXSlots; ++i) {
+      mbar_init(smem_addr(xbars + i), 1);                      // x full: the x producer
+      mbar_init(smem_addr(xbars + kXSlots + i), kWarps);       // x empty: every consumer warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sflag[0] = 0;
     sflag[1] = int(ld_relaxed(p.epoch));
@@ -507,10 +551,15 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   const uint32_t epoch = uint32_t(sflag[1]);
 
   if (warp == kWarps) {
-    // ================================================================ producer
+    // ========================================================= weight producer
     if (lane < kBlockTiles)
       producer(p, mats, phases, lane, smem_addr(smem + lane * kSlots * kSlotBytes),
                smem_addr(bars + lane * kSlots), smem_addr(bars + kWarps * kSlots + lane * kSlots));
+  } else if (warp == kWarps + 1) {
+    // ============================================================== x producer
+    if (lane == 0)
+      x_producer(p, mats, phases, smem_addr(smem + kRingBytes), smem_addr(xbars),
+                 smem_addr(xbars + kXSlots));
 
   } else {
     // =============================================================== consumers
@@ -520,18 +569,23 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     const uint32_t ring = smem_addr(smem + warp * kSlots * kSlotBytes);
     const uint32_t full0 = smem_addr(bars + warp * kSlots);
     const uint32_t empty0 = smem_addr(bars + kWarps * kSlots + warp * kSlots);
+    const uint32_t xfull0 = smem_addr(xbars), xempty0 = smem_addr(xbars + kXSlots);
+    // this lane's x columns inside an x slot, or the zero row for g >= N
+    const uint32_t xlane = uint32_t(g * kXRowBytes + t * 32);
+    const uint32_t xzero = smem_addr(smem + kZeroRowOff) + t * 32;
+    const uint32_t xring = smem_addr(smem + kRingBytes);
     Seq cons;
     cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
     bool aborted = false;
     int s = 0;                     // ring slot of the current item
     uint32_t par = 0;              // parity of that slot's current phase
-    int cur_ph = -1, cur_mi = -1;
+    int xsl = 0;                   // x slot of the current item
+    uint32_t xpar = 0;    int cur_ph = -1, cur_mi = -1;
     uint32_t tag = 0;              // tag of this pass and phase
     int piece_start = 0;
     int piece_c0 = 0;
     float acc[kAcc][4];
     // matrix fields cached while the matrix does not change
-    const uint16_t *xbase = nullptr;
     int K = 0, KU = 0, MT = 0, fmt = 0;
     while (cons.valid) {
       const int ph = cons.ph;
@@ -575,7 +629,6 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         KU = mm.KU;
         MT = mm.MT;
         fmt = mm.fmt;
-        xbase = mm.x + int64_t(g) * K + 16 * t;
       }
       const int rb = cons.rb, c = cons.c;
       if (c == 0 || cons.i == cons.i0) {
@@ -591,35 +644,44 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
       if (!aborted) {
         // every lane polls; a lane whose wait ran out stops the whole warp,
         // since mma.sync needs all of it
-        const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
+        const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns) &&
+                           mbar_wait_for(xfull0 + 8 * xsl, xpar, p.timeout_ns);
         if (!__all_sync(0xFFFFFFFFu, ready)) {
           if (lane == 0) set_error(p.error, kErrFullWait);
           aborted = true;
         }
       }
       if (!aborted && mt < MT) {
+        const uint32_t xs = on ? xring + xsl * kXSlotBytes + xlane : xzero;
         if (fmt == VG_FMT_NVFP4) {
           const int kc = c * (kNvChunkUnits * kUnitK);
           // warp-uniform test (mma.sync needs the whole warp): the chunk's
           // whole column range lies inside K
           if (kc + kNvChunkUnits * kUnitK <= K)
-            nv_chunk_full(slot, lane, on ? xbase + kc : g_zero_x, p.m8, p.m64, acc);
+            nv_chunk_full(slot, lane, xs, p.m8, p.m64, acc);
           else
-            nv_chunk_tail(slot, lane, xbase + kc, on, min(kNvChunkUnits, KU - c * kNvChunkUnits),
+            nv_chunk_tail(slot, lane, xs, on, min(kNvChunkUnits, KU - c * kNvChunkUnits),
                           K - kc - 16 * t, p.m8, p.m64, acc);
         } else {
           const int kc = c * (kF8ChunkUnits * kUnitK);
           const bool full = kc + kF8ChunkUnits * kUnitK <= K;
-          f8_chunk(slot, lane, full && !on ? g_zero_x : xbase + kc, on, full,
-                   min(kF8ChunkUnits, KU - c * kF8ChunkUnits), K - kc - 16 * t, acc);
+          f8_chunk(slot, lane, xs, on, full, min(kF8ChunkUnits, KU - c * kF8ChunkUnits),
+                   K - kc - 16 * t, acc);
         }
       }
-      // release the slot to the producer (every lane has read it)
+      // release the slots to the producers (every lane has read them)
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (lane == 0) {
+        mbar_arrive(empty0 + 8 * s);
+        mbar_arrive(xempty0 + 8 * xsl);
+      }
       if (++s == kSlots) {
         s = 0;
         par ^= 1u;
+      }
+      if (++xsl == kXSlots) {
+        xsl = 0;
+        xpar ^= 1u;
       }
 
       // ---------------------------------------------- end of a row-block piece
