@@ -29,32 +29,29 @@ constexpr int kF8ChunkUnits = 4;
 
 // A row block is 16 row tiles (256 rows); a work item is one chunk of every
 // tile of a row block.  Each of the 16 consumer warps owns one tile of the
-// row block and streams its own part of every item through a private ring
-// of kSlots shared-memory slots (one slot = one tile's chunk: 8 NVFP4 units
-// + their 512 scale bytes, or 4 FP8 units).  The item's x slice (N rows of
-// the chunk's columns) goes once per block through a shared ring of kXSlots
-// slots.
+// row block.  Items stream through a ring of kSlots shared-memory slots; one
+// slot holds a whole item: the 16 tiles' codes (8 NVFP4 units or 4 FP8 units
+// each, contiguous in the packed buffer), their block scales, and the x
+// slice (N rows of the chunk's columns).
 #ifndef VG_WARPS
 #define VG_WARPS 16
 #endif
 #ifndef VG_SLOTS
 #define VG_SLOTS 2
 #endif
-#ifndef VG_XSLOTS
-#define VG_XSLOTS 4
-#endif
 constexpr int kBlockTiles = 16;
 constexpr int kWarps = VG_WARPS;
 static_assert(kWarps == kBlockTiles, "one tile of the row block per warp");
 constexpr int kSlots = VG_SLOTS;
-constexpr int kSlotCodeBytes = kNvChunkUnits * kNvUnitBytes;          // 4096
-constexpr int kSlotBytes = kSlotCodeBytes + kNvScaleChunkBytes;        // 4608
+constexpr int kSlotCodeBytes = kNvChunkUnits * kNvUnitBytes;          // 4096: one tile's chunk
 constexpr int kThreads = kWarps * 32;
-constexpr int kXSlots = VG_XSLOTS;
 // One x row of a chunk (512 BF16 columns) plus 16 bytes of padding, so that
 // the 8 rows read by a quarter warp fall in different banks.
 constexpr int kXRowBytes = kNvChunkUnits * kUnitK * 2 + 16;             // 1040
-constexpr int kXSlotBytes = 8 * kXRowBytes;                            // 8 rows
+// An item slot: codes of 16 tiles, then their scales, then 8 x rows.
+constexpr int kItemScaleOff = kBlockTiles * kSlotCodeBytes;            // 65536
+constexpr int kItemXOff = kItemScaleOff + kBlockTiles * kNvScaleChunkBytes;  // 73728
+constexpr int kItemSlotBytes = kItemXOff + 8 * kXRowBytes;              // 82048
 
 static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
               "an FP8 chunk fills the code part of a slot");

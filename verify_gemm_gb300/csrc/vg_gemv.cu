@@ -91,23 +91,20 @@ struct Params {
 // One block's partial-sum slot: 4 FP32 sums per consumer thread, each in a
 // 64-bit word whose upper half is the tag of the pass and phase that wrote it.
 constexpr int kPartialWords = kBlockTiles * 32 * 4;
-// Shared memory: the consumer warps' rings, the x ring, one zero x row (read
-// for columns >= N), the mbarriers (full and empty per ring slot, then full
-// and empty per x slot) and a few flags.
-constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;
-constexpr int kXRingBytes = kXSlots * kXSlotBytes;
+// Shared memory: the item ring, one zero x row (read for columns >= N), the
+// mbarriers (full, then empty, per slot) and a few flags.
+constexpr int kRingBytes = kSlots * kItemSlotBytes;
 // The zero row starts 16 bytes past a 128-byte line, like x row 1 of a slot,
 // so that lanes reading it and lanes reading row 0 use different banks.
-constexpr int kZeroRowOff = kRingBytes + kXRingBytes + 16;
+constexpr int kZeroRowOff = kRingBytes + 16;
 constexpr int kBarOff = kZeroRowOff + kXRowBytes;
-constexpr int kNumBars = 2 * kWarps * kSlots + 2 * kXSlots;
-constexpr int kBarBytes = kNumBars * 8;
+constexpr int kBarBytes = 2 * kSlots * 8;
 constexpr int kSmemBytes = kBarOff + kBarBytes + 64;
 static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
-static_assert(kRingBytes % 128 == 0 && kXSlotBytes % 128 == 0, "x slots start 128-byte aligned");
+static_assert(kItemSlotBytes % 128 == 0 && kItemXOff % 128 == 0, "x rows start 128-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024, "fits one block per SM");
 constexpr int kConsumers = kWarps * 32;
-constexpr int kKernelThreads = kConsumers + 64;        // + weight and x producer warps
+constexpr int kKernelThreads = kConsumers + 32;        // + the producer warp
 constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3, kErrPartialWait = 4;
 // Header words of a workspace (GEMV) or plan state: error, finished blocks,
 // pass epoch; then, 256 bytes in, the per-phase counters (plans) and the
@@ -246,13 +243,13 @@ __device__ __forceinline__ void load_x(uint32_t xs, bool on, uint4 &xa, uint4 &x
 
 // A whole NVFP4 chunk (8 units) of this lane's tile: scale pairs from one
 // 16-byte load, codes and x for two units at a time, the next pair loaded
-// before the current one is multiplied.  xs is the shared-memory address of
-// the lane's x columns in the item's x slot, or of a zero row for a column
-// >= N.
-__device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, uint32_t xs, uint32_t m8,
-                                              uint32_t m64, float (&acc)[kAcc][4]) {
+// before the current one is multiplied.  slot, scl: shared-memory addresses
+// of the tile's codes and scales in the item slot; xs: the lane's x columns
+// in the slot, or a zero row for a column >= N.
+__device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                              uint32_t m8, uint32_t m64, float (&acc)[kAcc][4]) {
   constexpr int kXUnit = kUnitK * 2;   // bytes of one unit's columns in an x row
-  const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
+  const uint4 sc = lds128(scl + lane * kNvScaleLaneBytes);
   const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
   uint4 w0 = lds128(slot + lane * 16), w1 = lds128(slot + kNvUnitBytes + lane * 16);
   uint4 x0a = lds128(xs), x0b = lds128(xs + 16);
@@ -283,10 +280,10 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, int lane, uint32_t 
 }
 
 // A partial NVFP4 chunk (the K tail): nu units, columns checked against K.
-__device__ __forceinline__ void nv_chunk_tail(uint32_t slot, int lane, uint32_t xs, bool on,
-                                              int nu, int kleft, uint32_t m8, uint32_t m64,
+__device__ __forceinline__ void nv_chunk_tail(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                              bool on, int nu, int kleft, uint32_t m8, uint32_t m64,
                                               float (&acc)[kAcc][4]) {
-  const uint4 sc = lds128(slot + kSlotCodeBytes + lane * kNvScaleLaneBytes);
+  const uint4 sc = lds128(scl + lane * kNvScaleLaneBytes);
   for (int u = 0; u < nu; ++u) {
     const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
     uint4 xa, xb;
@@ -320,56 +317,56 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, b
   }
 }
 
-// Producer lane `tile` (0..15): refill consumer warp `tile`'s ring, one item
-// at a time, as soon as that warp has released the slot.  The lanes of the
-// producer warp progress independently: each pass of the loop a lane polls
-// its own slot once and issues only if it is free, so a slow consumer warp
-// never holds back the refills of the others.
-__device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases, int tile,
+// Byte offsets of tile `tile`'s codes and scales in item (rb, c) of m.
+__device__ __forceinline__ int64_t code_off(const MatDev &m, int rb, int c, int tiles, int tile,
+                                            int nu) {
+  return int64_t(rb) * m.rb_bytes + int64_t(c) * tiles * m.cu * m.ub + int64_t(tile) * nu * m.ub;
+}
+__device__ __forceinline__ int64_t scale_off(const MatDev &m, int rb, int c, int tiles, int tile) {
+  return (int64_t(rb) * kBlockTiles * m.KC + int64_t(c) * tiles + tile) * kNvScaleChunkBytes;
+}
+
+// The producer (one lane): fill the item ring, one whole item per slot, as
+// soon as all 16 consumer warps have released the slot.  An item's codes are
+// one contiguous range of the packed buffer and its scales another, so an
+// item is two bulk copies (L2 evict-first: read once) plus one per x row (x
+// is read by every block: evict-last).  Columns past K are not copied; the
+// consumers mask them.
+__device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0) {
-  const uint64_t policy = policy_evict_first();
+  const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
   Seq q;
   q.init(mats, phases, p.nphases, blockIdx.x, p.grid);
   int s = 0;
   uint32_t par = 0;
   int64_t issued = 0;
-  uint64_t deadline = 0;
-  bool waiting = false;
   while (q.valid) {
     if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
-      const uint64_t now = globaltimer();
-      if (!waiting) {
-        waiting = true;
-        deadline = now + p.timeout_ns;
-      } else if (now > deadline) {
+      const uint64_t deadline = globaltimer() + p.timeout_ns;
+      bool ok = false;
+      while (!(ok = mbar_test_wait(empty0 + 8 * s, par ^ 1u)) && globaltimer() <= deadline) {
+      }
+      if (!ok) {
         set_error(p.error, kErrEmptyWait);
         break;
       }
-      continue;
     }
-    waiting = false;
     const MatDev &m = mats[q.mi];
-    const uint32_t full = full0 + 8 * s;
     const int tiles = min(kBlockTiles, m.MT - q.rb * kBlockTiles);
-    if (tile >= tiles) {
-      mbar_arrive_expect_tx(full, 0);
-    } else {
-      const int nu = min(m.cu, m.KU - q.c * m.cu);
-      const uint32_t code_bytes = uint32_t(nu * m.ub);
-      const int64_t off = int64_t(q.rb) * m.rb_bytes + int64_t(q.c) * tiles * m.cu * m.ub +
-                          int64_t(tile) * nu * m.ub;
-      const uint32_t slot = ring + s * kSlotBytes;
-      if (m.fmt == VG_FMT_NVFP4) {
-        mbar_arrive_expect_tx(full, code_bytes + kNvScaleChunkBytes);
-        bulk_g2s(slot, m.w + off, code_bytes, full, policy);
-        const int64_t soff =
-            (int64_t(q.rb) * kBlockTiles * m.KC + int64_t(q.c) * tiles + tile) * kNvScaleChunkBytes;
-        bulk_g2s(slot + kSlotCodeBytes, m.sc + soff, kNvScaleChunkBytes, full, policy);
-      } else {
-        mbar_arrive_expect_tx(full, code_bytes);
-        bulk_g2s(slot, m.w + off, code_bytes, full, policy);
-      }
-    }
+    const int nu = min(m.cu, m.KU - q.c * m.cu);
+    const uint32_t code_bytes = uint32_t(tiles * nu * m.ub);
+    const uint32_t scale_bytes = m.fmt == VG_FMT_NVFP4 ? uint32_t(tiles * kNvScaleChunkBytes) : 0u;
+    const int k0 = q.c * m.cu * kUnitK;
+    const uint32_t x_bytes = uint32_t(min(m.cu * kUnitK, m.K - k0) * 2);
+    const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
+    mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes * uint32_t(p.N));
+    bulk_g2s(slot, m.w + code_off(m, q.rb, q.c, tiles, 0, nu), code_bytes, full, pol_w);
+    if (scale_bytes)
+      bulk_g2s(slot + kItemScaleOff, m.sc + scale_off(m, q.rb, q.c, tiles, 0), scale_bytes, full,
+               pol_w);
+    for (int n = 0; n < p.N; ++n)
+      bulk_g2s(slot + kItemXOff + n * kXRowBytes, m.x + int64_t(n) * m.K + k0, x_bytes, full,
+               pol_x);
     q.advance();
     ++issued;
     if (++s == kSlots) {
@@ -380,48 +377,6 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   // Never leave while a bulk copy may still be writing shared memory.
   for (int64_t k = i64max(0, issued - kSlots); k < issued; ++k)
     mbar_wait_for(full0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u, p.timeout_ns);
-}
-
-// The x producer (one lane of its own warp): copy each item's x slice, rows 0..N-1 of the chunk's
-// columns, into the block's shared x ring once all 16 consumer warps have
-// released the slot.  x is read by every block, so it is kept in L2
-// (evict-last).  Columns past K are not copied; the consumers mask them.
-__device__ void x_producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
-                           uint32_t xring, uint32_t xfull0, uint32_t xempty0) {
-  const uint64_t policy = policy_evict_last();
-  Seq q;
-  q.init(mats, phases, p.nphases, blockIdx.x, p.grid);
-  int s = 0;
-  uint32_t par = 0;
-  int64_t issued = 0;
-  while (q.valid) {
-    if (!mbar_test_wait(xempty0 + 8 * s, par ^ 1u)) {
-      const uint64_t deadline = globaltimer() + p.timeout_ns;
-      bool ok = false;
-      while (!(ok = mbar_test_wait(xempty0 + 8 * s, par ^ 1u)) && globaltimer() <= deadline) {
-      }
-      if (!ok) {
-        set_error(p.error, kErrEmptyWait);
-        break;
-      }
-    }
-    const MatDev &m = mats[q.mi];
-    const int k0 = q.c * m.cu * kUnitK;
-    const uint32_t bytes = uint32_t(min(m.cu * kUnitK, m.K - k0) * 2);
-    const uint32_t full = xfull0 + 8 * s;
-    mbar_arrive_expect_tx(full, bytes * uint32_t(p.N));
-    for (int n = 0; n < p.N; ++n)
-      bulk_g2s(xring + s * kXSlotBytes + n * kXRowBytes, m.x + int64_t(n) * m.K + k0, bytes, full,
-               policy);
-    q.advance();
-    ++issued;
-    if (++s == kXSlots) {
-      s = 0;
-      par ^= 1u;
-    }
-  }
-  for (int64_t k = i64max(0, issued - kXSlots); k < issued; ++k)
-    mbar_wait_for(xfull0 + 8 * int(k % kXSlots), uint32_t(k / kXSlots) & 1u, p.timeout_ns);
 }
 
 // The reducer of a split row block adds the partial sums of the other
@@ -529,7 +484,6 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
   volatile int *sflag = reinterpret_cast<volatile int *>(smem + kBarOff + kBarBytes);
-  uint64_t *xbars = bars + 2 * kWarps * kSlots;       // x full [kXSlots], x empty [kXSlots]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const MatDev *mats = p.mats ? p.mats : &p.mat0;
   const PhaseDev *phases = p.mats ? p.phases : &p.phase0;
@@ -537,10 +491,9 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   if (tid * 16 < kXRowBytes)
     *reinterpret_cast<uint4 *>(smem + kZeroRowOff + tid * 16) = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
-    for (int i = 0; i < 2 * kWarps * kSlots; ++i) mbar_init(smem_addr(bars + i), 1);
-    for (int i = 0; i < kXSlots; ++i) {
-      mbar_init(smem_addr(xbars + i), 1);                      // x full: the x producer
-      mbar_init(smem_addr(xbars + kXSlots + i), kWarps);       // x empty: every consumer warp
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_addr(bars + i), 1);                       // full: the producer
+      mbar_init(smem_addr(bars + kSlots + i), kWarps);         // empty: every consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sflag[0] = 0;
@@ -551,36 +504,26 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   const uint32_t epoch = uint32_t(sflag[1]);
 
   if (warp == kWarps) {
-    // ========================================================= weight producer
-    if (lane < kBlockTiles)
-      producer(p, mats, phases, lane, smem_addr(smem + lane * kSlots * kSlotBytes),
-               smem_addr(bars + lane * kSlots), smem_addr(bars + kWarps * kSlots + lane * kSlots));
-  } else if (warp == kWarps + 1) {
-    // ============================================================== x producer
+    // ================================================================ producer
     if (lane == 0)
-      x_producer(p, mats, phases, smem_addr(smem + kRingBytes), smem_addr(xbars),
-                 smem_addr(xbars + kXSlots));
+      producer(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots));
 
   } else {
     // =============================================================== consumers
     const int g = lane >> 2, t = lane & 3;
     const int N = p.N;
     const bool on = g < N;
-    const uint32_t ring = smem_addr(smem + warp * kSlots * kSlotBytes);
-    const uint32_t full0 = smem_addr(bars + warp * kSlots);
-    const uint32_t empty0 = smem_addr(bars + kWarps * kSlots + warp * kSlots);
-    const uint32_t xfull0 = smem_addr(xbars), xempty0 = smem_addr(xbars + kXSlots);
-    // this lane's x columns inside an x slot, or the zero row for g >= N
-    const uint32_t xlane = uint32_t(g * kXRowBytes + t * 32);
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kSlots);
+    // this lane's x columns inside an item slot, or the zero row for g >= N
+    const uint32_t xlane = uint32_t(kItemXOff + g * kXRowBytes + t * 32);
     const uint32_t xzero = smem_addr(smem + kZeroRowOff) + t * 32;
-    const uint32_t xring = smem_addr(smem + kRingBytes);
     Seq cons;
     cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
     bool aborted = false;
     int s = 0;                     // ring slot of the current item
     uint32_t par = 0;              // parity of that slot's current phase
-    int xsl = 0;                   // x slot of the current item
-    uint32_t xpar = 0;    int cur_ph = -1, cur_mi = -1;
+    int cur_ph = -1, cur_mi = -1;
     uint32_t tag = 0;              // tag of this pass and phase
     int piece_start = 0;
     int piece_c0 = 0;
@@ -639,49 +582,44 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
       }
-      const uint32_t slot = ring + s * kSlotBytes;
+      const uint32_t item = ring + s * kItemSlotBytes;
       const int mt = rb * kBlockTiles + warp;
       if (!aborted) {
         // every lane polls; a lane whose wait ran out stops the whole warp,
         // since mma.sync needs all of it
-        const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns) &&
-                           mbar_wait_for(xfull0 + 8 * xsl, xpar, p.timeout_ns);
+        const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
         if (!__all_sync(0xFFFFFFFFu, ready)) {
           if (lane == 0) set_error(p.error, kErrFullWait);
           aborted = true;
         }
       }
       if (!aborted && mt < MT) {
-        const uint32_t xs = on ? xring + xsl * kXSlotBytes + xlane : xzero;
+        const uint32_t xs = on ? item + xlane : xzero;
         if (fmt == VG_FMT_NVFP4) {
           const int kc = c * (kNvChunkUnits * kUnitK);
+          const uint32_t scl = item + kItemScaleOff + warp * kNvScaleChunkBytes;
           // warp-uniform test (mma.sync needs the whole warp): the chunk's
           // whole column range lies inside K
-          if (kc + kNvChunkUnits * kUnitK <= K)
-            nv_chunk_full(slot, lane, xs, p.m8, p.m64, acc);
-          else
-            nv_chunk_tail(slot, lane, xs, on, min(kNvChunkUnits, KU - c * kNvChunkUnits),
-                          K - kc - 16 * t, p.m8, p.m64, acc);
+          if (kc + kNvChunkUnits * kUnitK <= K) {
+            nv_chunk_full(item + warp * kSlotCodeBytes, scl, lane, xs, p.m8, p.m64, acc);
+          } else {
+            const int nu = min(kNvChunkUnits, KU - c * kNvChunkUnits);
+            nv_chunk_tail(item + warp * nu * kNvUnitBytes, scl, lane, xs, on, nu, K - kc - 16 * t,
+                          p.m8, p.m64, acc);
+          }
         } else {
           const int kc = c * (kF8ChunkUnits * kUnitK);
           const bool full = kc + kF8ChunkUnits * kUnitK <= K;
-          f8_chunk(slot, lane, xs, on, full, min(kF8ChunkUnits, KU - c * kF8ChunkUnits),
-                   K - kc - 16 * t, acc);
+          const int nu = min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
+          f8_chunk(item + warp * nu * kF8UnitBytes, lane, xs, on, full, nu, K - kc - 16 * t, acc);
         }
       }
-      // release the slots to the producers (every lane has read them)
+      // release the slot to the producer once every warp has read it
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty0 + 8 * s);
-        mbar_arrive(xempty0 + 8 * xsl);
-      }
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
       if (++s == kSlots) {
         s = 0;
         par ^= 1u;
-      }
-      if (++xsl == kXSlots) {
-        xsl = 0;
-        xpar ^= 1u;
       }
 
       // ---------------------------------------------- end of a row-block piece
