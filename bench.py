@@ -317,7 +317,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": WORKLOAD, "N": args.N, "mode": "ordered",
                        "bytes_per_pass": nbytes, "matrices": len(st.mats),
                        "pct_of_8TBps": round(100 * value / world / 8000, 1),
-                       "l2": "inputs 16.3 GB per pass >> 126 MB L2; no flush needed",
+                       "l2": "inputs 16.3 GB per pass >> 129 MB L2; no flush needed",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
