@@ -48,10 +48,14 @@ constexpr int kThreads = kWarps * 32;
 // One x row of a chunk (512 BF16 columns) plus 16 bytes of padding, so that
 // the 8 rows read by a quarter warp fall in different banks.
 constexpr int kXRowBytes = kNvChunkUnits * kUnitK * 2 + 16;             // 1040
-// An item slot: codes of 16 tiles, then their scales, then 8 x rows.
+// An item slot: codes of 16 tiles, then their scales, then the x slice: 8
+// rows, either padded rows of kXRowBytes (copied row by row) or one tensor
+// copy in the 128-byte-swizzled layout [unit][row][128 B], which needs
+// 1024-byte alignment (slots are multiples of 1024 bytes).
 constexpr int kItemScaleOff = kBlockTiles * kSlotCodeBytes;            // 65536
 constexpr int kItemXOff = kItemScaleOff + kBlockTiles * kNvScaleChunkBytes;  // 73728
-constexpr int kItemSlotBytes = kItemXOff + 8 * kXRowBytes;              // 82048
+constexpr int kItemSlotBytes = (kItemXOff + 8 * kXRowBytes + 1023) / 1024 * 1024;  // 82944
+static_assert(kItemXOff % 1024 == 0, "the swizzled x slice starts 1024-byte aligned");
 
 static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
               "an FP8 chunk fills the code part of a slot");
@@ -224,6 +228,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
       "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Tensor copy of a 3-D box at coordinates (c0, c1, c2) described by the
+// tensor map at `tmap` (param, const or global memory) into shared memory,
+// completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_tensor_3d(uint32_t dst, const void *tmap, int c0, int c1,
+                                               int c2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
       : "memory");
 }
 

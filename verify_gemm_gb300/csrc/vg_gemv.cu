@@ -33,8 +33,10 @@
 //    while the producer keeps prefetching group g's weights.  All waits are
 //    bounded by a timeout on %globaltimer and report an error word instead
 //    of hanging.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -59,6 +61,7 @@ struct MatDev {
   int cu, ub;        // units per chunk, bytes per unit
   int64_t rb_bytes;  // code bytes of a full row block (16 tiles x KU units)
   int item0;         // first item of this matrix within its phase
+  const CUtensorMap *xmap;  // x as [K/64 units][N rows][64 columns], or nullptr
 };
 
 // Item counts fit 32 bits: a matrix has fewer than 2^40 / (256 x 512) items
@@ -70,6 +73,7 @@ struct PhaseDev {
 };
 
 struct Params {
+  CUtensorMap xmap0;        // the single product's x tensor map (if x0_tensor)
   const MatDev *mats;       // nullptr: use mat0 / phase0
   const PhaseDev *phases;
   int nphases;
@@ -84,6 +88,7 @@ struct Params {
   uint32_t *done;           // per-phase completed row blocks (ordered only)
   uint64_t *partials;       // [grid][kPartialWords]: tagged FP32 partial sums
   uint32_t m8, m64;         // 8 and 64: shift multipliers kept in registers
+  int x0_tensor;
   MatDev mat0;
   PhaseDev phase0;
 };
@@ -99,7 +104,8 @@ constexpr int kRingBytes = kSlots * kItemSlotBytes;
 constexpr int kZeroRowOff = kRingBytes + 16;
 constexpr int kBarOff = kZeroRowOff + kXRowBytes;
 constexpr int kBarBytes = 2 * kSlots * 8;
-constexpr int kSmemBytes = kBarOff + kBarBytes + 64;
+constexpr int kSmemUsed = kBarOff + kBarBytes + 64;
+constexpr int kSmemBytes = kSmemUsed + 1024;   // room to align the base to 1024 bytes
 static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
 static_assert(kItemSlotBytes % 128 == 0 && kItemXOff % 128 == 0, "x rows start 128-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024, "fits one block per SM");
@@ -231,10 +237,10 @@ __device__ __forceinline__ void f8_unit(const uint4 w0, const uint4 w1, const ui
 // x fragment of one unit for lane (g, t): its 16 columns from the shared x
 // slot (two 16-byte loads at xs), or zeros when `on` is false (column g >= N
 // or columns past K, whose slot bytes are stale).
-__device__ __forceinline__ void load_x(uint32_t xs, bool on, uint4 &xa, uint4 &xb) {
+__device__ __forceinline__ void load_x(uint32_t xs, int xd, bool on, uint4 &xa, uint4 &xb) {
   if (on) {
     xa = lds128(xs);
-    xb = lds128(xs + 16);
+    xb = lds128(xs + xd);
   } else {
     xa = make_uint4(0, 0, 0, 0);
     xb = xa;
@@ -244,16 +250,21 @@ __device__ __forceinline__ void load_x(uint32_t xs, bool on, uint4 &xa, uint4 &x
 // A whole NVFP4 chunk (8 units) of this lane's tile: scale pairs from one
 // 16-byte load, codes and x for two units at a time, the next pair loaded
 // before the current one is multiplied.  slot, scl: shared-memory addresses
-// of the tile's codes and scales in the item slot; xs: the lane's x columns
-// in the slot, or a zero row for a column >= N.
+// of the tile's codes and scales in the item slot; xs: the lane's first 16
+// x columns of unit 0 in the slot (or in a zero row for a column >= N).
+// kTensorX: the slice is tensor-copied (units 1024 bytes apart, the next 16
+// columns at xd_t = +-16), else row-copied (units 128 bytes apart, +16).
+template <bool kTensorX>
 __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
-                                              uint32_t m8, uint32_t m64, float (&acc)[kAcc][4]) {
-  constexpr int kXUnit = kUnitK * 2;   // bytes of one unit's columns in an x row
+                                              int xd_t, uint32_t m8, uint32_t m64,
+                                              float (&acc)[kAcc][4]) {
+  constexpr int kXUnit = kTensorX ? 1024 : kUnitK * 2;
+  const int xd = kTensorX ? xd_t : 16;
   const uint4 sc = lds128(scl + lane * kNvScaleLaneBytes);
   const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
   uint4 w0 = lds128(slot + lane * 16), w1 = lds128(slot + kNvUnitBytes + lane * 16);
-  uint4 x0a = lds128(xs), x0b = lds128(xs + 16);
-  uint4 x1a = lds128(xs + kXUnit), x1b = lds128(xs + kXUnit + 16);
+  uint4 x0a = lds128(xs), x0b = lds128(xs + xd);
+  uint4 x1a = lds128(xs + kXUnit), x1b = lds128(xs + kXUnit + xd);
 #pragma unroll
   for (int h = 0; h < kNvChunkUnits / 2; ++h) {
     uint4 nw0, nw1, nx0a, nx0b, nx1a, nx1b;
@@ -261,9 +272,9 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int l
       nw0 = lds128(slot + (2 * h + 2) * kNvUnitBytes + lane * 16);
       nw1 = lds128(slot + (2 * h + 3) * kNvUnitBytes + lane * 16);
       nx0a = lds128(xs + (2 * h + 2) * kXUnit);
-      nx0b = lds128(xs + (2 * h + 2) * kXUnit + 16);
+      nx0b = lds128(xs + (2 * h + 2) * kXUnit + xd);
       nx1a = lds128(xs + (2 * h + 3) * kXUnit);
-      nx1b = lds128(xs + (2 * h + 3) * kXUnit + 16);
+      nx1b = lds128(xs + (2 * h + 3) * kXUnit + xd);
     }
     // unit 2h uses scale bytes 0,1 of word h; unit 2h+1 bytes 2,3
     nv_unit(w0, nv_scale_pair(scw[h], 0), nv_scale_pair(scw[h], 1), x0a, x0b, m8, m64, acc);
@@ -281,13 +292,13 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int l
 
 // A partial NVFP4 chunk (the K tail): nu units, columns checked against K.
 __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
-                                              bool on, int nu, int kleft, uint32_t m8, uint32_t m64,
-                                              float (&acc)[kAcc][4]) {
+                                              int xu, int xd, bool on, int nu, int kleft,
+                                              uint32_t m8, uint32_t m64, float (&acc)[kAcc][4]) {
   const uint4 sc = lds128(scl + lane * kNvScaleLaneBytes);
   for (int u = 0; u < nu; ++u) {
     const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
     uint4 xa, xb;
-    load_x(xs + u * kUnitK * 2, on && u * kUnitK < kleft, xa, xb);
+    load_x(xs + u * xu, xd, on && u * kUnitK < kleft, xa, xb);
     const int q = u >> 1;
     const uint32_t word = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
     const uint32_t b = uint32_t(u & 1) * 2u;
@@ -298,8 +309,11 @@ __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, uint32_t scl, int l
 // An FP8 chunk: nu (<= 4) units of 1024 bytes.  `full`: all 4 units lie
 // inside K, so x loads need no per-unit condition (xs then points at a zero
 // row for a column >= N).
-__device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, bool on, bool full,
-                                         int nu, int kleft, float (&acc)[kAcc][4]) {
+template <bool kTensorX>
+__device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, int xd_t, bool on,
+                                         bool full, int nu, int kleft, float (&acc)[kAcc][4]) {
+  constexpr int XU = kTensorX ? 1024 : kUnitK * 2;
+  const int xd = kTensorX ? xd_t : 16;
 #pragma unroll
   for (int u = 0; u < kF8ChunkUnits; ++u) {
     if (full || u < nu) {
@@ -307,10 +321,10 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, b
       const uint4 w1 = lds128(slot + u * kF8UnitBytes + lane * 32 + 16);
       uint4 xa, xb;
       if (full) {
-        xa = lds128(xs + u * kUnitK * 2);
-        xb = lds128(xs + u * kUnitK * 2 + 16);
+        xa = lds128(xs + u * XU);
+        xb = lds128(xs + u * XU + xd);
       } else {
-        load_x(xs + u * kUnitK * 2, on && u * kUnitK < kleft, xa, xb);
+        load_x(xs + u * XU, xd, on && u * kUnitK < kleft, xa, xb);
       }
       f8_unit(w0, w1, xa, xb, acc);
     }
@@ -357,16 +371,25 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     const uint32_t code_bytes = uint32_t(tiles * nu * m.ub);
     const uint32_t scale_bytes = m.fmt == VG_FMT_NVFP4 ? uint32_t(tiles * kNvScaleChunkBytes) : 0u;
     const int k0 = q.c * m.cu * kUnitK;
-    const uint32_t x_bytes = uint32_t(min(m.cu * kUnitK, m.K - k0) * 2);
+    const CUtensorMap *tmap = p.mats ? m.xmap : (p.x0_tensor ? &p.xmap0 : nullptr);
+    // x: one tensor copy of 8 rows x the chunk's units (rows >= N and units
+    // past K read as zeros), else one bulk copy per row
+    const uint32_t x_bytes = tmap ? uint32_t(8 * m.cu * kUnitK * 2)
+                                  : uint32_t(min(m.cu * kUnitK, m.K - k0) * 2 * p.N);
     const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
-    mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes * uint32_t(p.N));
+    mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes);
     bulk_g2s(slot, m.w + code_off(m, q.rb, q.c, tiles, 0, nu), code_bytes, full, pol_w);
     if (scale_bytes)
       bulk_g2s(slot + kItemScaleOff, m.sc + scale_off(m, q.rb, q.c, tiles, 0), scale_bytes, full,
                pol_w);
-    for (int n = 0; n < p.N; ++n)
-      bulk_g2s(slot + kItemXOff + n * kXRowBytes, m.x + int64_t(n) * m.K + k0, x_bytes, full,
-               pol_x);
+    if (tmap) {
+      bulk_tensor_3d(slot + kItemXOff, tmap, 0, 0, q.c * m.cu, full, pol_x);
+    } else {
+      const uint32_t row_bytes = x_bytes / uint32_t(p.N);
+      for (int n = 0; n < p.N; ++n)
+        bulk_g2s(slot + kItemXOff + n * kXRowBytes, m.x + int64_t(n) * m.K + k0, row_bytes, full,
+                 pol_x);
+    }
     q.advance();
     ++issued;
     if (++s == kSlots) {
@@ -481,7 +504,9 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
 }
 
 __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tensor copies need 1024-byte alignment in shared memory
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
   volatile int *sflag = reinterpret_cast<volatile int *>(smem + kBarOff + kBarBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -515,8 +540,14 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     const bool on = g < N;
     const uint32_t ring = smem_addr(smem);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kSlots);
-    // this lane's x columns inside an item slot, or the zero row for g >= N
-    const uint32_t xlane = uint32_t(kItemXOff + g * kXRowBytes + t * 32);
+    // This lane's x columns inside an item slot.  Tensor-copied slices are
+    // [unit][row][128 B] with the 16-byte chunks of row r at chunk ^ (r % 8)
+    // (128-byte swizzle), so a unit is 1024 bytes and the lane's two chunks
+    // 2t, 2t+1 of row g sit at (2t ^ g) and next to it.  Row-copied slices
+    // are padded rows of kXRowBytes, and a column g >= N reads a zero row.
+    const uint32_t xoff_t = uint32_t(kItemXOff + g * 128 + ((2 * t) ^ g) * 16);
+    const int xd_t = (g & 1) ? -16 : 16;
+    const uint32_t xoff_r = uint32_t(kItemXOff + g * kXRowBytes + t * 32);
     const uint32_t xzero = smem_addr(smem + kZeroRowOff) + t * 32;
     Seq cons;
     cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
@@ -530,6 +561,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     float acc[kAcc][4];
     // matrix fields cached while the matrix does not change
     int K = 0, KU = 0, MT = 0, fmt = 0;
+    bool xt = false;               // the matrix's x slice is tensor-copied
     while (cons.valid) {
       const int ph = cons.ph;
       // -------------------------------------- ordered: wait for group ph-1
@@ -572,6 +604,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         KU = mm.KU;
         MT = mm.MT;
         fmt = mm.fmt;
+        xt = p.mats ? mm.xmap != nullptr : p.x0_tensor != 0;
       }
       const int rb = cons.rb, c = cons.c;
       if (c == 0 || cons.i == cons.i0) {
@@ -594,24 +627,33 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         }
       }
       if (!aborted && mt < MT) {
-        const uint32_t xs = on ? item + xlane : xzero;
+        const uint32_t xs = xt ? item + xoff_t : (on ? item + xoff_r : xzero);
+        const int xd = xt ? xd_t : 16, xu = xt ? 1024 : kUnitK * 2;
         if (fmt == VG_FMT_NVFP4) {
           const int kc = c * (kNvChunkUnits * kUnitK);
           const uint32_t scl = item + kItemScaleOff + warp * kNvScaleChunkBytes;
           // warp-uniform test (mma.sync needs the whole warp): the chunk's
           // whole column range lies inside K
           if (kc + kNvChunkUnits * kUnitK <= K) {
-            nv_chunk_full(item + warp * kSlotCodeBytes, scl, lane, xs, p.m8, p.m64, acc);
+            const uint32_t code = item + warp * kSlotCodeBytes;
+            if (xt)
+              nv_chunk_full<true>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
+            else
+              nv_chunk_full<false>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
           } else {
             const int nu = min(kNvChunkUnits, KU - c * kNvChunkUnits);
-            nv_chunk_tail(item + warp * nu * kNvUnitBytes, scl, lane, xs, on, nu, K - kc - 16 * t,
-                          p.m8, p.m64, acc);
+            nv_chunk_tail(item + warp * nu * kNvUnitBytes, scl, lane, xs, xu, xd, on, nu,
+                          K - kc - 16 * t, p.m8, p.m64, acc);
           }
         } else {
           const int kc = c * (kF8ChunkUnits * kUnitK);
           const bool full = kc + kF8ChunkUnits * kUnitK <= K;
           const int nu = min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
-          f8_chunk(item + warp * nu * kF8UnitBytes, lane, xs, on, full, nu, K - kc - 16 * t, acc);
+          const uint32_t code = item + warp * nu * kF8UnitBytes;
+          if (xt)
+            f8_chunk<true>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
+          else
+            f8_chunk<false>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
         }
       }
       // release the slot to the producer once every warp has read it
@@ -701,6 +743,44 @@ vg_status device_info(int *dev_out, DeviceInfo **info) {
   return VG_OK;
 }
 
+// The tensor-map encoder of the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// x viewed as [K/64 units][N rows][64 columns] (strides 128 bytes and 2K
+// bytes), copied in boxes of `units` units x 8 rows with the 128-byte
+// swizzle; rows >= N and units past K read as zeros.  False when K is not a
+// multiple of 64, when N is below kXTensorMinN, or when the driver does not
+// take the map: the caller then copies x row by row.
+#ifndef VG_XT_MIN_N
+#define VG_XT_MIN_N 1
+#endif
+constexpr int kXTensorMinN = VG_XT_MIN_N;
+bool make_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+  if (!fn || K % kUnitK != 0 || N < kXTensorMinN) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(kUnitK), cuuint64_t(N), cuuint64_t(K / kUnitK)};
+  const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(kUnitK) * 2};
+  const cuuint32_t box[3] = {cuuint32_t(kUnitK), 8u, cuuint32_t(units)};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(x), dims, strides, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, const float *rs,
                 float gscale, const uint16_t *x, uint16_t *y) {
   MatDev m;
@@ -783,6 +863,7 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   set_head(p, ws);
   p.partials = reinterpret_cast<uint64_t *>(ws + kWsHead);
   p.mat0 = m0;
+  p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.cu) ? 1 : 0;
   p.phase0.items = int(T);
   p.phase0.rbs = m0.RB;
   p.phase0.mat_begin = 0;
@@ -805,6 +886,7 @@ struct vg_verify_plan {
   Params params;
   MatDev *d_mats = nullptr;
   PhaseDev *d_phases = nullptr;
+  CUtensorMap *d_xmaps = nullptr;  // per matrix (unused entries for row-copied x)
   uint8_t *d_state = nullptr;     // error, counters, partials
   size_t state_bytes = 0;
 };
@@ -938,6 +1020,14 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   cudaError_t e = cudaMalloc(&plan->d_mats, sizeof(MatDev) * hm.size());
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_phases, sizeof(PhaseDev) * hp.size());
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_state, plan->state_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_xmaps, sizeof(CUtensorMap) * hm.size());
+  if (e == cudaSuccess) {
+    std::vector<CUtensorMap> maps(hm.size());
+    for (size_t i = 0; i < hm.size(); ++i)
+      hm[i].xmap = make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].cu) ? plan->d_xmaps + i : nullptr;
+    e = cudaMemcpy(plan->d_xmaps, maps.data(), sizeof(CUtensorMap) * maps.size(),
+                   cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess)
     e = cudaMemcpy(plan->d_mats, hm.data(), sizeof(MatDev) * hm.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
@@ -1016,6 +1106,7 @@ extern "C" vg_status vg_verify_plan_destroy(vg_verify_plan *plan) {
   if (!plan) return VG_OK;
   cudaFree(plan->d_mats);
   cudaFree(plan->d_phases);
+  cudaFree(plan->d_xmaps);
   cudaFree(plan->d_state);
   delete plan;
   return VG_OK;
