@@ -33,6 +33,12 @@ WORKLOAD = ("verify stack: 64 layers x (NVFP4 q,k,v,o 5120x5120; NVFP4 gate+up 3
 FALLBACK_HBM_GBS = 6800.0
 
 
+def workload_name(args) -> str:
+    if args.attn_fmt == "fp8":
+        return WORKLOAD.replace("NVFP4 q,k,v,o 5120x5120", "row-scaled FP8 q,k,v,o 5120x5120")
+    return WORKLOAD
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -42,6 +48,9 @@ def parse():
     ap.add_argument("--N", type=int, default=8)
     ap.add_argument("--widths", default="1,2,4", help="extra widths reported per pass")
     ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--attn-fmt", choices=["nvfp4", "fp8"], default="nvfp4",
+                    help="stack q,k,v,o format: nvfp4 (16.34 GB pass, the headline) or fp8 "
+                         "(row-scaled, the pages' checkpoint mix: 19.28 GB)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="stack",
@@ -230,7 +239,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    st = build_stack(args.N, device=dev, layers=args.layers)
+    st = build_stack(args.N, device=dev, layers=args.layers, attn_fmt=args.attn_fmt)
     plan = st.plan(ordered=True)
     nbytes = st.bytes
     torch.cuda.synchronize()
@@ -314,14 +323,15 @@ def run_ours(args, world, rank, local):
             "ms_per_step": round(total_ms / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "nvfp4/fp8-e4m3 weights x bf16 -> f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "N": args.N, "mode": "ordered",
+            "config": {"workload": workload_name(args), "N": args.N, "mode": "ordered",
                        "bytes_per_pass": nbytes, "matrices": len(st.mats),
                        "pct_of_8TBps": round(100 * value / world / 8000, 1),
                        "l2": "inputs 16.3 GB per pass >> 129 MB L2; no flush needed",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": profiled_traffic(),
+                         "traffic": (profiled_traffic() if (args.attn_fmt, args.N, args.layers)
+                                     == ("nvfp4", 8, 64) else None),
                          "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
             "per_width": widths, **extra,
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,

@@ -22,10 +22,14 @@ constexpr int kF8UnitBytes = 1024;
 // A chunk is 8 NVFP4 units (512 columns, 4096 bytes per tile) or 4 FP8
 // units (256 columns, 4096 bytes).  NVFP4 block scales: per tile per chunk,
 // 32 lanes x 16 bytes: [unit 0..7][row g, row g+8].
-constexpr int kNvChunkUnits = 8;
+#ifndef VG_NV_CHUNK
+#define VG_NV_CHUNK 8
+#endif
+constexpr int kNvChunkUnits = VG_NV_CHUNK;
+static_assert(kNvChunkUnits == 4 || kNvChunkUnits == 8, "4- or 8-unit chunks");
 constexpr int kNvScaleLaneBytes = 2 * kNvChunkUnits;                    // 16
 constexpr int kNvScaleChunkBytes = 32 * kNvScaleLaneBytes;              // 512
-constexpr int kF8ChunkUnits = 4;
+constexpr int kF8ChunkUnits = kNvChunkUnits / 2;
 
 // A row block is 16 row tiles (256 rows); a work item is one chunk of every
 // tile of a row block.  Each of the 16 consumer warps owns one tile of the
@@ -58,7 +62,7 @@ constexpr int kItemSlotBytes = (kItemXOff + 8 * kXRowBytes + 1023) / 1024 * 1024
 static_assert(kItemXOff % 1024 == 0, "the swizzled x slice starts 1024-byte aligned");
 
 static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
-              "an FP8 chunk fills the code part of a slot");
+              "an FP8 chunk has the bytes of an NVFP4 chunk");
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -178,6 +178,25 @@ struct Seq {
     }
     valid = false;
   }
+  // Skip the n items left in the current row block's piece (never past the
+  // row block's end).
+  __device__ __forceinline__ void skip(int n) {
+    i += n;
+    if (i == i1) {
+      next_phase();
+      return;
+    }
+    c += n;
+    if (c == KC) {
+      c = 0;
+      if (++rb == RB) {
+        rb = 0;
+        ++mi;
+        KC = mats[mi].KC;
+        RB = mats[mi].RB;
+      }
+    }
+  }
   __device__ __forceinline__ void advance() {
     if (++i == i1) {
       next_phase();
@@ -247,6 +266,21 @@ __device__ __forceinline__ void load_x(uint32_t xs, int xd, bool on, uint4 &xa, 
   }
 }
 
+// The lane's scale words of a chunk: two units (rows g, g+8 each) per word.
+__device__ __forceinline__ void load_scale_words(uint32_t a, uint32_t (&w)[kNvChunkUnits / 2]) {
+  if constexpr (kNvChunkUnits == 8) {
+    const uint4 v = lds128(a);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else {
+    const uint2 v = lds64(a);
+    w[0] = v.x;
+    w[1] = v.y;
+  }
+}
+
 // A whole NVFP4 chunk (8 units) of this lane's tile: scale pairs from one
 // 16-byte load, codes and x for two units at a time, the next pair loaded
 // before the current one is multiplied.  slot, scl: shared-memory addresses
@@ -260,8 +294,8 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int l
                                               float (&acc)[kAcc][4]) {
   constexpr int kXUnit = kTensorX ? 1024 : kUnitK * 2;
   const int xd = kTensorX ? xd_t : 16;
-  const uint4 sc = lds128(scl + lane * kNvScaleLaneBytes);
-  const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+  uint32_t scw[kNvChunkUnits / 2];
+  load_scale_words(scl + lane * kNvScaleLaneBytes, scw);
   uint4 w0 = lds128(slot + lane * 16), w1 = lds128(slot + kNvUnitBytes + lane * 16);
   uint4 x0a = lds128(xs), x0b = lds128(xs + xd);
   uint4 x1a = lds128(xs + kXUnit), x1b = lds128(xs + kXUnit + xd);
@@ -294,13 +328,16 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int l
 __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
                                               int xu, int xd, bool on, int nu, int kleft,
                                               uint32_t m8, uint32_t m64, float (&acc)[kAcc][4]) {
-  const uint4 sc = lds128(scl + lane * kNvScaleLaneBytes);
+  uint32_t scw[kNvChunkUnits / 2];
+  load_scale_words(scl + lane * kNvScaleLaneBytes, scw);
   for (int u = 0; u < nu; ++u) {
     const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
     uint4 xa, xb;
     load_x(xs + u * xu, xd, on && u * kUnitK < kleft, xa, xb);
-    const int q = u >> 1;
-    const uint32_t word = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
+    // select without a runtime-indexed array (that would go to local memory)
+    uint32_t word = scw[0];
+#pragma unroll
+    for (int q = 1; q < kNvChunkUnits / 2; ++q) word = (u >> 1) == q ? scw[q] : word;
     const uint32_t b = uint32_t(u & 1) * 2u;
     nv_unit(wv, nv_scale_pair(word, b), nv_scale_pair(word, b + 1), xa, xb, m8, m64, acc);
   }
@@ -556,8 +593,6 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     uint32_t par = 0;              // parity of that slot's current phase
     int cur_ph = -1, cur_mi = -1;
     uint32_t tag = 0;              // tag of this pass and phase
-    int piece_start = 0;
-    int piece_c0 = 0;
     float acc[kAcc][4];
     // matrix fields cached while the matrix does not change
     int K = 0, KU = 0, MT = 0, fmt = 0;
@@ -606,80 +641,81 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         fmt = mm.fmt;
         xt = p.mats ? mm.xmap != nullptr : p.x0_tensor != 0;
       }
-      const int rb = cons.rb, c = cons.c;
-      if (c == 0 || cons.i == cons.i0) {
-        piece_start = cons.i;
-        piece_c0 = c;
+      // ------------------------------------------------- one row-block piece
+      // the block's contiguous items of one row block: set up once, then a
+      // tight loop over its chunks
+      const int rb = cons.rb, c0 = cons.c;
+      const int len = min(cons.KC - c0, cons.i1 - cons.i);
+      const int piece_start = cons.i;
 #pragma unroll
-        for (int a = 0; a < kAcc; ++a)
+      for (int a = 0; a < kAcc; ++a)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-      }
-      const uint32_t item = ring + s * kItemSlotBytes;
+        for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
       const int mt = rb * kBlockTiles + warp;
-      if (!aborted) {
-        // every lane polls; a lane whose wait ran out stops the whole warp,
-        // since mma.sync needs all of it
-        const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
-        if (!__all_sync(0xFFFFFFFFu, ready)) {
-          if (lane == 0) set_error(p.error, kErrFullWait);
-          aborted = true;
-        }
-      }
-      if (!aborted && mt < MT) {
-        const uint32_t xs = xt ? item + xoff_t : (on ? item + xoff_r : xzero);
-        const int xd = xt ? xd_t : 16, xu = xt ? 1024 : kUnitK * 2;
-        if (fmt == VG_FMT_NVFP4) {
-          const int kc = c * (kNvChunkUnits * kUnitK);
-          const uint32_t scl = item + kItemScaleOff + warp * kNvScaleChunkBytes;
-          // warp-uniform test (mma.sync needs the whole warp): the chunk's
-          // whole column range lies inside K
-          if (kc + kNvChunkUnits * kUnitK <= K) {
-            const uint32_t code = item + warp * kSlotCodeBytes;
-            if (xt)
-              nv_chunk_full<true>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
-            else
-              nv_chunk_full<false>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
-          } else {
-            const int nu = min(kNvChunkUnits, KU - c * kNvChunkUnits);
-            nv_chunk_tail(item + warp * nu * kNvUnitBytes, scl, lane, xs, xu, xd, on, nu,
-                          K - kc - 16 * t, p.m8, p.m64, acc);
+      const bool work = mt < MT;
+      for (int c = c0; c < c0 + len; ++c) {
+        const uint32_t item = ring + s * kItemSlotBytes;
+        if (!aborted) {
+          // every lane polls; a lane whose wait ran out stops the whole
+          // warp, since mma.sync needs all of it
+          const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
+          if (!__all_sync(0xFFFFFFFFu, ready)) {
+            if (lane == 0) set_error(p.error, kErrFullWait);
+            aborted = true;
           }
-        } else {
-          const int kc = c * (kF8ChunkUnits * kUnitK);
-          const bool full = kc + kF8ChunkUnits * kUnitK <= K;
-          const int nu = min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
-          const uint32_t code = item + warp * nu * kF8UnitBytes;
-          if (xt)
-            f8_chunk<true>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
-          else
-            f8_chunk<false>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
         }
-      }
-      // release the slot to the producer once every warp has read it
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      if (++s == kSlots) {
-        s = 0;
-        par ^= 1u;
+        if (!aborted && work) {
+          const uint32_t xs = xt ? item + xoff_t : (on ? item + xoff_r : xzero);
+          const int xd = xt ? xd_t : 16, xu = xt ? 1024 : kUnitK * 2;
+          if (fmt == VG_FMT_NVFP4) {
+            const int kc = c * (kNvChunkUnits * kUnitK);
+            const uint32_t scl = item + kItemScaleOff + warp * kNvScaleChunkBytes;
+            // warp-uniform test (mma.sync needs the whole warp): the chunk's
+            // whole column range lies inside K
+            if (kc + kNvChunkUnits * kUnitK <= K) {
+              const uint32_t code = item + warp * kSlotCodeBytes;
+              if (xt)
+                nv_chunk_full<true>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
+              else
+                nv_chunk_full<false>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
+            } else {
+              const int nu = min(kNvChunkUnits, KU - c * kNvChunkUnits);
+              nv_chunk_tail(item + warp * nu * kNvUnitBytes, scl, lane, xs, xu, xd, on, nu,
+                            K - kc - 16 * t, p.m8, p.m64, acc);
+            }
+          } else {
+            const int kc = c * (kF8ChunkUnits * kUnitK);
+            const bool full = kc + kF8ChunkUnits * kUnitK <= K;
+            const int nu = min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
+            const uint32_t code = item + warp * nu * kF8UnitBytes;
+            if (xt)
+              f8_chunk<true>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
+            else
+              f8_chunk<false>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
+          }
+        }
+        // release the slot to the producer once every warp has read it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (++s == kSlots) {
+          s = 0;
+          par ^= 1u;
+        }
       }
 
-      // ---------------------------------------------- end of a row-block piece
-      const bool piece_end = c == cons.KC - 1 || cons.i == cons.i1 - 1;
-      if (piece_end) {
-        float accs[4];
+      // ---------------------------------------------- end of the piece
+      float accs[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          accs[e] = acc[0][e];
+      for (int e = 0; e < 4; ++e) {
+        accs[e] = acc[0][e];
 #pragma unroll
-          for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
-        }
-        if (!finish_piece(p, mats[cons.mi], cons.items, cons.G, piece_start,
-                          piece_c0 == 0 && c == cons.KC - 1, rb, ph, tag, aborted, accs[0],
-                          accs[1], accs[2], accs[3]))
-          aborted = true;
+        for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
       }
-      cons.advance();
+      if (!finish_piece(p, mats[cons.mi], cons.items, cons.G, piece_start,
+                        c0 == 0 && len == cons.KC, rb, ph, tag, aborted, accs[0], accs[1], accs[2],
+                        accs[3]))
+        aborted = true;
+      cons.skip(len);
     }
   }
 
