@@ -377,6 +377,13 @@ __device__ __forceinline__ int64_t scale_off(const MatDev &m, int rb, int c, int
   return (int64_t(rb) * kBlockTiles * m.KC + int64_t(c) * tiles + tile) * kNvScaleChunkBytes;
 }
 
+// Items beyond the ring that the producer brings into L2 while the consumers
+// wait on a group dependency (the ring is full and DRAM would sit idle).
+#ifndef VG_BPF
+#define VG_BPF 4
+#endif
+constexpr int kBoundaryPf = VG_BPF;
+
 // The producer (one lane): fill the item ring, one whole item per slot, as
 // soon as all 16 consumer warps have released the slot.  An item's codes are
 // one contiguous range of the packed buffer and its scales another, so an
@@ -384,18 +391,32 @@ __device__ __forceinline__ int64_t scale_off(const MatDev &m, int rb, int c, int
 // is read by every block: evict-last).  Columns past K are not copied; the
 // consumers mask them.
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
-                         uint32_t ring, uint32_t full0, uint32_t empty0) {
+                         uint32_t ring, uint32_t full0, uint32_t empty0,
+                         const volatile int *dep_waiting) {
   const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
   Seq q;
   q.init(mats, phases, p.nphases, blockIdx.x, p.grid);
   int s = 0;
   uint32_t par = 0;
   int64_t issued = 0;
+  Seq pf = q;       // next item to bring into L2 during a dependency wait
+  int pf_ahead = 0; // items between q and pf
   while (q.valid) {
     if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
       const uint64_t deadline = globaltimer() + p.timeout_ns;
       bool ok = false;
       while (!(ok = mbar_test_wait(empty0 + 8 * s, par ^ 1u)) && globaltimer() <= deadline) {
+        if (kBoundaryPf > 0 && *dep_waiting && pf_ahead < kBoundaryPf && pf.valid) {
+          const MatDev &fm = mats[pf.mi];
+          const int ft = min(kBlockTiles, fm.MT - pf.rb * kBlockTiles);
+          const int fu = min(fm.cu, fm.KU - pf.c * fm.cu);
+          bulk_prefetch_l2(fm.w + code_off(fm, pf.rb, pf.c, ft, 0, fu), uint32_t(ft * fu * fm.ub));
+          if (fm.fmt == VG_FMT_NVFP4)
+            bulk_prefetch_l2(fm.sc + scale_off(fm, pf.rb, pf.c, ft, 0),
+                             uint32_t(ft * kNvScaleChunkBytes));
+          pf.advance();
+          ++pf_ahead;
+        }
       }
       if (!ok) {
         set_error(p.error, kErrEmptyWait);
@@ -428,6 +449,10 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
                  pol_x);
     }
     q.advance();
+    if (pf_ahead > 0)
+      --pf_ahead;
+    else
+      pf = q;
     ++issued;
     if (++s == kSlots) {
       s = 0;
@@ -561,6 +586,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     sflag[0] = 0;
     sflag[1] = int(ld_relaxed(p.epoch));
     sflag[2] = 0;
+    sflag[3] = 0;   // consumers waiting on a group dependency
   }
   __syncthreads();
   const uint32_t epoch = uint32_t(sflag[1]);
@@ -568,7 +594,8 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   if (warp == kWarps) {
     // ================================================================ producer
     if (lane == 0)
-      producer(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots));
+      producer(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots),
+               sflag + 3);
 
   } else {
     // =============================================================== consumers
@@ -606,6 +633,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
             int ok = 1;
             if (!aborted) {
               const uint32_t *d = p.done + (ph - 1);
+              sflag[3] = 1;
               const uint32_t target = uint32_t(phases[ph - 1].rbs);
               if (ld_acquire(d) < target) {
                 const uint64_t deadline = globaltimer() + p.timeout_ns;
@@ -623,6 +651,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
                 }
               }
             }
+            sflag[3] = 0;
             sflag[0] = ok ? 0 : 1;
           }
           named_bar(1, kConsumers);
