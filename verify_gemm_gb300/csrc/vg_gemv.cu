@@ -682,7 +682,50 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
       const int mt = rb * kBlockTiles + warp;
       const bool work = mt < MT;
-      for (int c = c0; c < c0 + len; ++c) {
+      int c = c0;
+      const int c_end = c0 + len;
+      // Fast loop: the common case (tensor-copied x, chunks wholly inside K,
+      // the warp's tile inside M) with nothing decided per item but the wait.
+      if (!aborted && work && xt) {
+        const uint32_t scl0 = kItemScaleOff + warp * kNvScaleChunkBytes;
+        const uint32_t code0 = warp * kSlotCodeBytes;
+        if (fmt == VG_FMT_NVFP4) {
+          const int c_full = min(c_end, K / (kNvChunkUnits * kUnitK));
+          for (; c < c_full; ++c) {
+            const uint32_t item = ring + s * kItemSlotBytes;
+            if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+              break;   // the general loop below records the failure
+            nv_chunk_full<true>(item + code0, item + scl0, lane, item + xoff_t, xd_t, p.m8, p.m64,
+                                acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (++s == kSlots) {
+              s = 0;
+              par ^= 1u;
+            }
+          }
+        } else {
+          const int c_full = min(c_end, K / (kF8ChunkUnits * kUnitK));
+          for (; c < c_full; ++c) {
+            const uint32_t item = ring + s * kItemSlotBytes;
+            if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+              break;
+            f8_chunk<true>(item + code0, lane, item + xoff_t, xd_t, true, true, kF8ChunkUnits, 0,
+                           acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (++s == kSlots) {
+              s = 0;
+              par ^= 1u;
+            }
+          }
+        }
+      }
+      // General loop: the rest of the piece (K tails, row-copied x, tiles past
+      // M, a failed wait).
+      for (; c < c_end; ++c) {
         const uint32_t item = ring + s * kItemSlotBytes;
         if (!aborted) {
           // every lane polls; a lane whose wait ran out stops the whole
