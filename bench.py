@@ -136,33 +136,23 @@ class ClockSampler:
 
 
 def dist_init(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
+    from verify_gemm_gb300 import replicas
 
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        dist.init_process_group(backend)
-    return world, rank, local
+    ranks = replicas.from_env()
+    replicas.init(ranks, "nccl" if args.impl == "ours" else "gloo")
+    return ranks.world, ranks.rank, ranks.local
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
+    from verify_gemm_gb300 import replicas
 
-        dist.barrier()
+    replicas.barrier(replicas.Ranks(world=world))
 
 
 def max_over_ranks(v, world, device=None):
-    if world == 1:
-        return v
-    import torch
-    import torch.distributed as dist
+    from verify_gemm_gb300 import replicas
 
-    t = torch.tensor([v], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return replicas.max_over_ranks(v, replicas.Ranks(world=world), device)
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -245,6 +235,7 @@ def run_ours(args, world, rank, local):
     import verify_gemm_gb300 as vg
     from verify_gemm_gb300 import build as vbuild
     from verify_gemm_gb300.workloads import build_stack
+    from verify_gemm_gb300 import replicas
 
     vbuild.build()
     torch.cuda.set_device(local)
@@ -278,7 +269,7 @@ def run_ours(args, world, rank, local):
     if plan.check() != 0:
         raise RuntimeError("verify pass reported a device error")
     total_ms = max_over_ranks(total_ms, world, dev)
-    value = nbytes * args.steps * world / (total_ms / 1e3) / 1e9
+    value = replicas.job_gbps(nbytes, args.steps, total_ms, replicas.Ranks(world=world))
     kernel_ms = statistics.mean(per)
     achieved = nbytes / (kernel_ms / 1e3) / 1e9
     peak, peak_kind = peaks()
@@ -319,7 +310,8 @@ def run_ours(args, world, rank, local):
 
         e_ms, _ = timed(e2e_step, args.steps, args.warmup)
         e_ms = max_over_ranks(e_ms, world, dev)
-        e2e = {"value": nbytes * args.steps * world / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e2e = {"value": replicas.job_gbps(nbytes, args.steps, e_ms, replicas.Ranks(world=world)),
+               "unit": "GB/s",
                "h2d_bytes_per_step": st.x_all.numel() * 2,
                "d2h_bytes_per_step": st.y_all.numel() * 2}
     plan.close()
