@@ -181,7 +181,10 @@ vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes
  *   workspace   device, >= vg_gemv_workspace_size bytes (see there).
  * Accumulation is FP32; y is rounded to nearest even.  The result for
  * column n does not depend on N or on the other columns, and a repeated
- * call gives the same bits. */
+ * call gives the same bits.  With K a multiple of 64, each work item's slice
+ * of x is one tensor copy (a tensor map encoded on the host through the
+ * driver); otherwise, or if the driver declines the map, x is copied one row
+ * at a time (same results, slower). */
 vg_status vg_gemv_nvfp4(const void *w, const void *scales, float gscale,
                         const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
                         void *workspace, size_t workspace_bytes, vg_stream_t stream);
@@ -276,10 +279,10 @@ typedef struct vg_plan_options {
  * columns; Measured section: 19.26 GB read per pass).  Allocates the
  * plan's descriptor table, counters and partial-sum space once.
  * Descriptors (pointers included) are copied; buffer contents may change
- * between passes.  Every group's x is read through the read-only data
- * path: an x must not alias any matrix's y within the same plan (group
- * order sequences the work; it does not forward one group's y as the
- * next group's x). */
+ * between passes.  Each item's slice of x is copied into shared memory by
+ * copies that run ahead of the group order, so an x must not alias any
+ * matrix's y within the same plan (group order sequences the work; it does
+ * not forward one group's y as the next group's x). */
 vg_status vg_verify_plan_create(const vg_matrix_desc *mats, int count, int N,
                                 int ordered, vg_verify_plan **plan_out);
 vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,

@@ -11,15 +11,17 @@
 //
 // Design (sm_103a):
 //  * Persistent thread blocks, one per SM: 16 consumer warps + 1 producer
-//    warp.  Producer lane t keeps consumer warp t's private 3-slot ring of
-//    shared memory full with 1-D bulk copies (cp.async.bulk, L2 evict-first),
-//    guarded by full/empty mbarriers; the weights never pass through
+//    warp.  The producer (one lane) keeps a 2-slot ring of shared memory
+//    full, one whole work item per slot, guarded by full/empty mbarriers:
+//    one bulk copy of the item's codes and one of its scales (contiguous in
+//    the packed buffers; L2 evict-first) and one TMA tensor copy of its x
+//    slice (128-byte swizzle; L2 evict-last).  The weights never pass through
 //    registers of the producer.
 //  * A work item is one chunk (512 columns NVFP4, 256 FP8) of a row block of
 //    16 tiles (256 rows); consumer warp t owns tile t of it.  It decodes the
 //    codes in registers to BF16 A fragments (bit placement + one BF16x2
-//    multiply by the block scale, exact) and runs mma.m16n8k16 with x as the
-//    B fragment (x read through L1, shared by all warps), accumulating FP32.
+//    multiply by the block scale, exact) and runs mma.m16n8k16 with x from
+//    the slot as the B fragment, accumulating FP32.
 //  * Items are split between thread blocks stream-K style (contiguous item
 //    ranges of equal length), so every SM streams the same number of bytes.
 //    A row block whose K range is split between blocks is summed by the
@@ -30,9 +32,9 @@
 //    fence, counter or barrier on its path.
 //  * Verify pass: matrices are grouped; in ordered mode the consumers of
 //    group g wait (bounded) until group g-1 has completed every row block,
-//    while the producer keeps prefetching group g's weights.  All waits are
-//    bounded by a timeout on %globaltimer and report an error word instead
-//    of hanging.
+//    while the producer keeps filling the ring with group g's items and
+//    brings a few more into L2.  All waits are bounded by a timeout on
+//    %globaltimer and report an error word instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
