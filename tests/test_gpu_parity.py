@@ -135,6 +135,9 @@ GEMV_SHAPES = [
     (272, 1088, (1, 2, 5, 8)),    # 17 tiles (two row blocks), K tail chunk
     (520, 2560, (8,)),            # several row blocks x chunks: stream-K splits
     (4096, 576, (2,)),            # many row blocks, short K
+    (1, 16, (1, 8)),              # one row, the smallest K (one scale block)
+    (33, 48, (4,)),               # K below one unit (row-copied x)
+    (300, 1600, (3, 8)),          # K a multiple of 64 with a 1-unit tail chunk
 ]
 
 
