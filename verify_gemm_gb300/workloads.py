@@ -26,6 +26,18 @@ class StackSetup:
     def bytes(self) -> int:
         return sum(w.nbytes for w in self.weights)
 
+    def with_new_buffers(self) -> "StackSetup":
+        """The same matrices and packed weights over a second pair of x / y
+        buffers (x copied): a pass on one pair can run while the other pair's
+        x is uploaded and its y read back."""
+        x_all = self.x_all.clone()
+        y_all = torch.zeros_like(self.y_all)
+        xs = [x_all[(x.data_ptr() - self.x_all.data_ptr()) // 2:][:x.numel()].view(x.shape)
+              for x in self.xs]
+        ys = [y_all[(y.data_ptr() - self.y_all.data_ptr()) // 2:][:y.numel()].view(y.shape)
+              for y in self.ys]
+        return StackSetup(self.mats, self.weights, xs, ys, x_all, y_all, self.N)
+
     def plan(self, ordered: bool = True, **kw) -> VerifyPlan:
         entries = [(w, x, y, m.group) for m, w, x, y in zip(self.mats, self.weights, self.xs,
                                                               self.ys)]
