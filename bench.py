@@ -31,6 +31,7 @@ WORKLOAD = ("verify stack: 64 layers x (NVFP4 q,k,v,o 5120x5120; NVFP4 gate+up 3
             "as two 17408x5120 halves; row-scaled FP8 down 5120x17408) + NVFP4 head "
             "151936x5120; W ~ N(0,0.02) RTN-quantised, x BF16 ~ N(0,1); seed 4")
 FALLBACK_HBM_GBS = 6800.0
+WEIGHTS = "nvfp4 / row-scaled fp8-e4m3, decoded exactly to bf16; fp32 accumulation"
 
 
 def workload_name(args) -> str:
@@ -370,7 +371,7 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_ms / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4/fp8-e4m3 weights x bf16 -> f32", "data": "synthetic",
+            "dtype": "bf16", "weights": WEIGHTS, "data": "synthetic",
             "config": {"workload": workload_name(args), "N": args.N, "mode": "ordered",
                        "bytes_per_pass": nbytes, "matrices": len(st.mats),
                        "pct_of_8TBps": round(100 * value / world / 8000, 1),
@@ -453,7 +454,7 @@ def run_single(args, local):
     line = {"metric": METRIC, "value": round(nbytes / (med / 1e3) / 1e9, 1), "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(med, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "nvfp4/fp8-e4m3 weights x bf16 -> f32",
+            "vs_baseline": None, "dtype": "bf16", "weights": WEIGHTS,
             "data": "synthetic",
             "config": {"workload": title, "N": args.N, "bytes": nbytes,
                        "l2": "flushed by a 512 MB write before every launch",
