@@ -277,7 +277,7 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-// Read-only 16-byte global load through L1 (x is reused by every warp).
+// Read-only 16-byte global load (the HBM probe's vector-load mode).
 __device__ __forceinline__ uint4 ldg128(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

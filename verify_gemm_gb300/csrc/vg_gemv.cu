@@ -130,7 +130,6 @@ __device__ inline int owner(int T, int G, int i) { return int((int64_t(i + 1) * 
 
 __device__ inline void set_error(int *error, int code) { atomicCAS(error, 0, code); }
 
-
 // Bounded wait with the clock read only after a first miss.
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t timeout) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -345,9 +344,9 @@ __device__ __forceinline__ void nv_chunk_tail(uint32_t slot, uint32_t scl, int l
   }
 }
 
-// An FP8 chunk: nu (<= 4) units of 1024 bytes.  `full`: all 4 units lie
-// inside K, so x loads need no per-unit condition (xs then points at a zero
-// row for a column >= N).
+// An FP8 chunk: nu (<= kF8ChunkUnits) units of 1024 bytes.  `full`: all units
+// lie inside K, so x loads need no per-unit condition (xs then points at a
+// zero row for a column >= N, or at the zero-filled rows of a tensor copy).
 template <bool kTensorX>
 __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, int xd_t, bool on,
                                          bool full, int nu, int kleft, float (&acc)[kAcc][4]) {
@@ -515,9 +514,10 @@ __device__ __noinline__ bool collect(const Params &p, int b0, int bl, uint32_t t
 // (the reducer) adds the other contributors' partial sums to its own and
 // writes y; every other contributor publishes its partial sums in its slot,
 // tagged, and moves on without waiting.  In ordered mode the completed row
-// block is counted for its phase.  Kept out of line: it runs once per piece,
-// and its registers must not crowd the streaming loop.  Returns false if the
-// wait for partial sums failed.
+// block is counted for its phase.  It runs once per piece, outside the
+// per-item loops; the reducer's collection of partial sums is kept out of
+// line (collect) so that its registers do not crowd those loops.  Returns
+// false if the wait for partial sums failed.
 __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, int T, int G,
                                           int piece_start, bool full_piece, int rb, int ph,
                                           uint32_t tag, bool aborted, float a0, float a1,
