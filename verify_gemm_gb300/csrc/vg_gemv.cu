@@ -468,43 +468,64 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
 // The reducer of a split row block adds the partial sums of the other
 // contributors, blocks b0..bl, in block order.  Each thread reads only its
 // own four words of every slot; a word counts once its tag matches `tag`, so
-// no fence is needed on either side.  Loads for two contributors are in
-// flight at once (more would crowd the streaming loop's registers).
+// no fence is needed on either side.  One round of loads covers kCollectW
+// contributors; while some are not yet published, only their words are read
+// again.  Each round costs an L2 round trip (about 1 us here), but wider
+// rounds need more than the 96 registers a thread gets with 17 warps per SM
+// and spill, which costs more than the rounds they save.
 // Returns false if the wait ran out or another block has already failed.
-__device__ __noinline__ bool collect(const Params &p, int b0, int bl, uint32_t tag, int at,
-                                     float (&accs)[4]) {
+#ifndef VG_COLLECT_W
+#define VG_COLLECT_W 2
+#endif
+constexpr int kCollectW = VG_COLLECT_W;
+
+__device__ __forceinline__ bool tags_match(const uint64_t (&v)[4], uint32_t tag) {
+  return uint32_t(v[0] >> 32) == tag && uint32_t(v[1] >> 32) == tag &&
+         uint32_t(v[2] >> 32) == tag && uint32_t(v[3] >> 32) == tag;
+}
+
+__device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_t tag, int at,
+                                        float (&accs)[4]) {
   uint64_t deadline = 0;
-  for (int bb = b0; bb <= bl; bb += 2) {
-    uint64_t v[2][4];
+  for (int bb = b0; bb <= bl; bb += kCollectW) {
+    uint64_t v[kCollectW][4];
+    uint32_t pending = 0;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kCollectW; ++j) {
       if (bb + j <= bl) {
         const uint64_t *src = p.partials + int64_t(bb + j) * kPartialWords + at;
         ld_relaxed_v2u64(src, v[j][0], v[j][1]);
         ld_relaxed_v2u64(src + 64, v[j][2], v[j][3]);
+        pending |= 1u << j;
       }
     }
+    for (;;) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (bb + j <= bl) {
-        while (uint32_t(v[j][0] >> 32) != tag || uint32_t(v[j][1] >> 32) != tag ||
-               uint32_t(v[j][2] >> 32) != tag || uint32_t(v[j][3] >> 32) != tag) {
-          const uint64_t now = globaltimer();
-          if (deadline == 0) {
-            deadline = now + p.timeout_ns;
-          } else if (now > deadline) {
-            set_error(p.error, kErrPartialWait);
-            return false;
-          }
-          if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
+      for (int j = 0; j < kCollectW; ++j)
+        if (((pending >> j) & 1u) && tags_match(v[j], tag)) pending &= ~(1u << j);
+      if (pending == 0) break;
+      const uint64_t now = globaltimer();
+      if (deadline == 0) {
+        deadline = now + p.timeout_ns;
+      } else if (now > deadline) {
+        set_error(p.error, kErrPartialWait);
+        return false;
+      }
+      if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
+#pragma unroll
+      for (int j = 0; j < kCollectW; ++j) {
+        if ((pending >> j) & 1u) {
           const uint64_t *src = p.partials + int64_t(bb + j) * kPartialWords + at;
           ld_relaxed_v2u64(src, v[j][0], v[j][1]);
           ld_relaxed_v2u64(src + 64, v[j][2], v[j][3]);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) accs[e] += __uint_as_float(uint32_t(v[j][e]));
       }
     }
+#pragma unroll
+    for (int j = 0; j < kCollectW; ++j)
+      if (bb + j <= bl)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accs[e] += __uint_as_float(uint32_t(v[j][e]));
   }
   return true;
 }
@@ -515,8 +536,7 @@ __device__ __noinline__ bool collect(const Params &p, int b0, int bl, uint32_t t
 // writes y; every other contributor publishes its partial sums in its slot,
 // tagged, and moves on without waiting.  In ordered mode the completed row
 // block is counted for its phase.  It runs once per piece, outside the
-// per-item loops; the reducer's collection of partial sums is kept out of
-// line (collect) so that its registers do not crowd those loops.  Returns
+// per-item loops.  Returns
 // false if the wait for partial sums failed.
 __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, int T, int G,
                                           int piece_start, bool full_piece, int rb, int ph,
