@@ -122,7 +122,7 @@ vg_status vg_nvfp4_pack(const float *W, int64_t M, int64_t K,
                         vg_stream_t stream);
 
 /* Row-scaled FP8-E4M3 quantisation (engine card, Model section: the draft
- * layer "re-encoded as row-scaled FP8"):  rs[m] = rowamax / 448,
+ * layer is stored as FP8 with one scale per row):  rs[m] = rowamax / 448,
  * code = E4M3(w / rs[m]) rounded to nearest even with saturation (all codes
  * 0 when rs[m] == 0).
  *   W            device FP32 [M][K].

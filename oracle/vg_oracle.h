@@ -16,9 +16,9 @@
  * The product being checked is y[N,M] = x[N,K] . dequant(W)[M,K]^T, the
  * weight-streaming product that the mtp7-device-confidence engine card
  * (crit-hub), Design table, "GEMVs" row, runs for 1-8 columns, and that
- * the same card's Measured section ("a verify pass reads 19.26 GB") and
- * Checks section ("FP8/NVFP4 GEMVs for 1-8 columns ... against FP64")
- * describe.  Accumulation is FP64; products of decoded weights and BF16
+ * the same card's Measured section (19.26 GB read per verify pass) and
+ * Checks section (the FP8 and NVFP4 GEMVs for 1-8 columns compared with an
+ * FP64 reference) describe.  Accumulation is FP64; products of decoded weights and BF16
  * activations are exact in FP64.
  */
 #ifndef VG_ORACLE_H

@@ -1,7 +1,7 @@
 // vg_probe.cu -- read-only HBM bandwidth probe.
 //
 // The verify GEMV is bound by weight reads (mtp7-device-confidence engine
-// card, Measured section: a verify pass "reads 19.26 GB", its floor set by
+// card, Measured section: 19.26 GB read per verify pass, its floor set by
 // the card's read rate; crit README, Eval: limits derived from the measured
 // memory bandwidth).  This probe measures the practical read ceiling of the
 // device with the two access styles the library could use, so that the
