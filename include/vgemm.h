@@ -38,9 +38,13 @@
  *  bytes, arranged so that every lane of a warp reads one 16-byte vector
  *  per unit holding 16 consecutive K positions of two rows (one scale block
  *  of each), with the bits of each code placed for a cheap in-register
- *  decode to BF16.  Units are ordered by row block (16 tiles), then chunk
- *  (8 units), then tile, so that one chunk of a whole row block -- the
- *  kernel's unit of work -- is one contiguous run of bytes.  Block scales
+ *  decode to BF16.  The kernel's unit of work, an item, is 16 tile-chunks
+ *  (a chunk is 8 units): one chunk of a row block of 16 tiles, or, for
+ *  matrices with few rows (when every item is whole in K), 16 / rt
+ *  consecutive chunks of a row block of rt = 8, 4 or 2 tiles.  rt follows
+ *  from M, K and the format alone, so the layout is fixed by the matrix
+ *  shape.  Units are ordered by row block, then item, then tile, then
+ *  chunk, so that every item is one contiguous run of bytes.  Block scales
  *  live in a separate buffer in the same order, 512 bytes per tile per
  *  chunk, re-encoded losslessly so that E4M3 subnormal scales decode like
  *  normal ones.  Row-scaled FP8 codes use 1024-byte units (4 per chunk) in
@@ -184,7 +188,9 @@ vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes
  * call gives the same bits.  With K a multiple of 64, each work item's slice
  * of x is one tensor copy (a tensor map encoded on the host through the
  * driver); otherwise, or if the driver declines the map, x is copied one row
- * at a time (same results, slower). */
+ * at a time (same results, slower).  Items of several chunks (see the weight
+ * layout) take x by tensor copy only: if the driver declines their map the
+ * call returns VG_ERR_UNSUPPORTED. */
 vg_status vg_gemv_nvfp4(const void *w, const void *scales, float gscale,
                         const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
                         void *workspace, size_t workspace_bytes, vg_stream_t stream);

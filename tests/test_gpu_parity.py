@@ -138,6 +138,11 @@ GEMV_SHAPES = [
     (1, 16, (1, 8)),              # one row, the smallest K (one scale block)
     (33, 48, (4,)),               # K below one unit (row-copied x)
     (300, 1600, (3, 8)),          # K a multiple of 64 with a 1-unit tail chunk
+    # items of several chunks of fewer tiles (row blocks of rt < 16 tiles)
+    (100, 1024, (1, 8)),          # NVFP4 rt 8: one ragged row block; FP8 rt 4: two
+    (100, 4096, (2, 8)),          # NVFP4 rt 4, FP8 rt 2 (8 chunks): row blocks split in two
+    (5000, 2048, (8,)),           # rt 4, 79 row blocks, the last of 2 tiles and 8 rows
+    (333, 3072, (5,)),            # NVFP4 rt 8, FP8 rt 4, three items per row block
 ]
 
 
@@ -159,11 +164,11 @@ def test_gemv_nvfp4_parity(vg, orc, M, K, Ns):
 
 
 def test_gemv_pass_counter_wrap(vg, orc):
-    """Split row blocks (32 items on 32 blocks, every row block summed from 8
-    blocks' tagged partials) stay exact when the pass counter that tags them
-    reaches its end: the pass then restarts the counter at 0 and clears every
-    slot, and the next pass's tags are fresh again."""
-    M, K, N = 1024, 4096, 8
+    """Split row blocks (32 items on 32 blocks, every row block of 16 tiles
+    summed from 8 blocks' tagged partials) stay exact when the pass counter
+    that tags them reaches its end: the pass then restarts the counter at 0
+    and clears every slot, and the next pass's tags are fresh again."""
+    M, K, N = 1024, 4032, 8
     W = rand_w(77, M, K)
     wt = vg.nvfp4_pack(W.cuda())
     nib, sc, gs = orc.nvfp4_quantise(W.numpy())
@@ -361,6 +366,34 @@ def test_verify_pass_small_stack(vg, orc, N, ordered):
                 q, rs = orc.fp8_quantise(Wh)
                 yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
             assert_close(orc, y, yref, a, m.name)
+    plan.close()
+
+
+@pytest.mark.parametrize("ordered", [True, False])
+@pytest.mark.parametrize("N", [3, 8])
+def test_verify_pass_multi_chunk_items(vg, orc, N, ordered):
+    """A stack whose matrices take items of several chunks: NVFP4 1024-column
+    matrices in row blocks of 8 tiles (2 chunks per item) and the FP8 down
+    projection (K 2048) in row blocks of 2 tiles (8 chunks per item), so the
+    warps sharing a tile add their sums in shared memory before the row
+    blocks split between thread blocks are reduced."""
+    from verify_gemm_gb300.inputs import draw_stack_matrix
+    from verify_gemm_gb300.workloads import build_stack
+
+    st = build_stack(N, layers=2, hidden=1024, inter=2048, vocab=1000, down_fmt="fp8", seed=11)
+    plan = st.plan(ordered=ordered)
+    plan.run()
+    assert plan.check() == 0
+    for m, wt, x, y in zip(st.mats, st.weights, st.xs, st.ys):
+        W, _ = draw_stack_matrix(m, N, 11, "cuda")
+        Wh = W.cpu().numpy()
+        if m.fmt == "nvfp4":
+            nib, sc, gs = orc.nvfp4_quantise(Wh)
+            yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
+        else:
+            q, rs = orc.fp8_quantise(Wh)
+            yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
+        assert_close(orc, y, yref, a, m.name)
     plan.close()
 
 

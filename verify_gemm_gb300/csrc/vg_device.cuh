@@ -31,12 +31,15 @@ constexpr int kNvScaleLaneBytes = 2 * kNvChunkUnits;                    // 16
 constexpr int kNvScaleChunkBytes = 32 * kNvScaleLaneBytes;              // 512
 constexpr int kF8ChunkUnits = kNvChunkUnits / 2;
 
-// A row block is 16 row tiles (256 rows); a work item is one chunk of every
-// tile of a row block.  Each of the 16 consumer warps owns one tile of the
-// row block.  Items stream through a ring of kSlots shared-memory slots; one
-// slot holds a whole item: the 16 tiles' codes (8 NVFP4 units or 4 FP8 units
-// each, contiguous in the packed buffer), their block scales, and the x
-// slice (N rows of the chunk's columns).
+// A work item is 16 tile-chunks, one per consumer warp, arranged as rt row
+// tiles x (16 / rt) consecutive chunks of each; a row block is rt tiles.
+// rt = 16 (one chunk of 16 tiles) suits matrices with many rows.  For
+// matrices with few rows, a smaller rt gives more, shorter row blocks, so
+// that fewer thread blocks share one row block's K range and its partial
+// sums are added in fewer rounds (layout_rt below).  Items stream through a
+// ring of kSlots shared-memory slots; one slot holds a whole item: the 16
+// tile-chunks' codes (contiguous in the packed buffer), their block scales,
+// and the x slice (N rows of the item's columns).
 #ifndef VG_WARPS
 #define VG_WARPS 16
 #endif
@@ -50,15 +53,21 @@ constexpr int kSlots = VG_SLOTS;
 constexpr int kSlotCodeBytes = kNvChunkUnits * kNvUnitBytes;          // 4096: one tile's chunk
 constexpr int kThreads = kWarps * 32;
 // One x row of a chunk (512 BF16 columns) plus 16 bytes of padding, so that
-// the 8 rows read by a quarter warp fall in different banks.
+// the 8 rows read by a quarter warp fall in different banks.  Row-copied x
+// only serves items of one chunk (rt = 16).
 constexpr int kXRowBytes = kNvChunkUnits * kUnitK * 2 + 16;             // 1040
-// An item slot: codes of 16 tiles, then their scales, then the x slice: 8
-// rows, either padded rows of kXRowBytes (copied row by row) or one tensor
-// copy in the 128-byte-swizzled layout [unit][row][128 B], which needs
-// 1024-byte alignment (slots are multiples of 1024 bytes).
+// Units (64 columns each) of x one item may span: the tensor-copied slice is
+// 8 rows x 128 bytes per unit, 32 KB at most.
+constexpr int kMaxItemUnits = 32;
+// An item slot: codes of 16 tile-chunks, then their scales, then the x
+// slice: 8 rows, either padded rows of kXRowBytes (copied row by row) or one
+// tensor copy in the 128-byte-swizzled layout [unit][row][128 B], which
+// needs 1024-byte alignment (slots are multiples of 1024 bytes).
 constexpr int kItemScaleOff = kBlockTiles * kSlotCodeBytes;            // 65536
 constexpr int kItemXOff = kItemScaleOff + kBlockTiles * kNvScaleChunkBytes;  // 73728
-constexpr int kItemSlotBytes = (kItemXOff + 8 * kXRowBytes + 1023) / 1024 * 1024;  // 82944
+constexpr int kItemXBytes =
+    kMaxItemUnits * 1024 > 8 * kXRowBytes ? kMaxItemUnits * 1024 : 8 * kXRowBytes;
+constexpr int kItemSlotBytes = (kItemXOff + kItemXBytes + 1023) / 1024 * 1024;  // 106496
 static_assert(kItemXOff % 1024 == 0, "the swizzled x slice starts 1024-byte aligned");
 
 static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
@@ -66,24 +75,54 @@ static_assert(kF8ChunkUnits * kF8UnitBytes == kSlotCodeBytes,
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Item-contiguous order of the packed buffers.  Codes are grouped by row
-// block (16 tiles), then by chunk (cu units), then by tile, then by unit, so
-// that one work item -- one chunk of every tile of a row block -- is one
-// contiguous run of bytes and consecutive chunks of a row block follow each
-// other.  Only the last row block may have fewer than 16 tiles and only the
-// last chunk fewer than cu units; nothing is padded.
-__host__ __device__ inline int64_t code_offset(int64_t mt, int64_t u, int64_t MT, int64_t KU,
-                                               int64_t cu, int64_t ub) {
-  const int64_t rb = mt / 16, tile = mt % 16, c = u / cu, uu = u % cu;
-  const int64_t tiles = (MT - rb * 16) < 16 ? (MT - rb * 16) : 16;
-  const int64_t nu = (KU - c * cu) < cu ? (KU - c * cu) : cu;
-  return rb * 16 * KU * ub + c * tiles * cu * ub + tile * nu * ub + uu * ub;
+// Row tiles per row block of an M x K matrix with cu units per chunk.  The
+// work of one verify group is split over all SMs in contiguous item ranges,
+// so a row block of KC / (16 / rt) items is shared by about
+// rt * SMs / MT thread blocks.  The largest rt (fewest pieces per block) that
+// keeps that at 3 or less is taken; if none does, the smallest allowed.  An
+// rt below 16 is allowed only when every item is whole: K a multiple of the
+// chunk, the item's chunks dividing KC, and its x slice within
+// kMaxItemUnits.  The choice depends on (M, K, cu) alone, so the packers and
+// the GEMV agree on it; kLayoutSMs is the SM count it is tuned for (any
+// device runs any layout).
+constexpr int kLayoutSMs = 152;
+__host__ __device__ inline int layout_rt(int64_t M, int64_t K, int cu) {
+  const int64_t chunk_cols = int64_t(cu) * kUnitK;
+  if (K % chunk_cols != 0) return kBlockTiles;
+  const int64_t KC = K / chunk_cols, MT = ceil_div(M, kTileRows);
+  int smallest = kBlockTiles;
+  for (int rt = kBlockTiles; rt >= 2; rt /= 2) {
+    const int cpi = kBlockTiles / rt;
+    if (KC % cpi != 0 || cpi * cu > kMaxItemUnits) continue;
+    if (int64_t(rt) * kLayoutSMs <= 3 * MT) return rt;
+    smallest = rt;
+  }
+  return smallest;
 }
-// Byte offset of the scale chunk c of tile mt (same grouping).
-__host__ __device__ inline int64_t scale_offset(int64_t mt, int64_t c, int64_t MT, int64_t KC) {
-  const int64_t rb = mt / 16, tile = mt % 16;
-  const int64_t tiles = (MT - rb * 16) < 16 ? (MT - rb * 16) : 16;
-  return (rb * 16 * KC + c * tiles + tile) * kNvScaleChunkBytes;
+
+// Item-contiguous order of the packed buffers.  Codes are grouped by row
+// block (rt tiles), then by item (16 / rt consecutive chunks of cu units),
+// then by tile-chunk (tile-major: tile, then chunk), then by unit, so that
+// one work item is one contiguous run of bytes and consecutive items of a
+// row block follow each other.  Only the last row block may have fewer than
+// rt tiles and, with rt = 16, only the last chunk fewer than cu units;
+// nothing is padded.
+__host__ __device__ inline int64_t code_offset(int64_t mt, int64_t u, int64_t MT, int64_t KU,
+                                               int64_t cu, int64_t ub, int64_t rt) {
+  const int64_t cpi = kBlockTiles / rt, iu = cpi * cu;   // chunks, units per item
+  const int64_t rb = mt / rt, tl = mt % rt, c = u / cu, uu = u % cu, ci = c / cpi, cc = c % cpi;
+  const int64_t tiles = (MT - rb * rt) < rt ? (MT - rb * rt) : rt;
+  const int64_t nui = (KU - ci * iu) < iu ? (KU - ci * iu) : iu;  // a tail only when cpi == 1
+  return rb * rt * KU * ub + ci * tiles * iu * ub + (tl * cpi + cc) * (nui / cpi) * ub + uu * ub;
+}
+// Byte offset of the scales of chunk c of tile mt (same grouping; every
+// tile-chunk has kNvScaleChunkBytes of scales, also a K tail).
+__host__ __device__ inline int64_t scale_offset(int64_t mt, int64_t c, int64_t MT, int64_t KC,
+                                                int64_t rt) {
+  const int64_t cpi = kBlockTiles / rt;
+  const int64_t rb = mt / rt, tl = mt % rt, ci = c / cpi, cc = c % cpi;
+  const int64_t tiles = (MT - rb * rt) < rt ? (MT - rb * rt) : rt;
+  return (rb * rt * KC + ci * tiles * cpi + tl * cpi + cc) * kNvScaleChunkBytes;
 }
 
 // ------------------------------------------------------ decode constants
@@ -269,6 +308,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {

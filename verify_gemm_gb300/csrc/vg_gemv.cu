@@ -17,11 +17,14 @@
 //    the packed buffers; L2 evict-first) and one TMA tensor copy of its x
 //    slice (128-byte swizzle; L2 evict-last).  The weights never pass through
 //    registers of the producer.
-//  * A work item is one chunk (512 columns NVFP4, 256 FP8) of a row block of
-//    16 tiles (256 rows); consumer warp t owns tile t of it.  It decodes the
-//    codes in registers to BF16 A fragments (bit placement + one BF16x2
-//    multiply by the block scale, exact) and runs mma.m16n8k16 with x from
-//    the slot as the B fragment, accumulating FP32.
+//  * A work item is 16 tile-chunks (a chunk is 512 columns NVFP4, 256 FP8):
+//    one chunk of a row block of 16 tiles, or, for matrices with few rows,
+//    16 / rt consecutive chunks of a row block of rt tiles.  Consumer warp w
+//    owns tile-chunk w.  It decodes the codes in registers to BF16 A
+//    fragments (bit placement + one BF16x2 multiply by the block scale,
+//    exact) and runs mma.m16n8k16 with x from the slot as the B fragment,
+//    accumulating FP32; the warps that share a tile add their sums in
+//    shared memory at the end of a row block's piece.
 //  * Items are split between thread blocks stream-K style (contiguous item
 //    ranges of equal length), so every SM streams the same number of bytes.
 //    A row block whose K range is split between blocks is summed by the
@@ -61,7 +64,10 @@ struct MatDev {
   int fmt;
   int M, K, MT, KU, KC, RB;
   int cu, ub;        // units per chunk, bytes per unit
-  int64_t rb_bytes;  // code bytes of a full row block (16 tiles x KU units)
+  int rt, cpi;       // tiles per row block, chunks per item (16 / rt)
+  int iu, KI;        // units per item (cpi * cu), items per row block
+  int kfull;         // items wholly inside K
+  int64_t rb_bytes;  // code bytes of a full row block (rt tiles x KU units)
   int item0;         // first item of this matrix within its phase
   const CUtensorMap *xmap;  // x as [K/64 units][N rows][64 columns], or nullptr
 };
@@ -95,20 +101,25 @@ struct Params {
   PhaseDev phase0;
 };
 
-// One block's partial-sum slot: 4 FP32 sums per consumer thread, each in a
-// 64-bit word whose upper half is the tag of the pass and phase that wrote it.
+// One block's partial-sum slot: the 128 FP32 sums of each of up to 16 tiles,
+// each in a 64-bit word whose upper half is the tag of the pass and phase
+// that wrote it.
 constexpr int kPartialWords = kBlockTiles * 32 * 4;
 // Shared memory: the item ring, one zero x row (read for columns >= N), the
-// mbarriers (full, then empty, per slot) and a few flags.
+// mbarriers (full, then empty, per slot), a few flags, and the scratch in
+// which the warps sharing a tile hand their sums to the first of them.
 constexpr int kRingBytes = kSlots * kItemSlotBytes;
 // The zero row starts 16 bytes past a 128-byte line, like x row 1 of a slot,
 // so that lanes reading it and lanes reading row 0 use different banks.
 constexpr int kZeroRowOff = kRingBytes + 16;
 constexpr int kBarOff = kZeroRowOff + kXRowBytes;
 constexpr int kBarBytes = 2 * kSlots * 8;
-constexpr int kSmemUsed = kBarOff + kBarBytes + 64;
+constexpr int kRedOff = kBarOff + kBarBytes + 64;
+constexpr int kRedBytes = kWarps * 32 * 16;             // 4 FP32 sums per consumer thread
+constexpr int kSmemUsed = kRedOff + kRedBytes;
 constexpr int kSmemBytes = kSmemUsed + 1024;   // room to align the base to 1024 bytes
 static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
+static_assert(kRedOff % 16 == 0, "the sum scratch is read as 16-byte vectors");
 static_assert(kItemSlotBytes % 128 == 0 && kItemXOff % 128 == 0, "x rows start 128-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024, "fits one block per SM");
 constexpr int kConsumers = kWarps * 32;
@@ -137,42 +148,37 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uin
 }
 
 // The items one thread block processes, in order, across all phases: for
-// each phase with items for this block, its contiguous range [i0, i1).  The
-// position inside the current matrix (row block rb, chunk c) advances
-// incrementally; the only divisions happen when a phase starts.
+// each phase with items for this block, its contiguous range [i, i1).  The
+// position inside the current matrix (row block rb, item c) advances
+// incrementally; the only divisions happen when a phase starts.  The tables
+// and the grid come from the caller, so the sequencer holds only the
+// position (it is live across the streaming loops).
 struct Seq {
-  const MatDev *mats;
-  const PhaseDev *phases;
-  int nphases, ph, mi, mend;
-  int rb, c, KC, RB;
-  int b, grid, G, i, i0, i1, items;
+  int ph, mi;
+  int rb, c, KI, RB;   // row block, item within it; items per row block, row blocks
+  int i, i1, items, G; // item, end of the block's range; the phase's items and blocks
   bool valid;
 
-  __device__ void init(const MatDev *m, const PhaseDev *p, int np, int blk, int g) {
-    mats = m;
-    phases = p;
-    nphases = np;
-    b = blk;
-    grid = g;
+  __device__ void init(const MatDev *mats, const PhaseDev *phases, const Params &p) {
     ph = -1;
-    next_phase();
+    next_phase(mats, phases, p);
   }
-  __device__ void next_phase() {
-    for (++ph; ph < nphases; ++ph) {
+  __device__ void next_phase(const MatDev *mats, const PhaseDev *phases, const Params &p) {
+    const int b = int(blockIdx.x);
+    for (++ph; ph < p.nphases; ++ph) {
       items = phases[ph].items;
-      G = min(grid, items);
+      G = min(p.grid, items);
       if (b < G) {
-        i0 = item_begin(items, G, b);
+        i = item_begin(items, G, b);
         i1 = item_begin(items, G, b + 1);
-        i = i0;
         mi = phases[ph].mat_begin;
-        mend = phases[ph].mat_end;
-        while (mi + 1 < mend && i >= mats[mi].item0 + mats[mi].RB * mats[mi].KC) ++mi;
-        KC = mats[mi].KC;
+        const int mend = phases[ph].mat_end;
+        while (mi + 1 < mend && i >= mats[mi].item0 + mats[mi].RB * mats[mi].KI) ++mi;
+        KI = mats[mi].KI;
         RB = mats[mi].RB;
         const int rel = i - mats[mi].item0;
-        rb = rel / KC;
-        c = rel - rb * KC;
+        rb = rel / KI;
+        c = rel - rb * KI;
         valid = true;
         return;
       }
@@ -181,37 +187,27 @@ struct Seq {
   }
   // Skip the n items left in the current row block's piece (never past the
   // row block's end).
-  __device__ __forceinline__ void skip(int n) {
+  __device__ __forceinline__ void skip(int n, const MatDev *mats, const PhaseDev *phases,
+                                       const Params &p) {
     i += n;
     if (i == i1) {
-      next_phase();
+      next_phase(mats, phases, p);
       return;
     }
     c += n;
-    if (c == KC) {
+    if (c == KI) {
       c = 0;
       if (++rb == RB) {
         rb = 0;
         ++mi;
-        KC = mats[mi].KC;
+        KI = mats[mi].KI;
         RB = mats[mi].RB;
       }
     }
   }
-  __device__ __forceinline__ void advance() {
-    if (++i == i1) {
-      next_phase();
-      return;
-    }
-    if (++c == KC) {
-      c = 0;
-      if (++rb == RB) {
-        rb = 0;
-        ++mi;
-        KC = mats[mi].KC;
-        RB = mats[mi].RB;
-      }
-    }
+  __device__ __forceinline__ void advance(const MatDev *mats, const PhaseDev *phases,
+                                          const Params &p) {
+    skip(1, mats, phases, p);
   }
 };
 
@@ -369,13 +365,13 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, i
   }
 }
 
-// Byte offsets of tile `tile`'s codes and scales in item (rb, c) of m.
-__device__ __forceinline__ int64_t code_off(const MatDev &m, int rb, int c, int tiles, int tile,
-                                            int nu) {
-  return int64_t(rb) * m.rb_bytes + int64_t(c) * tiles * m.cu * m.ub + int64_t(tile) * nu * m.ub;
+// Byte offsets of item (rb, ci)'s codes and scales in m (of `tiles` tiles);
+// its tile-chunks follow one another in warp order.
+__device__ __forceinline__ int64_t item_code_off(const MatDev &m, int rb, int ci, int tiles) {
+  return int64_t(rb) * m.rb_bytes + int64_t(ci) * tiles * m.iu * m.ub;
 }
-__device__ __forceinline__ int64_t scale_off(const MatDev &m, int rb, int c, int tiles, int tile) {
-  return (int64_t(rb) * kBlockTiles * m.KC + int64_t(c) * tiles + tile) * kNvScaleChunkBytes;
+__device__ __forceinline__ int64_t item_scale_off(const MatDev &m, int rb, int ci, int tiles) {
+  return (int64_t(rb) * m.rt * m.KC + int64_t(ci) * tiles * m.cpi) * kNvScaleChunkBytes;
 }
 
 // Items beyond the ring that the producer brings into L2 while the consumers
@@ -396,12 +392,19 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
                          const volatile int *dep_waiting) {
   const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
   Seq q;
-  q.init(mats, phases, p.nphases, blockIdx.x, p.grid);
+  q.init(mats, phases, p);
   int s = 0;
   uint32_t par = 0;
   int64_t issued = 0;
   Seq pf = q;       // next item to bring into L2 during a dependency wait
   int pf_ahead = 0; // items between q and pf
+  // the current matrix's fields, cached while the matrix does not change
+  int cur_mi = -1;
+  const uint8_t *w = nullptr, *sc = nullptr;
+  const uint16_t *xg = nullptr;
+  const CUtensorMap *tmap = nullptr;
+  int rt = 0, MT = 0, KU = 0, K = 0, iu = 0, tile_item_bytes = 0, rb_scale_chunks = 0, cpi = 0, ub = 0;
+  int64_t rb_bytes = 0;
   while (q.valid) {
     if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
       const uint64_t deadline = globaltimer() + p.timeout_ns;
@@ -409,13 +412,13 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
       while (!(ok = mbar_test_wait(empty0 + 8 * s, par ^ 1u)) && globaltimer() <= deadline) {
         if (kBoundaryPf > 0 && *dep_waiting && pf_ahead < kBoundaryPf && pf.valid) {
           const MatDev &fm = mats[pf.mi];
-          const int ft = min(kBlockTiles, fm.MT - pf.rb * kBlockTiles);
-          const int fu = min(fm.cu, fm.KU - pf.c * fm.cu);
-          bulk_prefetch_l2(fm.w + code_off(fm, pf.rb, pf.c, ft, 0, fu), uint32_t(ft * fu * fm.ub));
+          const int ft = min(fm.rt, fm.MT - pf.rb * fm.rt);
+          const int fu = min(fm.iu, fm.KU - pf.c * fm.iu);
+          bulk_prefetch_l2(fm.w + item_code_off(fm, pf.rb, pf.c, ft), uint32_t(ft * fu * fm.ub));
           if (fm.fmt == VG_FMT_NVFP4)
-            bulk_prefetch_l2(fm.sc + scale_off(fm, pf.rb, pf.c, ft, 0),
-                             uint32_t(ft * kNvScaleChunkBytes));
-          pf.advance();
+            bulk_prefetch_l2(fm.sc + item_scale_off(fm, pf.rb, pf.c, ft),
+                             uint32_t(ft * fm.cpi * kNvScaleChunkBytes));
+          pf.advance(mats, phases, p);
           ++pf_ahead;
         }
       }
@@ -424,32 +427,50 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
         break;
       }
     }
-    const MatDev &m = mats[q.mi];
-    const int tiles = min(kBlockTiles, m.MT - q.rb * kBlockTiles);
-    const int nu = min(m.cu, m.KU - q.c * m.cu);
-    const uint32_t code_bytes = uint32_t(tiles * nu * m.ub);
-    const uint32_t scale_bytes = m.fmt == VG_FMT_NVFP4 ? uint32_t(tiles * kNvScaleChunkBytes) : 0u;
-    const int k0 = q.c * m.cu * kUnitK;
-    const CUtensorMap *tmap = p.mats ? m.xmap : (p.x0_tensor ? &p.xmap0 : nullptr);
-    // x: one tensor copy of 8 rows x the chunk's units (rows >= N and units
-    // past K read as zeros), else one bulk copy per row
-    const uint32_t x_bytes = tmap ? uint32_t(8 * m.cu * kUnitK * 2)
-                                  : uint32_t(min(m.cu * kUnitK, m.K - k0) * 2 * p.N);
+    if (q.mi != cur_mi) {
+      const MatDev &m = mats[q.mi];
+      cur_mi = q.mi;
+      w = m.w;
+      sc = m.fmt == VG_FMT_NVFP4 ? m.sc : nullptr;
+      xg = m.x;
+      tmap = p.mats ? m.xmap : (p.x0_tensor ? &p.xmap0 : nullptr);
+      rt = m.rt;
+      MT = m.MT;
+      KU = m.KU;
+      K = m.K;
+      iu = m.iu;
+      tile_item_bytes = m.iu * m.ub;
+      rb_bytes = m.rb_bytes;
+      rb_scale_chunks = m.rt * m.KC;
+      cpi = m.cpi;
+      ub = m.ub;
+    }
+    const int tiles = min(rt, MT - q.rb * rt);
+    const int nu = min(iu, KU - q.c * iu);   // units per tile in this item
+    const uint32_t code_bytes = uint32_t(tiles * nu * ub);
+    const uint32_t scale_bytes = sc ? uint32_t(tiles * cpi * kNvScaleChunkBytes) : 0u;
+    const int k0 = q.c * iu * kUnitK;
+    // x: one tensor copy of 8 rows x the item's units (rows >= N and units
+    // past K read as zeros), else one bulk copy per row (one-chunk items)
+    const uint32_t x_bytes = tmap ? uint32_t(8 * iu * kUnitK * 2)
+                                  : uint32_t(min(iu * kUnitK, K - k0) * 2 * p.N);
     const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
     mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes);
-    bulk_g2s(slot, m.w + code_off(m, q.rb, q.c, tiles, 0, nu), code_bytes, full, pol_w);
-    if (scale_bytes)
-      bulk_g2s(slot + kItemScaleOff, m.sc + scale_off(m, q.rb, q.c, tiles, 0), scale_bytes, full,
-               pol_w);
+    bulk_g2s(slot, w + int64_t(q.rb) * rb_bytes + int64_t(q.c) * tiles * tile_item_bytes, code_bytes,
+             full, pol_w);
+    if (sc)
+      bulk_g2s(slot + kItemScaleOff,
+               sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * kNvScaleChunkBytes,
+               scale_bytes, full, pol_w);
     if (tmap) {
-      bulk_tensor_3d(slot + kItemXOff, tmap, 0, 0, q.c * m.cu, full, pol_x);
+      bulk_tensor_3d(slot + kItemXOff, tmap, 0, 0, q.c * iu, full, pol_x);
     } else {
       const uint32_t row_bytes = x_bytes / uint32_t(p.N);
       for (int n = 0; n < p.N; ++n)
-        bulk_g2s(slot + kItemXOff + n * kXRowBytes, m.x + int64_t(n) * m.K + k0, row_bytes, full,
+        bulk_g2s(slot + kItemXOff + n * kXRowBytes, xg + int64_t(n) * K + k0, row_bytes, full,
                  pol_x);
     }
-    q.advance();
+    q.advance(mats, phases, p);
     if (pf_ahead > 0)
       --pf_ahead;
     else
@@ -474,10 +495,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
 // rounds need more than the 96 registers a thread gets with 17 warps per SM
 // and spill, which costs more than the rounds they save.
 // Returns false if the wait ran out or another block has already failed.
-#ifndef VG_COLLECT_W
-#define VG_COLLECT_W 2
-#endif
-constexpr int kCollectW = VG_COLLECT_W;
+constexpr int kCollectW = 2;
 
 __device__ __forceinline__ bool tags_match(const uint64_t (&v)[4], uint32_t tag) {
   return uint32_t(v[0] >> 32) == tag && uint32_t(v[1] >> 32) == tag &&
@@ -530,28 +548,46 @@ __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_
   return true;
 }
 
-// End of a row-block piece.  A block that covered the whole row block writes
-// y.  Otherwise the row block is split: the block holding its first item
-// (the reducer) adds the other contributors' partial sums to its own and
-// writes y; every other contributor publishes its partial sums in its slot,
-// tagged, and moves on without waiting.  In ordered mode the completed row
-// block is counted for its phase.  It runs once per piece, outside the
-// per-item loops.  Returns
+// End of a row-block piece.  With several chunks per item (cpi > 1) the
+// warps that share a tile first hand their sums to its first warp (cc == 0)
+// through shared memory, added in chunk order; only that warp goes on.
+// Then a block that covered the whole row block writes y.  Otherwise the
+// row block is split: the block holding its first item (the reducer) adds
+// the other contributors' partial sums to its own and writes y; every other
+// contributor publishes its partial sums in its slot, tagged, and moves on
+// without waiting.  In ordered mode the completed row block is counted for
+// its phase.  It runs once per piece, outside the per-item loops.  Returns
 // false if the wait for partial sums failed.
 __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, int T, int G,
                                           int piece_start, bool full_piece, int rb, int ph,
-                                          uint32_t tag, bool aborted, float a0, float a1,
-                                          float a2, float a3) {
+                                          uint32_t tag, bool aborted, int tl, int cc,
+                                          uint32_t red, float a0, float a1, float a2, float a3) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int mt = rb * kBlockTiles + warp;
+  const int mt = rb * m.rt + tl;
   const int at = ((warp * 2) * 32 + lane) * 2;    // this thread's words in a slot
   float accs[4] = {a0, a1, a2, a3};
+  if (m.cpi > 1) {
+    // barriers of the tile's warps only (ids 3.., one per tile of the block)
+    if (cc != 0) sts128(red + uint32_t(warp * 32 + lane) * 16u, accs[0], accs[1], accs[2], accs[3]);
+    named_bar(3 + tl, m.cpi * 32);
+    if (cc == 0) {
+      for (int j = 1; j < m.cpi; ++j) {
+        const uint4 q = lds128(red + uint32_t((warp + j) * 32 + lane) * 16u);
+        accs[0] += __uint_as_float(q.x);
+        accs[1] += __uint_as_float(q.y);
+        accs[2] += __uint_as_float(q.z);
+        accs[3] += __uint_as_float(q.w);
+      }
+    }
+    named_bar(3 + tl, m.cpi * 32);   // the scratch is free again
+  }
+  const bool lead = cc == 0;
   bool ok = true;
   if (!full_piece) {
-    const int first = m.item0 + rb * m.KC;
+    const int first = m.item0 + rb * m.KI;
     if (piece_start != first) {
-      if (!aborted) {
+      if (!aborted && lead) {
         uint64_t *dst = p.partials + int64_t(blockIdx.x) * kPartialWords + at;
         const uint64_t hi = uint64_t(tag) << 32;
         st_relaxed_v2u64(dst, hi | __float_as_uint(accs[0]), hi | __float_as_uint(accs[1]));
@@ -559,11 +595,12 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
       }
       return true;
     }
-    if (!aborted) ok = collect(p, int(blockIdx.x) + 1, owner(T, G, first + m.KC - 1), tag, at, accs);
+    if (!aborted && lead)
+      ok = collect(p, int(blockIdx.x) + 1, owner(T, G, first + m.KI - 1), tag, at, accs);
     // mma.sync needs whole warps: a failure anywhere in the warp stops it all
     ok = __all_sync(0xFFFFFFFFu, ok);
   }
-  if (ok && !aborted && mt < m.MT) {
+  if (ok && !aborted && lead && mt < m.MT) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = mt * kTileRows + g + 8 * h;
@@ -631,12 +668,12 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     // (128-byte swizzle), so a unit is 1024 bytes and the lane's two chunks
     // 2t, 2t+1 of row g sit at (2t ^ g) and next to it.  Row-copied slices
     // are padded rows of kXRowBytes, and a column g >= N reads a zero row.
-    const uint32_t xoff_t = uint32_t(kItemXOff + g * 128 + ((2 * t) ^ g) * 16);
+    const uint32_t xoff_t0 = uint32_t(kItemXOff + g * 128 + ((2 * t) ^ g) * 16);
     const int xd_t = (g & 1) ? -16 : 16;
     const uint32_t xoff_r = uint32_t(kItemXOff + g * kXRowBytes + t * 32);
     const uint32_t xzero = smem_addr(smem + kZeroRowOff) + t * 32;
     Seq cons;
-    cons.init(mats, phases, p.nphases, blockIdx.x, p.grid);
+    cons.init(mats, phases, p);
     bool aborted = false;
     int s = 0;                     // ring slot of the current item
     uint32_t par = 0;              // parity of that slot's current phase
@@ -644,8 +681,11 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     uint32_t tag = 0;              // tag of this pass and phase
     float acc[kAcc][4];
     // matrix fields cached while the matrix does not change
-    int K = 0, KU = 0, MT = 0, fmt = 0;
+    int K = 0, KU = 0, MT = 0, fmt = 0, rt = kBlockTiles, kfull = 0, iu = 0;
+    int tl = warp, cc = 0;         // this warp's tile and chunk within an item
+    uint32_t xoff_t = xoff_t0;     // ... and its x columns (tensor-copied x)
     bool xt = false;               // the matrix's x slice is tensor-copied
+    const uint32_t red = smem_addr(smem + kRedOff);   // tile-sum scratch
     while (cons.valid) {
       const int ph = cons.ph;
       // -------------------------------------- ordered: wait for group ph-1
@@ -690,19 +730,26 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         KU = mm.KU;
         MT = mm.MT;
         fmt = mm.fmt;
+        rt = mm.rt;
+        iu = mm.iu;
+        kfull = mm.kfull;
+        tl = warp / mm.cpi;
+        cc = warp - tl * mm.cpi;
+        // the warp's chunk starts cc chunks into the item's x slice
+        xoff_t = xoff_t0 + uint32_t(cc * mm.cu * 1024);
         xt = p.mats ? mm.xmap != nullptr : p.x0_tensor != 0;
       }
       // ------------------------------------------------- one row-block piece
       // the block's contiguous items of one row block: set up once, then a
       // tight loop over its chunks
       const int rb = cons.rb, c0 = cons.c;
-      const int len = min(cons.KC - c0, cons.i1 - cons.i);
+      const int len = min(cons.KI - c0, cons.i1 - cons.i);
       const int piece_start = cons.i;
 #pragma unroll
       for (int a = 0; a < kAcc; ++a)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-      const int mt = rb * kBlockTiles + warp;
+      const int mt = rb * rt + tl;
       const bool work = mt < MT;
       int c = c0;
       const int c_end = c0 + len;
@@ -711,8 +758,8 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
       if (!aborted && work && xt) {
         const uint32_t scl0 = kItemScaleOff + warp * kNvScaleChunkBytes;
         const uint32_t code0 = warp * kSlotCodeBytes;
+        const int c_full = min(c_end, kfull);
         if (fmt == VG_FMT_NVFP4) {
-          const int c_full = min(c_end, K / (kNvChunkUnits * kUnitK));
           for (; c < c_full; ++c) {
             const uint32_t item = ring + s * kItemSlotBytes;
             if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
@@ -728,7 +775,6 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
             }
           }
         } else {
-          const int c_full = min(c_end, K / (kF8ChunkUnits * kUnitK));
           for (; c < c_full; ++c) {
             const uint32_t item = ring + s * kItemSlotBytes;
             if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
@@ -761,12 +807,13 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         if (!aborted && work) {
           const uint32_t xs = xt ? item + xoff_t : (on ? item + xoff_r : xzero);
           const int xd = xt ? xd_t : 16, xu = xt ? 1024 : kUnitK * 2;
+          // item c's first column; items past kfull (a K tail) have one chunk
+          const int kc = c * iu * kUnitK;
           if (fmt == VG_FMT_NVFP4) {
-            const int kc = c * (kNvChunkUnits * kUnitK);
             const uint32_t scl = item + kItemScaleOff + warp * kNvScaleChunkBytes;
-            // warp-uniform test (mma.sync needs the whole warp): the chunk's
+            // warp-uniform test (mma.sync needs the whole warp): the item's
             // whole column range lies inside K
-            if (kc + kNvChunkUnits * kUnitK <= K) {
+            if (c < kfull) {
               const uint32_t code = item + warp * kSlotCodeBytes;
               if (xt)
                 nv_chunk_full<true>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
@@ -778,9 +825,8 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
                             K - kc - 16 * t, p.m8, p.m64, acc);
             }
           } else {
-            const int kc = c * (kF8ChunkUnits * kUnitK);
-            const bool full = kc + kF8ChunkUnits * kUnitK <= K;
-            const int nu = min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
+            const bool full = c < kfull;
+            const int nu = full ? kF8ChunkUnits : min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
             const uint32_t code = item + warp * nu * kF8UnitBytes;
             if (xt)
               f8_chunk<true>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
@@ -806,10 +852,10 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
       }
       if (!finish_piece(p, mats[cons.mi], cons.items, cons.G, piece_start,
-                        c0 == 0 && len == cons.KC, rb, ph, tag, aborted, accs[0], accs[1], accs[2],
-                        accs[3]))
+                        c0 == 0 && len == cons.KI, rb, ph, tag, aborted, tl, cc, red, accs[0],
+                        accs[1], accs[2], accs[3]))
         aborted = true;
-      cons.skip(len);
+      cons.skip(len, mats, phases, p);
     }
   }
 
@@ -929,8 +975,13 @@ MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, co
   m.cu = fmt == VG_FMT_NVFP4 ? kNvChunkUnits : kF8ChunkUnits;
   m.ub = fmt == VG_FMT_NVFP4 ? kNvUnitBytes : kF8UnitBytes;
   m.KC = int(ceil_div(m.KU, m.cu));
-  m.RB = int(ceil_div(m.MT, kBlockTiles));
-  m.rb_bytes = int64_t(kBlockTiles) * m.KU * m.ub;
+  m.rt = layout_rt(M, K, m.cu);
+  m.cpi = kBlockTiles / m.rt;
+  m.iu = m.cpi * m.cu;
+  m.KI = int(ceil_div(m.KU, m.iu));
+  m.kfull = int(K / (int64_t(m.iu) * kUnitK));
+  m.RB = int(ceil_div(m.MT, m.rt));
+  m.rb_bytes = int64_t(m.rt) * m.KU * m.ub;
   return m;
 }
 
@@ -973,7 +1024,7 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   int dev;
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
-  const int64_t T = int64_t(m0.RB) * m0.KC;
+  const int64_t T = int64_t(m0.RB) * m0.KI;
   int grid = 0;
   if (vg_status s = max_grid(*di, &grid)) return s;
   grid = int(i64min(grid, T));
@@ -993,7 +1044,9 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   set_head(p, ws);
   p.partials = reinterpret_cast<uint64_t *>(ws + kWsHead);
   p.mat0 = m0;
-  p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.cu) ? 1 : 0;
+  p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu) ? 1 : 0;
+  // items of several chunks take x by tensor copy only
+  if (!p.x0_tensor && m0.cpi > 1) return VG_ERR_UNSUPPORTED;
   p.phase0.items = int(T);
   p.phase0.rbs = m0.RB;
   p.phase0.mat_begin = 0;
@@ -1030,7 +1083,7 @@ extern "C" vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, si
   const MatDev m = make_mat(format, M, K, nullptr, nullptr, nullptr, 0.f, nullptr, nullptr);
   int grid = 0;
   if (vg_status s = max_grid(*di, &grid)) return s;
-  *bytes = ws_bytes(int(i64min(grid, int64_t(m.RB) * m.KC)));
+  *bytes = ws_bytes(int(i64min(grid, int64_t(m.RB) * m.KI)));
   return VG_OK;
 }
 
@@ -1127,8 +1180,8 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
     PhaseDev &ph = hp.back();
     hm[i].item0 = ph.items;
     // a phase's items are counted in 32 bits on the device
-    if (int64_t(ph.items) + int64_t(hm[i].RB) * hm[i].KC > int64_t(1) << 30) return VG_ERR_UNSUPPORTED;
-    ph.items += hm[i].RB * hm[i].KC;
+    if (int64_t(ph.items) + int64_t(hm[i].RB) * hm[i].KI > int64_t(1) << 30) return VG_ERR_UNSUPPORTED;
+    ph.items += hm[i].RB * hm[i].KI;
     ph.rbs += hm[i].RB;
     ph.mat_end = i + 1;
     bytes += algorithmic_bytes(hm[i]);
@@ -1151,10 +1204,13 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_phases, sizeof(PhaseDev) * hp.size());
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_state, plan->state_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_xmaps, sizeof(CUtensorMap) * hm.size());
+  bool untensored = false;   // an item of several chunks whose x has no tensor map
   if (e == cudaSuccess) {
     std::vector<CUtensorMap> maps(hm.size());
-    for (size_t i = 0; i < hm.size(); ++i)
-      hm[i].xmap = make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].cu) ? plan->d_xmaps + i : nullptr;
+    for (size_t i = 0; i < hm.size(); ++i) {
+      hm[i].xmap = make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].iu) ? plan->d_xmaps + i : nullptr;
+      if (!hm[i].xmap && hm[i].cpi > 1) untensored = true;
+    }
     e = cudaMemcpy(plan->d_xmaps, maps.data(), sizeof(CUtensorMap) * maps.size(),
                    cudaMemcpyHostToDevice);
   }
@@ -1163,6 +1219,11 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   if (e == cudaSuccess)
     e = cudaMemcpy(plan->d_phases, hp.data(), sizeof(PhaseDev) * hp.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(plan->d_state, 0, plan->state_bytes);
+  if (e == cudaSuccess && untensored) {
+    // items of several chunks take x by tensor copy only
+    vg_verify_plan_destroy(plan);
+    return VG_ERR_UNSUPPORTED;
+  }
   if (e != cudaSuccess) {
     set_cuda_error(e);
     vg_verify_plan_destroy(plan);

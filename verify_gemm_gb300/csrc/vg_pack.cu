@@ -73,19 +73,23 @@ __device__ __forceinline__ int f8_byte(int ri, int j, int ii) {
   return 4 * (2 * j + (ii >> 1)) + 2 * (ii & 1) + ri;
 }
 
+// Geometry of a packed matrix; rt: row tiles per row block (layout_rt).
 struct Geom {
-  int64_t M, K, MT, KU, KC;
+  int64_t M, K, MT, KU, KC, rt;
 };
 
-__host__ __device__ inline Geom nv_geom(int64_t M, int64_t K) {
+inline Geom geom(int64_t M, int64_t K, int cu) {
   Geom g;
   g.M = M;
   g.K = K;
   g.MT = ceil_div(M, kTileRows);
   g.KU = ceil_div(K, kUnitK);
-  g.KC = ceil_div(g.KU, kNvChunkUnits);
+  g.KC = ceil_div(g.KU, cu);
+  g.rt = layout_rt(M, K, cu);
   return g;
 }
+inline Geom nv_geom(int64_t M, int64_t K) { return geom(M, K, kNvChunkUnits); }
+inline Geom f8_geom(int64_t M, int64_t K) { return geom(M, K, kF8ChunkUnits); }
 
 // ----------------------------------------------------------- amax kernels
 
@@ -143,10 +147,10 @@ __global__ void nv_pack_kernel(const float *__restrict__ W, Geom G, float gs,
         words[kk >> 2] |= nv_place(c, ri, kk & 3);
       }
     }
-    sc_out[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC) + lane * kNvScaleLaneBytes +
+    sc_out[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC, G.rt) + lane * kNvScaleLaneBytes +
            (u % kNvChunkUnits) * 2 + ri] = uint8_t(scale_code_from_e4m3(code));
   }
-  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes) +
+  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes, G.rt) +
                              lane * 16) =
       make_uint4(words[0], words[1], words[2], words[3]);
 }
@@ -161,7 +165,7 @@ __global__ void nv_unpack_kernel(const uint8_t *__restrict__ w, const uint8_t *_
   const int64_t k0 = u * kUnitK + 16 * t;
   if (k0 >= G.K) return;
   const uint4 v = *reinterpret_cast<const uint4 *>(
-      w + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes) + lane * 16);
+      w + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes, G.rt) + lane * 16);
   const uint32_t words[4] = {v.x, v.y, v.z, v.w};
   for (int ri = 0; ri < 2; ++ri) {
     const int64_t row = mt * kTileRows + g + 8 * ri;
@@ -176,7 +180,7 @@ __global__ void nv_unpack_kernel(const uint8_t *__restrict__ w, const uint8_t *_
         hi |= c << (4 * (kk - 8));
     }
     *reinterpret_cast<uint2 *>(nib + row * (G.K / 2) + k0 / 2) = make_uint2(lo, hi);
-    const uint8_t d = sc[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC) + lane * kNvScaleLaneBytes +
+    const uint8_t d = sc[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC, G.rt) + lane * kNvScaleLaneBytes +
                          (u % kNvChunkUnits) * 2 + ri];
     scc[row * (G.K / 16) + k0 / 16] = uint8_t(e4m3_from_scale_code(d));
   }
@@ -219,10 +223,10 @@ __global__ void nv_from_canonical_kernel(const uint8_t *__restrict__ nib,
         }
       }
     }
-    sc_out[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC) + lane * kNvScaleLaneBytes +
+    sc_out[scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC, G.rt) + lane * kNvScaleLaneBytes +
            (u % kNvChunkUnits) * 2 + ri] = uint8_t(scale_code_from_e4m3(code));
   }
-  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes) +
+  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes, G.rt) +
                              lane * 16) =
       make_uint4(words[0], words[1], words[2], words[3]);
 }
@@ -252,7 +256,7 @@ __global__ void f8_pack_kernel(const float *__restrict__ W, const float *__restr
     }
   }
   uint4 *dst = reinterpret_cast<uint4 *>(
-      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes) + lane * 32);
+      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes, G.rt) + lane * 32);
   dst[0] = *reinterpret_cast<const uint4 *>(out);
   dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
 }
@@ -267,7 +271,7 @@ __global__ void f8_unpack_kernel(const uint8_t *__restrict__ w, Geom G, uint8_t 
   if (k0 >= G.K) return;
   uint8_t in[32];
   const uint4 *src = reinterpret_cast<const uint4 *>(
-      w + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes) + lane * 32);
+      w + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes, G.rt) + lane * 32);
   *reinterpret_cast<uint4 *>(in) = src[0];
   *reinterpret_cast<uint4 *>(in + 16) = src[1];
   for (int ri = 0; ri < 2; ++ri) {
@@ -309,7 +313,7 @@ __global__ void f8_from_canonical_kernel(const uint8_t *__restrict__ q, Geom G,
     for (int kk = 0; kk < 16; ++kk) out[f8_byte(ri, kk >> 2, kk & 3)] = in[kk];
   }
   uint4 *dst = reinterpret_cast<uint4 *>(
-      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes) + lane * 32);
+      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes, G.rt) + lane * 32);
   dst[0] = *reinterpret_cast<const uint4 *>(out);
   dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
 }
@@ -340,7 +344,7 @@ extern "C" vg_status vg_nvfp4_sizes(int64_t M, int64_t K, size_t *w_bytes, size_
 
 extern "C" vg_status vg_fp8_sizes(int64_t M, int64_t K, size_t *w_bytes) {
   if (vg_status s = check_mk(M, K)) return s;
-  const Geom G = nv_geom(M, K);
+  const Geom G = f8_geom(M, K);
   if (w_bytes) *w_bytes = size_t(G.MT * G.KU * kF8UnitBytes);
   return VG_OK;
 }
@@ -378,7 +382,7 @@ extern "C" vg_status vg_fp8_pack(const float *W, int64_t M, int64_t K, void *w_o
   if (!W || !w_out || !rowscale_out) return VG_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(w_out) || !aligned16(rowscale_out)) return VG_ERR_ALIGNMENT;
   cudaStream_t st = as_cuda(stream);
-  const Geom G = nv_geom(M, K);
+  const Geom G = f8_geom(M, K);
   f8_rowscale_kernel<<<blocks_for(M, 8), 256, 0, st>>>(W, M, K, rowscale_out);
   VG_LAUNCH_CHECK();
   std::vector<float> rs(static_cast<size_t>(M));
@@ -413,7 +417,7 @@ extern "C" vg_status vg_fp8_unpack(const void *w, int64_t M, int64_t K, uint8_t 
   if (vg_status s = check_mk(M, K)) return s;
   if (!w || !q_out) return VG_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(q_out)) return VG_ERR_ALIGNMENT;
-  const Geom G = nv_geom(M, K);
+  const Geom G = f8_geom(M, K);
   const int64_t threads = G.MT * G.KU * 32;
   f8_unpack_kernel<<<blocks_for(threads, 256), 256, 0, as_cuda(stream)>>>(
       static_cast<const uint8_t *>(w), G, q_out);
@@ -452,7 +456,7 @@ extern "C" vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t 
   if (!q || !w_out) return VG_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(w_out)) return VG_ERR_ALIGNMENT;
   cudaStream_t st = as_cuda(stream);
-  const Geom G = nv_geom(M, K);
+  const Geom G = f8_geom(M, K);
   uint32_t *bad_dev = static_cast<uint32_t *>(w_out);   // scratch, rewritten below
   VG_CUDA(cudaMemsetAsync(bad_dev, 0, sizeof(uint32_t), st));
   f8_check_canonical_kernel<<<reduce_blocks(M * K), 256, 0, st>>>(q, M * K, bad_dev);
