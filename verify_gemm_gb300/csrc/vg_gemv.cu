@@ -167,7 +167,10 @@ struct Seq {
     const int b = int(blockIdx.x);
     for (++ph; ph < p.nphases; ++ph) {
       items = phases[ph].items;
-      G = min(p.grid, items);
+      // as few blocks as keep the largest per-block item count: fewer
+      // blocks then share each row block (shorter reductions)
+      const int per = (items + p.grid - 1) / p.grid;
+      G = (items + per - 1) / per;
       if (b < G) {
         i = item_begin(items, G, b);
         i1 = item_begin(items, G, b + 1);
