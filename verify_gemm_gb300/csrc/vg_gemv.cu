@@ -387,9 +387,12 @@ constexpr int kBoundaryPf = VG_BPF;
 // The producer (one lane): fill the item ring, one whole item per slot, as
 // soon as all 16 consumer warps have released the slot.  An item's codes are
 // one contiguous range of the packed buffer and its scales another, so an
-// item is two bulk copies (L2 evict-first: read once) plus one per x row (x
-// is read by every block: evict-last).  Columns past K are not copied; the
-// consumers mask them.
+// item is two bulk copies (L2 evict-first: read once) plus the x slice (x is
+// read by every block: evict-last), one tensor copy or one copy per x row.
+// Columns past K are zero-filled or not copied; the consumers mask them.
+// The current matrix's fields are kept in registers: this lane shares an SM
+// sub-partition with busy consumer warps, and descriptor reads per item
+// delay the refill.
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0,
                          const volatile int *dep_waiting) {
