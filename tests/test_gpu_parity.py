@@ -412,6 +412,46 @@ def test_verify_pass_ordered_and_unordered_agree(vg):
     assert torch.allclose(outs[0].float(), outs[1].float(), rtol=2e-2, atol=1e-2)
 
 
+def test_graph_capture_replays_gemv_and_verify_pass(vg):
+    """A GEMV and an ordered verify pass captured in one CUDA graph replay to
+    the same bits as the eager calls: the launches are cooperative, their x
+    tensor maps travel in the kernel parameters, and the workspace and plan
+    state advance on the device, so each replay leaves them clean."""
+    M, K, N = 520, 2560, 8
+    wt = vg.nvfp4_pack(rand_w(5, M, K).cuda())
+    x = rand_x(6, N, K).cuda()
+    ws = vg.workspace_for(wt)
+    y_eager = vg.gemv(wt, x, workspace=ws)
+    st = _small_stack(vg, 4, True)
+    plan = st.plan(ordered=True)
+    st.y_all.zero_()
+    plan.run()
+    torch.cuda.synchronize()
+    stack_eager = st.y_all.clone()
+    y = torch.empty_like(y_eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):            # warm-up on a side stream
+        vg.gemv(wt, x, y=y, workspace=ws)
+        plan.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        vg.gemv(wt, x, y=y, workspace=ws)
+        plan.run()
+    for _ in range(3):
+        y.zero_()
+        st.y_all.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_eager)
+        assert torch.equal(st.y_all, stack_eager)
+    assert vg.workspace_error(ws) == 0
+    assert plan.check() == 0
+    plan.close()
+
+
 def test_verify_pass_wait_timeout_reports_error(vg):
     """A group whose completion is never signalled makes the next group's
     bounded wait run out: the pass returns, the plan reports a timeout, and
