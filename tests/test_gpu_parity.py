@@ -397,6 +397,38 @@ def test_verify_pass_multi_chunk_items(vg, orc, N, ordered):
     plan.close()
 
 
+@pytest.mark.parametrize("ordered", [True, False])
+def test_verify_pass_mixed_item_shapes_in_one_group(vg, orc, ordered):
+    """One group holding matrices whose items have different shapes: 16-tile
+    row blocks (256 x 512), 8-tile row blocks of 2-chunk items (NVFP4
+    100 x 1024) and 2-tile row blocks of 8-chunk items (FP8 100 x 4096),
+    followed by a second group; every product matches the oracle."""
+    N = 6
+    specs = [("nvfp4", 256, 512, 0), ("nvfp4", 100, 1024, 0), ("fp8", 100, 4096, 0),
+             ("nvfp4", 300, 1024, 1)]
+    entries, refs = [], []
+    for i, (fmt, M, K, group) in enumerate(specs):
+        W = rand_w(90 + i, M, K)
+        x = rand_x(190 + i, N, K).cuda()
+        y = torch.zeros((N, M), dtype=torch.bfloat16, device="cuda")
+        if fmt == "nvfp4":
+            wt = vg.nvfp4_pack(W.cuda())
+            nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+            refs.append(orc.gemv_nvfp4(nib, sc, gs, bits(x.cpu()), threads=THREADS))
+        else:
+            wt = vg.fp8_pack(W.cuda())
+            q, rs = orc.fp8_quantise(W.numpy())
+            refs.append(orc.gemv_fp8(q, rs, bits(x.cpu()), threads=THREADS))
+        entries.append((wt, x, y, group))
+    plan = vg.VerifyPlan(entries, N, ordered=ordered)
+    for _ in range(2):
+        plan.run()
+        assert plan.check() == 0
+        for (fmt, M, K, _), (_, _, y, _), (yref, a) in zip(specs, entries, refs):
+            assert_close(orc, y, yref, a, f"{fmt} {M}x{K}")
+    plan.close()
+
+
 def test_verify_pass_ordered_and_unordered_agree(vg):
     st = _small_stack(vg, 4, True, layers=3)
     outs = []
