@@ -390,9 +390,16 @@ constexpr int kBoundaryPf = VG_BPF;
 // item is two bulk copies (L2 evict-first: read once) plus the x slice (x is
 // read by every block: evict-last), one tensor copy or one copy per x row.
 // Columns past K are zero-filled or not copied; the consumers mask them.
-// The current matrix's fields are kept in registers: this lane shares an SM
-// sub-partition with busy consumer warps, and descriptor reads per item
-// delay the refill.
+// The time from a slot's release to its refill adds to every item, so the
+// next item's addresses and sizes are worked out before the wait (the
+// current matrix's fields kept in registers), and the wait parks the lane in
+// hardware (mbarrier try_wait with a time hint) instead of spinning on the
+// sub-partition it shares with four consumer warps.  While the consumers
+// wait on a group dependency it polls instead and brings items beyond the
+// ring into L2.
+#ifndef VG_PARK_NS
+#define VG_PARK_NS 2000
+#endif
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0,
                          const volatile int *dep_waiting) {
@@ -403,7 +410,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   uint32_t par = 0;
   int64_t issued = 0;
   Seq pf = q;       // next item to bring into L2 during a dependency wait
-  int pf_ahead = 0; // items between q and pf
+  int pf_ahead = 0; // items between q and pf (pf is stale while 0)
   // the current matrix's fields, cached while the matrix does not change
   int cur_mi = -1;
   const uint8_t *w = nullptr, *sc = nullptr;
@@ -412,27 +419,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   int rt = 0, MT = 0, KU = 0, K = 0, iu = 0, tile_item_bytes = 0, rb_scale_chunks = 0, cpi = 0, ub = 0;
   int64_t rb_bytes = 0;
   while (q.valid) {
-    if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
-      const uint64_t deadline = globaltimer() + p.timeout_ns;
-      bool ok = false;
-      while (!(ok = mbar_test_wait(empty0 + 8 * s, par ^ 1u)) && globaltimer() <= deadline) {
-        if (kBoundaryPf > 0 && *dep_waiting && pf_ahead < kBoundaryPf && pf.valid) {
-          const MatDev &fm = mats[pf.mi];
-          const int ft = min(fm.rt, fm.MT - pf.rb * fm.rt);
-          const int fu = min(fm.iu, fm.KU - pf.c * fm.iu);
-          bulk_prefetch_l2(fm.w + item_code_off(fm, pf.rb, pf.c, ft), uint32_t(ft * fu * fm.ub));
-          if (fm.fmt == VG_FMT_NVFP4)
-            bulk_prefetch_l2(fm.sc + item_scale_off(fm, pf.rb, pf.c, ft),
-                             uint32_t(ft * fm.cpi * kNvScaleChunkBytes));
-          pf.advance(mats, phases, p);
-          ++pf_ahead;
-        }
-      }
-      if (!ok) {
-        set_error(p.error, kErrEmptyWait);
-        break;
-      }
-    }
+    // ---- the item's copies, worked out before its slot is free
     if (q.mi != cur_mi) {
       const MatDev &m = mats[q.mi];
       cur_mi = q.mi;
@@ -460,14 +447,45 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     // past K read as zeros), else one bulk copy per row (one-chunk items)
     const uint32_t x_bytes = tmap ? uint32_t(8 * iu * kUnitK * 2)
                                   : uint32_t(min(iu * kUnitK, K - k0) * 2 * p.N);
+    const uint8_t *code_src = w + int64_t(q.rb) * rb_bytes + int64_t(q.c) * tiles * tile_item_bytes;
+    const uint8_t *scale_src =
+        sc ? sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * kNvScaleChunkBytes : nullptr;
     const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
+
+    // ---- wait for the slot
+    if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
+      const uint64_t deadline = globaltimer() + p.timeout_ns;
+      bool ok = false;
+      for (;;) {
+        if (kBoundaryPf > 0 && *dep_waiting && pf_ahead < kBoundaryPf) {
+          if (pf_ahead == 0) pf = q;   // start at the item waiting for this slot
+          if (pf.valid) {
+            const MatDev &fm = mats[pf.mi];
+            const int ft = min(fm.rt, fm.MT - pf.rb * fm.rt);
+            const int fu = min(fm.iu, fm.KU - pf.c * fm.iu);
+            bulk_prefetch_l2(fm.w + item_code_off(fm, pf.rb, pf.c, ft), uint32_t(ft * fu * fm.ub));
+            if (fm.fmt == VG_FMT_NVFP4)
+              bulk_prefetch_l2(fm.sc + item_scale_off(fm, pf.rb, pf.c, ft),
+                               uint32_t(ft * fm.cpi * kNvScaleChunkBytes));
+            pf.advance(mats, phases, p);
+            ++pf_ahead;
+          }
+          if ((ok = mbar_test_wait(empty0 + 8 * s, par ^ 1u))) break;
+        } else if ((ok = mbar_try_wait_hint(empty0 + 8 * s, par ^ 1u, VG_PARK_NS))) {
+          break;
+        }
+        if (globaltimer() > deadline) break;
+      }
+      if (!ok) {
+        set_error(p.error, kErrEmptyWait);
+        break;
+      }
+    }
+
+    // ---- issue
     mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes);
-    bulk_g2s(slot, w + int64_t(q.rb) * rb_bytes + int64_t(q.c) * tiles * tile_item_bytes, code_bytes,
-             full, pol_w);
-    if (sc)
-      bulk_g2s(slot + kItemScaleOff,
-               sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * kNvScaleChunkBytes,
-               scale_bytes, full, pol_w);
+    bulk_g2s(slot, code_src, code_bytes, full, pol_w);
+    if (sc) bulk_g2s(slot + kItemScaleOff, scale_src, scale_bytes, full, pol_w);
     if (tmap) {
       bulk_tensor_3d(slot + kItemXOff, tmap, 0, 0, q.c * iu, full, pol_x);
     } else {
@@ -477,10 +495,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
                  pol_x);
     }
     q.advance(mats, phases, p);
-    if (pf_ahead > 0)
-      --pf_ahead;
-    else
-      pf = q;
+    if (pf_ahead > 0) --pf_ahead;
     ++issued;
     if (++s == kSlots) {
       s = 0;
