@@ -217,7 +217,7 @@ struct Seq {
 // MMA steps j = 0..3 of a unit accumulate into acc[j % kAcc]: with kAcc
 // accumulators the dependent MMA chains are kAcc times shorter.
 #ifndef VG_NACC
-#define VG_NACC 2
+#define VG_NACC 1   // one chain measured fastest: 16 warps hide the MMA latency
 #endif
 constexpr int kAcc = VG_NACC;
 
