@@ -10,9 +10,11 @@
 // rate), so the kernel is built to stream bytes at HBM speed.
 //
 // Design (sm_103a):
-//  * Persistent thread blocks, one per SM: 16 consumer warps + 1 producer
-//    warp.  The producer (one lane) keeps a 2-slot ring of shared memory
-//    full, one whole work item per slot, guarded by full/empty mbarriers:
+//  * Persistent thread blocks, one per SM: 16 consumer warps + 2 producer
+//    warps.  The producers (one lane each; in a verify pass one per slot,
+//    in a single product the first alone) keep a 2-slot ring of shared
+//    memory full, one whole work item per slot, guarded by full/empty
+//    mbarriers:
 //    one bulk copy of the item's codes and one of its scales (contiguous in
 //    the packed buffers; L2 evict-first) and one TMA tensor copy of its x
 //    slice (128-byte swizzle; L2 evict-last).  The weights never pass through
@@ -123,7 +125,10 @@ static_assert(kRedOff % 16 == 0, "the sum scratch is read as 16-byte vectors");
 static_assert(kItemSlotBytes % 128 == 0 && kItemXOff % 128 == 0, "x rows start 128-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024, "fits one block per SM");
 constexpr int kConsumers = kWarps * 32;
-constexpr int kKernelThreads = kConsumers + 32;        // + the producer warp
+// + two producer warps (sub-partitions 0 and 1): in a verify pass each fills
+// one ring slot, every other item; a single product uses the first alone
+constexpr int kProducers = 2;
+constexpr int kKernelThreads = kConsumers + 32 * kProducers;
 constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3, kErrPartialWait = 4;
 // Header words of a workspace (GEMV) or plan state: error, finished blocks,
 // pass epoch; then, 256 bytes in, the per-phase counters (plans) and the
@@ -397,18 +402,26 @@ constexpr int kBoundaryPf = VG_BPF;
 // sub-partition it shares with four consumer warps.  While the consumers
 // wait on a group dependency it polls instead and brings items beyond the
 // ring into L2.
+//
+// A verify pass runs two producers (np = 2), each owning one ring slot and
+// so every other item: the refill work, which slows the consumer warps that
+// share its sub-partition (and every slot release waits for the slowest
+// warp), is split over two sub-partitions.  A single product, a short
+// launch, runs one producer over both slots (np = 1): there the second
+// measured 1-2 us slower per launch.  `which` is the producer's index.
 #ifndef VG_PARK_NS
 #define VG_PARK_NS 2000
 #endif
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0,
-                         const volatile int *dep_waiting) {
+                         const volatile int *dep_waiting, int which, int np) {
   const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
   Seq q;
   q.init(mats, phases, p);
-  int s = 0;
+  if (which && q.valid) q.advance(mats, phases, p);
+  int s = which;
+  uint32_t used = 0, last_par = 0;   // per slot (bit s): issued into, its last parity
   uint32_t par = 0;
-  int64_t issued = 0;
   Seq pf = q;       // next item to bring into L2 during a dependency wait
   int pf_ahead = 0; // items between q and pf (pf is stale while 0)
   // the current matrix's fields, cached while the matrix does not change
@@ -457,7 +470,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
       const uint64_t deadline = globaltimer() + p.timeout_ns;
       bool ok = false;
       for (;;) {
-        if (kBoundaryPf > 0 && *dep_waiting && pf_ahead < kBoundaryPf) {
+        if (kBoundaryPf > 0 && which == 0 && *dep_waiting && pf_ahead < kBoundaryPf) {
           if (pf_ahead == 0) pf = q;   // start at the item waiting for this slot
           if (pf.valid) {
             const MatDev &fm = mats[pf.mi];
@@ -494,17 +507,19 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
         bulk_g2s(slot + kItemXOff + n * kXRowBytes, xg + int64_t(n) * K + k0, row_bytes, full,
                  pol_x);
     }
-    q.advance(mats, phases, p);
-    if (pf_ahead > 0) --pf_ahead;
-    ++issued;
-    if (++s == kSlots) {
-      s = 0;
+    used |= 1u << s;
+    last_par = (last_par & ~(1u << s)) | (par << s);
+    for (int k = 0; k < np && q.valid; ++k) q.advance(mats, phases, p);
+    pf_ahead = pf_ahead > np ? pf_ahead - np : 0;
+    s += np;
+    if (s >= kSlots) {
+      s -= kSlots;
       par ^= 1u;
     }
   }
   // Never leave while a bulk copy may still be writing shared memory.
-  for (int64_t k = i64max(0, issued - kSlots); k < issued; ++k)
-    mbar_wait_for(full0 + 8 * int(k % kSlots), uint32_t(k / kSlots) & 1u, p.timeout_ns);
+  for (int k = 0; k < kSlots; ++k)
+    if ((used >> k) & 1u) mbar_wait_for(full0 + 8 * k, (last_par >> k) & 1u, p.timeout_ns);
 }
 
 // The reducer of a split row block adds the partial sums of the other
@@ -671,11 +686,12 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   __syncthreads();
   const uint32_t epoch = uint32_t(sflag[1]);
 
-  if (warp == kWarps) {
+  if (warp >= kWarps) {
     // ================================================================ producer
-    if (lane == 0)
+    const int np = p.mats ? kProducers : 1;
+    if (lane == 0 && warp - kWarps < np)
       producer(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots),
-               sflag + 3);
+               sflag + 3, warp - kWarps, np);
 
   } else {
     // =============================================================== consumers
