@@ -293,10 +293,13 @@ __device__ __forceinline__ void load_scale_words(uint32_t a, uint32_t (&w)[kNvCh
 // x columns of unit 0 in the slot (or in a zero row for a column >= N).
 // kTensorX: the slice is tensor-copied (units 1024 bytes apart, the next 16
 // columns at xd_t = +-16), else row-copied (units 128 bytes apart, +16).
+// empty: if nonzero, the slot's empty mbarrier, arrived on (lane 0, after a
+// warp sync) as soon as the last two units are in registers, so the slot is
+// refilled while the warp computes them.
 template <bool kTensorX>
 __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
                                               int xd_t, uint32_t m8, uint32_t m64,
-                                              float (&acc)[kAcc][4]) {
+                                              float (&acc)[kAcc][4], uint32_t empty = 0) {
   constexpr int kXUnit = kTensorX ? 1024 : kUnitK * 2;
   const int xd = kTensorX ? xd_t : 16;
   uint32_t scw[kNvChunkUnits / 2];
@@ -314,6 +317,11 @@ __device__ __forceinline__ void nv_chunk_full(uint32_t slot, uint32_t scl, int l
       nx0b = lds128(xs + (2 * h + 2) * kXUnit + xd);
       nx1a = lds128(xs + (2 * h + 3) * kXUnit);
       nx1b = lds128(xs + (2 * h + 3) * kXUnit + xd);
+    }
+    if (h + 1 == kNvChunkUnits / 2 && empty != 0) {
+      // every read of the slot is done (the arrive releases them)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty);
     }
     // unit 2h uses scale bytes 0,1 of word h; unit 2h+1 bytes 2,3
     nv_unit(w0, nv_scale_pair(scw[h], 0), nv_scale_pair(scw[h], 1), x0a, x0b, m8, m64, acc);
@@ -802,10 +810,9 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
             if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
                 !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
               break;   // the general loop below records the failure
+            // releases the slot itself, before computing its last two units
             nv_chunk_full<true>(item + code0, item + scl0, lane, item + xoff_t, xd_t, p.m8, p.m64,
-                                acc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+                                acc, empty0 + 8 * s);
             if (++s == kSlots) {
               s = 0;
               par ^= 1u;
