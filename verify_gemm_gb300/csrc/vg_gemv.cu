@@ -128,6 +128,9 @@ constexpr int kConsumers = kWarps * 32;
 // + two producer warps (sub-partitions 0 and 1): in a verify pass each fills
 // one ring slot, every other item; a single product uses the first alone
 constexpr int kProducers = 2;
+// each producer owns whole slots (items of one slot in order): a slot's parity
+// waits would alias if two producers took turns on it
+static_assert(kSlots % kProducers == 0, "every producer owns its own ring slots");
 constexpr int kKernelThreads = kConsumers + 32 * kProducers;
 constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3, kErrPartialWait = 4;
 // Header words of a workspace (GEMV) or plan state: error, finished blocks,
