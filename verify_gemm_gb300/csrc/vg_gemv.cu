@@ -552,6 +552,7 @@ __device__ __forceinline__ bool tags_match(const uint64_t (&v)[4], uint32_t tag)
 __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_t tag, int at,
                                         float (&accs)[4]) {
   uint64_t deadline = 0;
+  uint32_t polls = 0;
   for (int bb = b0; bb <= bl; bb += kCollectW) {
     uint64_t v[kCollectW][4];
     uint32_t pending = 0;
@@ -569,14 +570,16 @@ __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_
       for (int j = 0; j < kCollectW; ++j)
         if (((pending >> j) & 1u) && tags_match(v[j], tag)) pending &= ~(1u << j);
       if (pending == 0) break;
-      const uint64_t now = globaltimer();
-      if (deadline == 0) {
-        deadline = now + p.timeout_ns;
-      } else if (now > deadline) {
-        set_error(p.error, kErrPartialWait);
-        return false;
+      if ((++polls & 7u) == 0) {   // clock and error word every 8th poll
+        const uint64_t now = globaltimer();
+        if (deadline == 0) {
+          deadline = now + p.timeout_ns;
+        } else if (now > deadline) {
+          set_error(p.error, kErrPartialWait);
+          return false;
+        }
+        if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
       }
-      if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
 #pragma unroll
       for (int j = 0; j < kCollectW; ++j) {
         if ((pending >> j) & 1u) {
@@ -747,15 +750,20 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
               const uint32_t target = uint32_t(phases[ph - 1].rbs);
               if (ld_acquire(d) < target) {
                 const uint64_t deadline = globaltimer() + p.timeout_ns;
+                uint32_t it = 0;
+                // one L2 round trip per poll: the clock and the error word
+                // are looked at every 8th poll only
                 while (ld_acquire(d) < target) {
-                  if (globaltimer() > deadline) {
-                    ok = 0;
-                    set_error(p.error, kErrDepWait);
-                    break;
-                  }
-                  if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) {
-                    ok = 0;   // another block has failed: results are void
-                    break;
+                  if ((++it & 7u) == 0) {
+                    if (globaltimer() > deadline) {
+                      ok = 0;
+                      set_error(p.error, kErrDepWait);
+                      break;
+                    }
+                    if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) {
+                      ok = 0;   // another block has failed: results are void
+                      break;
+                    }
                   }
                   __nanosleep(32);
                 }
