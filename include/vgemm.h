@@ -15,8 +15,8 @@
  * the card's Decode row runs 2-8 columns and a decode step one.  The
  * card's Measured section states what makes it the hot path: a verify pass
  * reads every weight once (19.26 GB), so its time is the weight-read time;
- * the crit README's quality-mode comparison says the same ("a decode pass
- * reads every weight once").
+ * the crit README's quality-mode comparison makes the same point for a
+ * decode pass.
  *
  * Conventions (all entry points):
  *  - Plain C; nothing throws across the ABI; every call returns a

@@ -62,8 +62,9 @@ float vgo_amax(const float *W, int64_t n);
 void vgo_nvfp4_quantise_gs(const float *W, int64_t M, int64_t K, float gs,
                            uint8_t *nib, uint8_t *sc);
 
-/* Row-scaled FP8-E4M3 quantisation (engine card, Model section: "re-encoded
- * as row-scaled FP8").  Returns 0, or -1 if W holds a NaN/Inf. */
+/* Row-scaled FP8-E4M3 quantisation (engine card, Model section: a layer
+ * stored as FP8 with one scale per row).  Returns 0, or -1 if W holds a
+ * NaN/Inf. */
 int vgo_fp8_quantise(const float *W, int64_t M, int64_t K,
                      uint8_t *q, float *rs_out);
 
