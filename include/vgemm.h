@@ -281,8 +281,8 @@ typedef struct vg_plan_options {
 
 /* Plan a fused verify pass over `count` matrices for N columns: one
  * persistent, cooperative launch streams every weight once, groups in
- * order (engine card, Decode row: the verify pass for the drafts made, 2-8
- * columns; Measured section: 19.26 GB read per pass).  Allocates the
+ * order (engine card, Decode row: one verify step checks all drafted
+ * tokens at once, 2-8 columns; Measured section: 19.26 GB read per pass).  Allocates the
  * plan's descriptor table, counters and partial-sum space once.
  * Descriptors (pointers included) are copied; buffer contents may change
  * between passes.  Each item's slice of x is copied into shared memory by
