@@ -139,7 +139,7 @@ GEMV_SHAPES = [
     (33, 48, (4,)),               # K below one unit (row-copied x)
     (300, 1600, (3, 8)),          # K a multiple of 64 with a 1-unit tail chunk
     # items of several chunks of fewer tiles (row blocks of rt < 16 tiles)
-    (100, 1024, (1, 8)),          # NVFP4 rt 8: one ragged row block; FP8 rt 4: two
+    (100, 1024, (1, 7, 8)),       # NVFP4 rt 8: one ragged row block; FP8 rt 4: two
     (100, 4096, (2, 8)),          # NVFP4 rt 4, FP8 rt 2 (8 chunks): row blocks split in two
     (5000, 2048, (8,)),           # rt 4, 79 row blocks, the last of 2 tiles and 8 rows
     (333, 3072, (5,)),            # NVFP4 rt 8, FP8 rt 4, three items per row block
