@@ -528,3 +528,17 @@ def test_full_stack_sampled(vg, orc):
             yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
         assert_close(orc, y[:, rows], yref, a, m.name)
     plan.close()
+
+
+def test_readme_python_example_runs(vg):
+    """The Python example in README.md runs as written."""
+    import os
+    import re
+
+    text = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "README.md")).read()
+    blocks = re.findall(r"```python\n(.*?)```", text, re.S)
+    assert blocks, "README has a Python example"
+    scope = {}
+    exec(compile(blocks[0], "README.md example", "exec"), scope)
+    y = scope["y"]
+    assert y.shape == (8, 5120) and y.dtype == torch.bfloat16 and torch.isfinite(y.float()).all()
