@@ -144,6 +144,12 @@ def dist_init(args):
     return ranks.world, ranks.rank, ranks.local
 
 
+def pcts(xs, qs):
+    """Nearest-rank percentiles of xs for each q in qs (0..100)."""
+    v = sorted(xs)
+    return [v[min(len(v) - 1, max(0, int(round(q / 100 * (len(v) - 1)))))] for q in qs]
+
+
 def barrier(world):
     from verify_gemm_gb300 import replicas
 
@@ -370,6 +376,8 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_ms / args.steps, 4),
+            # this rank's per-pass times (events between passes), p10 / p50 / p90
+            "us_per_step_p10_p50_p90": [round(1e3 * q, 1) for q in pcts(per, (10, 50, 90))],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "weights": WEIGHTS, "data": "synthetic",
             "config": {"workload": workload_name(args), "N": args.N, "mode": "ordered",
