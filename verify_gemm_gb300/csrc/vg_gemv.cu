@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     *reinterpret_cast<uint4 *>(smem + kZeroRowOff + tid * 16) = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(smem_addr(bars + i), 1);                       // full: the producer
+      mbar_init(smem_addr(bars + i), 1);                       // full: the slot's producer
       mbar_init(smem_addr(bars + kSlots + i), kWarps);         // empty: every consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
