@@ -501,14 +501,16 @@ def test_verify_pass_wait_timeout_reports_error(vg):
     plan.close()
 
 
-def test_full_stack_sampled(vg, orc):
+@pytest.mark.parametrize("attn_fmt", ["nvfp4", "fp8"])
+def test_full_stack_sampled(vg, orc, attn_fmt):
     """The 64-layer stack + head in the launch configuration the benchmark
-    times (ordered, N = 8): sampled matrices checked row-sampled."""
+    times (ordered, N = 8): sampled matrices checked row-sampled.  With FP8
+    q/k/v/o (the 19.28 GB mix) those run as items of 4 tiles x 4 chunks."""
     from verify_gemm_gb300.inputs import draw_stack_matrix
     from verify_gemm_gb300.workloads import build_stack
 
     N = 8
-    st = build_stack(N)
+    st = build_stack(N, attn_fmt=attn_fmt)
     plan = st.plan(ordered=True)
     plan.run()
     assert plan.check() == 0
