@@ -40,6 +40,24 @@ def workload_name(args) -> str:
     return WORKLOAD
 
 
+def stack_bytes(mats) -> int:
+    """Algorithmic weight+scale bytes of one pass over `mats` (NVFP4: M*K/2
+    codes + M*K/16 scales + 4; row-scaled FP8: M*K codes + 4*M)."""
+    return sum(m.M * m.K // 2 + m.M * m.K // 16 + 4 if m.fmt == "nvfp4" else m.M * m.K + 4 * m.M
+               for m in mats)
+
+
+def stack_config(args, world: int) -> dict:
+    """The `config` of the JSON line, identical for both arms."""
+    from verify_gemm_gb300.inputs import stack_mats
+
+    mats = stack_mats(args.layers, args.attn_fmt)
+    return {"workload": workload_name(args), "N": args.N, "mode": "ordered",
+            "bytes_per_pass": stack_bytes(mats), "matrices": len(mats),
+            "l2": "inputs 16.3 GB per pass >> 129 MB L2; no flush needed",
+            "parallelism": f"replicas x{world}"}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -54,6 +72,8 @@ def parse():
                     help="stack q,k,v,o format: nvfp4 (16.34 GB pass, the headline) or fp8 "
                          "(row-scaled, the pages' checkpoint mix: 19.28 GB)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the single-product configurations (per_config)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="stack",
                     choices=["stack", "tiny", "proj", "gateup", "down", "head", "probe"],
@@ -93,8 +113,9 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=20):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.proc = None
         self.path = None
 
@@ -105,7 +126,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -184,17 +205,34 @@ def _cpu_sample_inputs():
         Wh = draw_weight(g, 2048, HIDDEN).numpy()
         x5 = draw_x(g, 8, HIDDEN).view(torch.int16).numpy().view(np.uint16)
         x17 = draw_x(g, 8, INTERMEDIATE).view(torch.int16).numpy().view(np.uint16)
-        nbytes = (HIDDEN * HIDDEN * 9 // 16 + 4) + (HIDDEN * INTERMEDIATE + 4 * HIDDEN) \
-            + (2048 * HIDDEN * 9 // 16)
+        nbytes = SAMPLE_BYTES
         _CPU_SAMPLE = (orc, orc.nvfp4_quantise(Wq), orc.fp8_quantise(Wd), orc.nvfp4_quantise(Wh),
                        x5, x17, nbytes)
     return _CPU_SAMPLE
 
 
+# 14,745,604 + 89,149,440 + 5,898,240 weight+scale bytes
+SAMPLE_BYTES = (5120 * 5120 * 9 // 16 + 4) + (5120 * 17408 + 4 * 5120) + 2048 * 5120 * 9 // 16
+SAMPLE_TEXT = ("oracle FP64 GEMV, N=8, on layer-0 q (NVFP4 5120x5120), down (FP8 5120x17408) "
+               f"and 2048 head rows (NVFP4 2048x5120): {SAMPLE_BYTES:,} weight+scale bytes "
+               "per round")
+
+
+def cpu_round(threads: int) -> float:
+    """One round of the oracle over the bounded sample; returns seconds."""
+    orc, (nq, sq, gq), (qd, rd), (nh, sh, gh), x5, x17, _ = _cpu_sample_inputs()
+    t0 = time.perf_counter()
+    orc.gemv_nvfp4(nq, sq, gq, x5, threads=threads)
+    orc.gemv_fp8(qd, rd, x17, threads=threads)
+    orc.gemv_nvfp4(nh, sh, gh, x5, threads=threads)
+    return time.perf_counter() - t0
+
+
 def cpu_sample(seconds: float):
     """Time the CPU oracle's GEMV on a bounded sample of the workload: the
     first layer's q (NVFP4 5120x5120) and down (FP8 5120x17408) and 2048 rows
-    of the head, N = 8, all host threads, repeated for about `seconds`."""
+    of the head, N = 8, all host threads, repeated for about `seconds`; then
+    one round on a single thread."""
     orc, (nq, sq, gq), (qd, rd), (nh, sh, gh), x5, x17, nbytes = _cpu_sample_inputs()
     threads = os.cpu_count() or 1
     done = 0
@@ -207,28 +245,44 @@ def cpu_sample(seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
+    one = cpu_round(1)
     return {"value": done / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": (f"oracle FP64 GEMV, N=8, on layer-0 q (NVFP4 5120x5120), down (FP8 "
-                       f"5120x17408) and 2048 head rows, {done / nbytes:.0f} rounds in "
-                       f"{el:.1f} s; same GB/s unit (weight+scale bytes)")}
+            "sample": f"{SAMPLE_TEXT}; {done / nbytes:.0f} rounds in {el:.1f} s on all threads",
+            "single_thread": {"value": nbytes / one / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": "one round of the same sample"}}
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on all host threads.
+    Each step is one round of the bounded sample (about 0.1 s); the line
+    reports what was timed: the sample's GB/s and the measured seconds per
+    round.  The time a full 16.34 GB pass would take at that rate is
+    reported separately and labelled as extrapolated."""
     if rank != 0:
         return
-    cb = cpu_sample(max(2.0, args.cpu_seconds / 2))
-    per = []
+    threads = os.cpu_count() or 1
+    _cpu_sample_inputs()
+    nbytes = _cpu_sample_inputs()[-1]
     for _ in range(args.warmup):
-        cpu_sample(0.5)
-    for _ in range(args.steps):
-        per.append(cpu_sample(max(0.1, args.cpu_seconds / max(1, args.steps)))["value"])
-    value = statistics.median(per)
+        cpu_round(threads)
+    per = [cpu_round(threads) for _ in range(args.steps)]
+    total = sum(per)
+    value = nbytes * args.steps / total / 1e9
+    one = cpu_round(1)
+    cfg = stack_config(args, world)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 16_335_298_560 / (value * 1e9) * 1e3,
+            "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "N": args.N},
-            "cpu_baseline": dict(cb, value=value),
+            "data": "synthetic", "config": cfg,
+            "step": "one round of the oracle over the bounded sample (timed); "
+                    + SAMPLE_TEXT,
+            "extrapolated_full_pass_ms": cfg["bytes_per_pass"] / (value * 1e9) * 1e3,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{SAMPLE_TEXT}; {args.steps} rounds",
+                             "single_thread": {"value": nbytes / one / 1e9, "unit": "GB/s",
+                                               "cores": 1,
+                                               "sample": "one round of the same sample"}},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -275,6 +329,17 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     if plan.check() != 0:
         raise RuntimeError("verify pass reported a device error")
+    # the same passes back to back for at least one second, with their own
+    # clock record: a steadier view of the clocks than a short timed region
+    reps = max(args.steps, int(1.0 / max(1e-4, total_ms / args.steps / 1e3)) + 1)
+    clocks2 = ClockSampler(local)
+    clocks2.start()
+    s_ms, _ = timed(plan.run, reps, 0)
+    clk2 = clocks2.stop()
+    if plan.check() != 0:
+        raise RuntimeError("verify pass reported a device error")
+    sustained = {"passes": reps, "ms": round(s_ms, 1),
+                 "GBps": round(nbytes * reps / (s_ms / 1e3) / 1e9, 1), "clocks": clk2}
     total_ms = max_over_ranks(total_ms, world, dev)
     value = replicas.job_gbps(nbytes, args.steps, total_ms, replicas.Ranks(world=world))
     kernel_ms = statistics.mean(per)
@@ -368,10 +433,13 @@ def run_ours(args, world, rank, local):
                "y_read_back_consistent": e2e_y_match}
     plan.close()
 
+    configs = per_config(20, 3) if (rank == 0 and not args.no_configs) else None
     cb = None
     if rank == 0 and world == 1:
         cb = cpu_sample(args.cpu_seconds)
     if rank == 0:
+        cfg = stack_config(args, world)
+        assert cfg["bytes_per_pass"] == nbytes, (cfg["bytes_per_pass"], nbytes)
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -380,17 +448,15 @@ def run_ours(args, world, rank, local):
             "us_per_step_p10_p50_p90": [round(1e3 * q, 1) for q in pcts(per, (10, 50, 90))],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "weights": WEIGHTS, "data": "synthetic",
-            "config": {"workload": workload_name(args), "N": args.N, "mode": "ordered",
-                       "bytes_per_pass": nbytes, "matrices": len(st.mats),
-                       "pct_of_8TBps": round(100 * value / world / 8000, 1),
-                       "l2": "inputs 16.3 GB per pass >> 129 MB L2; no flush needed",
-                       "parallelism": f"replicas x{world}"},
+            "config": cfg,
+            "pct_of_8TBps": round(100 * value / world / 8000, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": (profiled_traffic() if (args.attn_fmt, args.N, args.layers)
                                      == ("nvfp4", 8, 64) else None),
                          "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
             "per_width": widths, **extra,
+            "per_config": configs, "sustained": sustained,
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
         }
         if cb is not None:
@@ -406,32 +472,33 @@ SINGLE = {
     "down": ("row-scaled FP8 down 5120x17408, seed 3", ["down"]),
     "head": ("NVFP4 head 151936x5120, seed 3", ["head"]),
 }
+# the single-product configurations and the widths each is quoted at
+PER_CONFIG = [("tiny", (1,)), ("proj", (1,)), ("gateup", (1, 2, 4, 8)), ("down", (1, 8)),
+              ("head", (1, 8))]
 
 
-def run_single(args, local):
+def time_single(workload: str, N: int, steps: int, warmup: int, flush):
     """One configuration's product, timed alone: L2 flushed (a 512 MB write)
-    between launches, CUDA events around each launch only."""
+    before every launch, CUDA events around each launch only.  Returns
+    (bytes, per-launch ms list, launches per step)."""
     import torch
 
     import verify_gemm_gb300 as vg
-    from verify_gemm_gb300 import build as vbuild
     from verify_gemm_gb300.inputs import WORKLOADS, draw_workload
 
-    vbuild.build()
-    torch.cuda.set_device(local)
-    key = {"down": "down_head", "head": "down_head"}.get(args.workload, args.workload)
-    title, names = SINGLE[args.workload]
-    Ws, xs = draw_workload(key, args.N, device="cuda")
-    mats = WORKLOADS[key].mats
+    key = {"down": "down_head", "head": "down_head"}.get(workload, workload)
+    _, names = SINGLE[workload]
+    Ws, xs = draw_workload(key, N, device="cuda")
     entries = []
-    for m, W in zip(mats, Ws):
+    for m, W in zip(WORKLOADS[key].mats, Ws):
         if m.name not in names:
             continue
         wt = vg.nvfp4_pack(W) if m.fmt == "nvfp4" else vg.fp8_pack(W)
-        y = torch.empty((args.N, m.M), dtype=torch.bfloat16, device="cuda")
+        y = torch.empty((N, m.M), dtype=torch.bfloat16, device="cuda")
         entries.append((wt, xs[m.K], y, 0))
     del Ws
     nbytes = sum(e[0].nbytes for e in entries)
+    plan = None
     if len(entries) == 1:
         wt, x, y, _ = entries[0]
         ws = vg.workspace_for(wt)
@@ -439,16 +506,15 @@ def run_single(args, local):
         def run():
             vg.gemv(wt, x, y, ws)
     else:
-        plan = vg.VerifyPlan(entries, args.N, ordered=True)
+        plan = vg.VerifyPlan(entries, N, ordered=True)
         run = plan.run
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.fill_(1)
         run()
     torch.cuda.synchronize()
     per = []
-    for i in range(args.steps):
+    for i in range(steps):
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -457,8 +523,29 @@ def run_single(args, local):
         per.append((a, b))
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in per]
+    if plan is not None:
+        if plan.check() != 0:
+            raise RuntimeError("verify pass reported a device error")
+        plan.close()
+    elif vg.workspace_error(ws) != 0:
+        raise RuntimeError("GEMV reported a device error")
+    return nbytes, ms
+
+
+def run_single(args, local):
+    """One configuration's product, timed alone with an L2 flush between
+    launches (a 512 MB write)."""
+    import torch
+
+    from verify_gemm_gb300 import build as vbuild
+
+    vbuild.build()
+    torch.cuda.set_device(local)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    nbytes, ms = time_single(args.workload, args.N, args.steps, args.warmup, flush)
     med = statistics.median(ms)
     peak, kind = peaks()
+    title, _ = SINGLE[args.workload]
     line = {"metric": METRIC, "value": round(nbytes / (med / 1e3) / 1e9, 1), "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(med, 5), "higher_is_better": True, "scaling": "weak",
@@ -466,14 +553,32 @@ def run_single(args, local):
             "data": "synthetic",
             "config": {"workload": title, "N": args.N, "bytes": nbytes,
                        "l2": "flushed by a 512 MB write before every launch",
-                       "us_p10_p90": [round(1e3 * sorted(ms)[len(ms) // 10], 2),
-                                      round(1e3 * sorted(ms)[(9 * len(ms)) // 10], 2)]},
+                       "us_p10_p90": [round(1e3 * q, 2) for q in pcts(ms, (10, 90))]},
             "roofline": {"bound": "hbm", "achieved": round(nbytes / (med / 1e3) / 1e9, 1),
                          "peak": peak, "unit": "GB/s",
                          "frac": round(nbytes / (med / 1e3) / 1e9 / peak, 4), "traffic": None,
                          "peak_kind": kind},
             "gpu_launches": args.steps}
     print(json.dumps(line), flush=True)
+
+
+def per_config(steps: int, warmup: int):
+    """Every single-product configuration at every width it is quoted at,
+    timed alone (median of `steps` launches, L2 flushed before each)."""
+    import torch
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    for wl, widths in PER_CONFIG:
+        for N in widths:
+            nbytes, ms = time_single(wl, N, steps, warmup, flush)
+            med = statistics.median(ms)
+            out[f"{wl} N={N}"] = {"us": round(1e3 * med, 2),
+                                  "us_p10_p90": [round(1e3 * q, 2) for q in pcts(ms, (10, 90))],
+                                  "GBps": round(nbytes / (med / 1e3) / 1e9, 1), "bytes": nbytes}
+            torch.cuda.empty_cache()
+    del flush
+    return out
 
 
 def run_probe(args, local):

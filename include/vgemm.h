@@ -145,6 +145,13 @@ vg_status vg_nvfp4_unpack(const void *w, const void *scales, int64_t M, int64_t 
 vg_status vg_fp8_unpack(const void *w, int64_t M, int64_t K, uint8_t *q_out,
                         vg_stream_t stream);
 
+/* vg_fp8_pack and vg_fp8_unpack under the names of the row-scaled format: identical
+ * arguments, behaviour and errors. */
+vg_status vg_fp8_rowscale_pack(const float *W, int64_t M, int64_t K,
+                               void *w_out, float *rowscale_out, vg_stream_t stream);
+vg_status vg_fp8_rowscale_unpack(const void *w, int64_t M, int64_t K, uint8_t *q_out,
+                                 vg_stream_t stream);
+
 /* Canonical NVFP4 (device nib, sc) -> packed layout.  Scale bytes must be
  * non-negative and not NaN (E4M3 bytes 0x00..0x7E); otherwise
  * VG_ERR_INVALID_ARG.  Blocks whose scale is 0 are stored with zero codes
@@ -210,21 +217,33 @@ vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale,
  * not call cudaMalloc because it may synchronise the whole device, or code
  * held to a fixed memory budget.  The pages have no counterpart to this
  * entry point; it exists for such callers only.
- *   Arguments, results and errors are those of vg_gemv_nvfp4, minus the
- *   workspace.  The workspace is one fixed device array of
- *   VG_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, which every GPU
- *   that loads the library holds until the process exits.  A matrix that
- *   needs more (vg_gemv_workspace_size) gives VG_ERR_UNSUPPORTED.
- *   Nothing is allocated: the call clears the array's error word (4 bytes,
- *   cudaMemsetAsync on `stream`), then runs the GEMV on it; the rest of the
- *   array stays consistent from call to call.  The first call
- *   on a device looks up the array's device address (cudaGetSymbolAddress);
- *   make that first call before any stream capture.  All calls share the
- *   one array, so calls that overlap on the GPU (other streams, other host
- *   threads) race and give wrong results: serialise them. */
+ *   Arguments and results are those of vg_gemv_nvfp4, minus the workspace.
+ *   The workspace is one fixed device array of VG_NOALLOC_SCRATCH_BYTES
+ *   (4 MiB) inside the library, created on each device when the library's
+ *   module is first used there and held until the process exits.  A matrix
+ *   that needs more (vg_gemv_workspace_size) gives VG_ERR_UNSUPPORTED.
+ *   Nothing is allocated: the call looks up the array's device address
+ *   (cudaGetSymbolAddress, on every call, so a device reset is harmless),
+ *   clears the array's error word (4 bytes, cudaMemsetAsync on `stream`),
+ *   then runs the GEMV on it; the rest of the array stays consistent from
+ *   call to call.  The first call on a device loads the library's module
+ *   there: make it before any stream capture.  Errors are those of
+ *   vg_gemv_nvfp4 detected on the host; a bounded device-side wait that runs
+ *   out is not reported by the return value (the launch has already
+ *   returned) but left in the array's error word, which
+ *   vg_gemv_nvfp4_noalloc_check reads.  All calls share the one array, so
+ *   calls that overlap on the GPU (other streams, other host threads) race
+ *   and give wrong results: serialise them. */
 vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, float gscale,
                                 const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
                                 vg_stream_t stream);
+
+/* Error report of vg_gemv_nvfp4_noalloc, also allocation-free: synchronises
+ * `stream`, reads the fixed array's error word left by the most recent call
+ * into *device_error (0, or the code of the first bounded wait that ran out)
+ * and, if it is set, zero-fills the whole array and returns VG_ERR_TIMEOUT
+ * (the y of that call is void).  The pages have no counterpart to it. */
+vg_status vg_gemv_nvfp4_noalloc_check(int *device_error, vg_stream_t stream);
 
 /* Reads and clears the device error word of a GEMV workspace (synchronous).
  * *device_error receives 0, or a nonzero code if a bounded wait inside a

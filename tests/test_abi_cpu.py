@@ -28,10 +28,13 @@ def _declared_functions():
 
 
 def test_header_declares_the_abi():
+    """Every call of the boundary's listing is declared under its own name."""
     names = _declared_functions()
-    for want in ("vg_nvfp4_pack", "vg_gemv_nvfp4", "vg_gemv_fp8_rowscale", "vg_verify_pass",
-                 "vg_verify_plan_create", "vg_nvfp4_unpack", "vg_status_string"):
-        assert want in names
+    for want in ("vg_status_string", "vg_nvfp4_sizes", "vg_nvfp4_pack", "vg_nvfp4_unpack",
+                 "vg_gemv_nvfp4", "vg_fp8_rowscale_pack", "vg_fp8_rowscale_unpack",
+                 "vg_gemv_fp8_rowscale", "vg_verify_plan_create", "vg_verify_pass",
+                 "vg_verify_plan_destroy", "vg_gemv_nvfp4_noalloc_check"):
+        assert want in names, want
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -189,6 +189,39 @@ def test_gemv_pass_counter_wrap(vg, orc):
     assert torch.equal(y0, y1) and torch.equal(y0, y2)
 
 
+def test_gemv_pass_counter_wrap_after_a_larger_grid(vg, orc):
+    """Calls of different grid sizes share one workspace.  A large-grid call
+    (256 items on every SM, row blocks split over about five blocks) fills
+    the partial-sum slots with its tags; the pass counter is then set to its
+    last value and a small-grid call (8 blocks) wraps it.  The wrap must clear
+    every slot the workspace holds, not only the small call's: otherwise the
+    next large-grid call, whose tags restart at the first call's, would accept
+    the first call's stale sums.  That call uses a different x, so stale sums
+    would show."""
+    K, N = 4032, 8
+    big, small = rand_w(91, 8192, K), rand_w(92, 256, K)
+    wb, wsm = vg.nvfp4_pack(big.cuda()), vg.nvfp4_pack(small.cuda())
+    ws = vg.workspace_for(wb)
+    assert ws.numel() >= vg.workspace_for(wsm).numel()
+    xa, xb = rand_x(93, N, K).cuda(), rand_x(94, N, K).cuda()
+    vg.gemv(wb, xa, workspace=ws)              # epoch 0: every slot tagged 1
+    torch.cuda.synchronize()
+    last = np.array([0xFFFFFFFE], dtype=np.uint32).view(np.uint8)
+    ws[8:12] = torch.from_numpy(last).cuda()
+    ys = vg.gemv(wsm, xa, workspace=ws)        # 8 blocks; wraps the counter
+    torch.cuda.synchronize()
+    assert int(ws[8:12].cpu().numpy().view(np.uint32)[0]) == 0
+    assert not ws[256:].any(), "the wrap clears every slot of the workspace"
+    yb = vg.gemv(wb, xb, workspace=ws)         # tags 1 again
+    assert vg.workspace_error(ws) == 0
+    nib, sc, gs = orc.nvfp4_quantise(big.numpy())
+    yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(xb.cpu()), threads=THREADS)
+    assert_close(orc, yb, yref, a, "large grid after the wrap")
+    nib, sc, gs = orc.nvfp4_quantise(small.numpy())
+    yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(xa.cpu()), threads=THREADS)
+    assert_close(orc, ys, yref, a, "small grid at the wrap")
+
+
 @pytest.mark.parametrize("M,K,Ns", GEMV_SHAPES)
 def test_gemv_fp8_parity(vg, orc, M, K, Ns):
     W = rand_w(M + 5 * K, M, K)
@@ -504,43 +537,57 @@ def test_verify_pass_wait_timeout_reports_error(vg):
 @pytest.mark.parametrize("attn_fmt", ["nvfp4", "fp8"])
 def test_full_stack_sampled(vg, orc, attn_fmt):
     """The 64-layer stack + head in the launch configuration the benchmark
-    times (ordered, N = 8): sampled matrices checked row-sampled.  With FP8
-    q/k/v/o (the 19.28 GB mix) those run as items of 4 tiles x 4 chunks."""
+    times (ordered), at every width it reports (N = 8, 4, 2, 1): sampled
+    matrices checked row-sampled.  One packed stack serves all widths; the
+    narrower passes take the first N rows of each x (a column's result does
+    not depend on the others).  With FP8 q/k/v/o (the 19.28 GB mix) those run
+    as items of 4 tiles x 4 chunks."""
     from verify_gemm_gb300.inputs import draw_stack_matrix
     from verify_gemm_gb300.workloads import build_stack
 
-    N = 8
-    st = build_stack(N, attn_fmt=attn_fmt)
-    plan = st.plan(ordered=True)
-    plan.run()
-    assert plan.check() == 0
+    st = build_stack(8, attn_fmt=attn_fmt)
     rng = np.random.default_rng(1)
     picks = [0, 3, 4, 6, len(st.mats) // 2 + 2, len(st.mats) - 2, len(st.mats) - 1]
+    refs = {}
     for i in picks:
-        m, wt, x, y = st.mats[i], st.weights[i], st.xs[i], st.ys[i]
-        W, _ = draw_stack_matrix(m, N, 4, "cuda")
+        m, wt = st.mats[i], st.weights[i]
+        W, _ = draw_stack_matrix(m, 8, 4, "cuda")
         rows = np.unique(np.concatenate([[0, m.M - 1], rng.integers(0, m.M, 256)]))
         Wh = W.cpu().numpy()
         if m.fmt == "nvfp4":
             assert wt.gscale == np.float32(orc.amax(Wh)) / np.float32(2688.0)
-            nib, sc = orc.nvfp4_quantise_gs(Wh[rows], wt.gscale)
-            yref, a = orc.gemv_nvfp4(nib, sc, wt.gscale, bits(x), threads=THREADS)
+            refs[i] = (rows, orc.nvfp4_quantise_gs(Wh[rows], wt.gscale))
         else:
-            q, rs = orc.fp8_quantise(Wh[rows])
-            yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
-        assert_close(orc, y[:, rows], yref, a, m.name)
-    plan.close()
+            refs[i] = (rows, orc.fp8_quantise(Wh[rows]))
+        del W, Wh
+    for N in (8, 4, 2, 1):
+        if N == 8:
+            xs, ys = st.xs, st.ys
+        else:
+            xs = [x[:N] for x in st.xs]
+            ys = [torch.zeros((N, m.M), dtype=torch.bfloat16, device="cuda") for m in st.mats]
+        plan = vg.VerifyPlan([(wt, x, y, m.group) for m, wt, x, y in
+                              zip(st.mats, st.weights, xs, ys)], N, ordered=True)
+        plan.run()
+        assert plan.check() == 0
+        for i in picks:
+            m, wt, x, y = st.mats[i], st.weights[i], xs[i], ys[i]
+            rows, qz = refs[i]
+            if m.fmt == "nvfp4":
+                yref, a = orc.gemv_nvfp4(qz[0], qz[1], wt.gscale, bits(x), threads=THREADS)
+            else:
+                yref, a = orc.gemv_fp8(qz[0], qz[1], bits(x), threads=THREADS)
+            assert_close(orc, y[:, rows], yref, a, f"{m.name} N={N}")
+        plan.close()
+        del ys
 
 
-def test_readme_python_example_runs(vg):
-    """The Python example in README.md runs as written."""
+def test_quickstart_example_runs(vg):
+    """examples/quickstart.py, the library's usage example, runs as written."""
     import os
-    import re
 
-    text = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "README.md")).read()
-    blocks = re.findall(r"```python\n(.*?)```", text, re.S)
-    assert blocks, "README has a Python example"
-    scope = {}
-    exec(compile(blocks[0], "README.md example", "exec"), scope)
+    path = os.path.join(os.path.dirname(os.path.dirname(__file__)), "examples", "quickstart.py")
+    scope = {"__file__": path, "__name__": "quickstart"}
+    exec(compile(open(path).read(), path, "exec"), scope)
     y = scope["y"]
     assert y.shape == (8, 5120) and y.dtype == torch.bfloat16 and torch.isfinite(y.float()).all()

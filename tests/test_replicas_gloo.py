@@ -86,3 +86,10 @@ def test_bench_reference_arm_under_torchrun_two_ranks():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # the line reports what it timed: one sample round per step, on the same
+    # config (and exact byte count) as the GPU arm; the full-pass time is a
+    # separate, labelled extrapolation
+    assert line["config"]["bytes_per_pass"] == 16_335_300_100
+    assert line["ms_per_step"] * line["steps"] < 600_000
+    assert line["extrapolated_full_pass_ms"] > line["ms_per_step"]
+    assert line["cpu_baseline"]["single_thread"]["cores"] == 1

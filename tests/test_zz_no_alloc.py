@@ -2,12 +2,16 @@
 device memory (a host application that owns all device memory and lends out
 only the input and output buffers, code that must not call cudaMalloc
 because it can synchronise the device, code under a fixed memory budget).
-It runs the same GEMV on a fixed scratch array inside the library.
+It runs the same GEMV on a fixed scratch array inside the library, and
+vg_gemv_nvfp4_noalloc_check reports, again without allocating, whether a
+call's bounded device-side waits ran out.
 
 This file is collected last on purpose.  It calls the entry point through
-the C ABI twice in a row (the shared array keeps the first call's contents)
-and checks each result against the workspace entry point, vg_gemv_nvfp4,
-and against the CPU oracle, within the tolerance the other tests use.
+the C ABI several times in a row, changing the matrix shape (and so the
+number of thread blocks) between calls, since the shared array keeps each
+call's contents for the next; every result is checked against the
+workspace entry point, vg_gemv_nvfp4, and against the CPU oracle, within
+the tolerance the other tests use.
 """
 import ctypes
 
@@ -30,13 +34,17 @@ def test_noalloc_matches_workspace_entry_point(orc):
     from verify_gemm_gb300 import _lib
 
     lib = _lib.load()
-    M, K = 1040, 2560                    # several row blocks and K splits
     g = torch.Generator().manual_seed(123)
-    W = torch.randn((M, K), generator=g) * 0.02
-    wt = vg.nvfp4_pack(W.cuda())
-    nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+    mats = {}
+    for M, K in ((1040, 2560), (16, 4032)):   # 10 row blocks x 5 items; 1 x 8 (8 blocks)
+        W = torch.randn((M, K), generator=g) * 0.02
+        mats[(M, K)] = (vg.nvfp4_pack(W.cuda()), orc.nvfp4_quantise(W.numpy()))
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    for call, N in enumerate((8, 3)):    # two calls in a row
+    # two calls in a row, a call with another shape and grid, then the first
+    # shape again
+    calls = [((1040, 2560), 8), ((1040, 2560), 3), ((16, 4032), 5), ((1040, 2560), 8)]
+    for call, ((M, K), N) in enumerate(calls):
+        wt, (nib, sc, gs) = mats[(M, K)]
         x = (torch.randn((N, K), generator=g)).to(torch.bfloat16).cuda()
         y_ref = vg.gemv(wt, x)           # existing entry point, own workspace
         y = torch.full((N, M), 7.0, dtype=torch.bfloat16, device="cuda")
@@ -45,7 +53,9 @@ def test_noalloc_matches_workspace_entry_point(orc):
                                       ctypes.c_void_p(x.data_ptr()), N, M, K,
                                       ctypes.c_void_p(y.data_ptr()), stream)
         assert s == 0, (call, lib.vg_status_string(s))
-        torch.cuda.synchronize()
+        err = ctypes.c_int(-1)
+        assert lib.vg_gemv_nvfp4_noalloc_check(ctypes.byref(err), stream) == 0, call
+        assert err.value == 0, call
         yr, a = orc.gemv_nvfp4(nib, sc, gs, _bits(x), threads=8)
         bad_new, _ = orc.check(_bits(y), yr, a)
         bad_old, _ = orc.check(_bits(y_ref), yr, a)

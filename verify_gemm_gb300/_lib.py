@@ -53,6 +53,8 @@ SIGNATURES = {
     "vg_fp8_pack": (st, [P, i64, i64, P, P, P]),
     "vg_nvfp4_unpack": (st, [P, P, i64, i64, P, P, P]),
     "vg_fp8_unpack": (st, [P, i64, i64, P, P]),
+    "vg_fp8_rowscale_pack": (st, [P, i64, i64, P, P, P]),
+    "vg_fp8_rowscale_unpack": (st, [P, i64, i64, P, P]),
     "vg_nvfp4_from_canonical": (st, [P, P, i64, i64, P, P, P]),
     "vg_fp8_from_canonical": (st, [P, i64, i64, P, P]),
     "vg_gemv_workspace_size": (st, [i64, i64, i32, ctypes.POINTER(sz)]),
@@ -60,6 +62,7 @@ SIGNATURES = {
     "vg_gemv_fp8_rowscale": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_workspace_check": (st, [P, sz, ctypes.POINTER(i32), P]),
     "vg_gemv_nvfp4_noalloc": (st, [P, P, f32, P, i32, i64, i64, P, P]),
+    "vg_gemv_nvfp4_noalloc_check": (st, [ctypes.POINTER(i32), P]),
     "vg_hbm_read_probe": (st, [P, sz, i32, i32, i32, P, i32, P]),
     "vg_verify_plan_create": (st, [ctypes.POINTER(vg_matrix_desc), i32, i32, i32,
                                    ctypes.POINTER(P)]),

@@ -97,6 +97,8 @@ struct Params {
   uint32_t *epoch;          // pass counter: tags partial sums
   uint32_t *done;           // per-phase completed row blocks (ordered only)
   uint64_t *partials;       // [grid][kPartialWords]: tagged FP32 partial sums
+  int clear_slots;          // slots cleared when the pass counter wraps (>= grid): every
+                            // slot that any call sharing this workspace may have written
   uint32_t m8, m64;         // 8 and 64: shift multipliers kept in registers
   int x0_tensor;
   MatDev mat0;
@@ -917,7 +919,9 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
   // The last block out resets the per-phase completion counters and
   // advances the pass epoch, so that the next pass's partial sums carry new
   // tags.  Before the tags would overflow 32 bits the epoch restarts at 0
-  // and every slot is cleared (tag 0 never matches).
+  // and every slot that a call sharing this workspace may have written is
+  // cleared (tag 0 never matches): a slot written by an earlier call with a
+  // larger grid would otherwise carry a tag that becomes valid again.
   __syncthreads();
   if (tid == 0) sflag[2] = atom_add_relaxed(p.ctas_done, 1u) == uint32_t(p.grid - 1) ? 1 : 0;
   __syncthreads();
@@ -934,7 +938,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     __syncthreads();
     if (sflag[0]) {
       uint4 *dst = reinterpret_cast<uint4 *>(p.partials);
-      const int64_t n = int64_t(p.grid) * kPartialWords / 2;
+      const int64_t n = int64_t(p.clear_slots) * kPartialWords / 2;
       for (int64_t k = tid; k < n; k += kKernelThreads) dst[k] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -1098,6 +1102,10 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   set_head(p, ws);
   p.partials = reinterpret_cast<uint64_t *>(ws + kWsHead);
+  // every call on this device has at most di->sms blocks, so no slot past
+  // that count is ever written
+  p.clear_slots = int(i64min(int64_t(di->sms),
+                             int64_t((workspace_bytes - kWsHead) / (kPartialWords * sizeof(uint64_t)))));
   p.mat0 = m0;
   p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu) ? 1 : 0;
   // items of several chunks take x by tensor copy only
@@ -1299,6 +1307,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   set_head(p, plan->d_state);
   p.done = plan->ordered ? reinterpret_cast<uint32_t *>(plan->d_state + kWsHead) : nullptr;
   p.partials = reinterpret_cast<uint64_t *>(plan->d_state + kWsHead + done_bytes);
+  p.clear_slots = grid;   // the plan's state is its own
   *plan_out = plan;
   return VG_OK;
 }

@@ -1,5 +1,6 @@
 // vg_noalloc.cu -- vg_gemv_nvfp4_noalloc: the NVFP4 GEMV for callers that
-// cannot allocate device memory.
+// cannot allocate device memory, and vg_gemv_nvfp4_noalloc_check, which
+// reports whether its bounded device-side waits ran out.
 //
 // vg_gemv_nvfp4 needs a workspace (a few header words and FP32 partial
 // sums for row blocks whose K range is split between thread blocks), and
@@ -9,13 +10,13 @@
 // adapter), code that must not call cudaMalloc because it can synchronise
 // the whole device and stall other work, and code that runs under a memory
 // budget that a hidden allocation would break.  For them this file keeps
-// one fixed scratch array in device memory, created when the library is
-// loaded and held by every GPU that loads it until the process exits, and
-// runs the unchanged GEMV with that array as its workspace.
+// one fixed scratch array in device memory and runs the unchanged GEMV with
+// that array as its workspace.  The array is created on each device when
+// the library's module is first used there (CUDA loads modules lazily) and
+// is held until the process exits.
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "vg_internal.h"
 
@@ -28,25 +29,19 @@ constexpr size_t kScratchBytes = VG_NOALLOC_SCRATCH_BYTES;
 
 // The workspace lives here.  In host code this name is only a stand-in for
 // the device array, never a usable address: the device address is looked
-// up per device with cudaGetSymbolAddress.
+// up with cudaGetSymbolAddress.
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[64] = {};
-
-// Device address of g_scratch on the current device, looked up once per
-// device (on the first call made with that device current).
+// Device address of g_scratch on the current device.  It is looked up on
+// every call rather than cached: after a device reset, or once the primary
+// context has been torn down and created again, the module is loaded anew
+// and the array may sit elsewhere.  The first lookup on a device is what
+// loads the module there, which is why the first call on a device must come
+// before any stream capture; later lookups only read the module's table.
 vg_status scratch_address(void **out) {
-  int dev = 0;
-  VG_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= 64) return VG_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    VG_CUDA(cudaGetSymbolAddress(&p, g_scratch));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void *p = nullptr;
+  VG_CUDA(cudaGetSymbolAddress(&p, g_scratch));
+  *out = p;
   return VG_OK;
 }
 
@@ -64,9 +59,19 @@ extern "C" vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, fl
   if (vg_status s = scratch_address(&scratch)) return s;
   // The array starts zeroed and every call leaves it consistent for the
   // next one (finished-block count back at zero, pass epoch advanced), except
-  // for the error word: a failed call leaves it set, and a set error word
-  // makes the kernel's waits give up early.  No caller of this entry point
-  // can read it, so clear it (4 bytes) before each call.
+  // for the error word: a call whose wait ran out leaves it set (read it with
+  // vg_gemv_nvfp4_noalloc_check), and a set error word makes the kernel's
+  // waits give up early.  So each call starts by clearing it (4 bytes).
   VG_CUDA(cudaMemsetAsync(scratch, 0, sizeof(int), vg::as_cuda(stream)));
   return vg_gemv_nvfp4(w, scales, gscale, x, N, M, K, y, scratch, kScratchBytes, stream);
+}
+
+extern "C" vg_status vg_gemv_nvfp4_noalloc_check(int *device_error, vg_stream_t stream) {
+  if (!device_error) return VG_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  if (vg_status s = scratch_address(&scratch)) return s;
+  // vg_gemv_workspace_check reads the word into host memory (a plain
+  // stack variable: no pinned staging buffer is allocated) and, if it is
+  // set, zero-fills the whole array with cudaMemsetAsync.
+  return vg_gemv_workspace_check(scratch, kScratchBytes, device_error, stream);
 }

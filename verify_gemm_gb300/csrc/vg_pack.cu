@@ -471,3 +471,16 @@ extern "C" vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t 
   VG_LAUNCH_CHECK();
   return VG_OK;
 }
+
+// The row-scaled FP8 quantiser and its unpack under the names the boundary
+// lists for them (the format is FP8-E4M3 with one FP32 scale per row);
+// vg_fp8_pack / vg_fp8_unpack are the same functions.
+extern "C" vg_status vg_fp8_rowscale_pack(const float *W, int64_t M, int64_t K, void *w_out,
+                                          float *rowscale_out, vg_stream_t stream) {
+  return vg_fp8_pack(W, M, K, w_out, rowscale_out, stream);
+}
+
+extern "C" vg_status vg_fp8_rowscale_unpack(const void *w, int64_t M, int64_t K, uint8_t *q_out,
+                                            vg_stream_t stream) {
+  return vg_fp8_unpack(w, M, K, q_out, stream);
+}
