@@ -351,23 +351,44 @@ def run_ours(args, world, rank, local):
     u_ms, _ = timed(unordered.run, max(3, args.steps // 2), 2)
     unordered.close()
     extra["unordered_gbs"] = nbytes * max(3, args.steps // 2) / (u_ms / 1e3) / 1e9
+    # the other widths through the same plan: each pass reads its width from
+    # a device word (no new plan, no host-side width)
     widths = {}
+    width = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan.set_width(width)
     for w in [int(v) for v in args.widths.split(",") if v]:
         if w == args.N:
             continue
-        xs = [torch.randn((w, m.K), device=dev).to(torch.bfloat16) for m in st.mats]
-        ys = [torch.empty((w, m.M), dtype=torch.bfloat16, device=dev) for m in st.mats]
-        pw = vg.VerifyPlan([(wt, x, y, m.group) for m, wt, x, y in
-                            zip(st.mats, st.weights, xs, ys)], w, ordered=True)
-        ms, _ = timed(pw.run, max(3, args.steps // 2), 2)
-        if pw.check() != 0:
+        width.fill_(w)
+        ms, _ = timed(plan.run, max(3, args.steps // 2), 2)
+        if plan.check() != 0:
             raise RuntimeError("verify pass reported a device error")
-        pw.close()
         us = ms / max(3, args.steps // 2) * 1e3
         widths[str(w)] = {"us_per_pass": round(us, 1), "GBps": round(nbytes / us / 1e3, 1)}
-        del xs, ys
+    plan.set_width(None)
     widths[str(args.N)] = {"us_per_pass": round(total_ms / args.steps * 1e3, 1),
                            "GBps": round(nbytes / (total_ms / args.steps) / 1e6, 1)}
+
+    # one draft step (row-scaled FP8 layer + NVFP4 head) at N = 1
+    draft = None
+    if not args.no_configs:
+        from verify_gemm_gb300.inputs import DRAFT_SEED, draft_mats
+
+        ds = build_stack(1, device=dev, mats=draft_mats(), seed=DRAFT_SEED)
+        dplan = ds.plan(ordered=True)
+        ms, per_d = timed(dplan.run, args.steps, args.warmup)
+        if dplan.check() != 0:
+            raise RuntimeError("draft step reported a device error")
+        dplan.close()
+        med = statistics.median(per_d)
+        draft = {"workload": "draft step: row-scaled FP8 q,k,v,o 5120x5120, gate+up "
+                             "2x17408x5120, down 5120x17408 + NVFP4 head 151936x5120, N=1, "
+                             "ordered; seed 5",
+                 "bytes": ds.bytes, "us_per_step": round(1e3 * med, 1),
+                 "us_p10_p90": [round(1e3 * q, 1) for q in pcts(per_d, (10, 90))],
+                 "GBps": round(ds.bytes / (med / 1e3) / 1e9, 1)}
+        del ds
+        torch.cuda.empty_cache()
 
     e2e = None
     if not args.no_e2e:
@@ -456,7 +477,7 @@ def run_ours(args, world, rank, local):
                                      == ("nvfp4", 8, 64) else None),
                          "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
             "per_width": widths, **extra,
-            "per_config": configs, "sustained": sustained,
+            "per_config": configs, "draft_step": draft, "sustained": sustained,
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
         }
         if cb is not None:

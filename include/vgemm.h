@@ -317,6 +317,21 @@ vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,
  * on the GPU. */
 vg_status vg_verify_pass(vg_verify_plan *plan, vg_stream_t stream);
 
+/* Width dispatch on the device (engine card, Design table, Decode row: the
+ * verify pass runs for however many drafts the round made, 2-8 columns, with
+ * no host wait mid-round).  After this call every pass of `plan` reads its
+ * width from the device word *d_width when the pass starts, instead of
+ * using the N the plan was created with: the pass computes and writes y
+ * columns 0..width-1 only (the other columns of each y are left untouched,
+ * and rows >= width of each x are never used), so one plan, or one CUDA
+ * graph holding its pass, serves every width 1..N and a kernel earlier on
+ * the stream can choose it.  A width outside 1..N makes the pass do nothing
+ * and set the device error word to 5 (read by vg_verify_plan_check).
+ *   d_width  device int32 (4-byte aligned), or NULL to return to the fixed N.
+ * The pointer is captured by the launch (and by graph capture), the value
+ * is read by each pass. */
+vg_status vg_verify_plan_set_width(vg_verify_plan *plan, const int32_t *d_width);
+
 /* Synchronises the stream, reads the plan's device error word and, if it is
  * set, clears it and resets the plan's counters.  *device_error: 0 or a
  * nonzero code (a bounded wait ran out).  Returns VG_ERR_TIMEOUT if set. */

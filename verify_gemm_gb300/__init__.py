@@ -223,6 +223,18 @@ class VerifyPlan:
     def run(self, stream=None):
         _lib.check(_lib.vg_verify_pass(self._h, _stream(stream)), "vg_verify_pass")
 
+    def set_width(self, width: torch.Tensor | None):
+        """Read each pass's width from a device int32 tensor (one element)
+        instead of the fixed N; None returns to the fixed N."""
+        if width is not None:
+            if not (width.is_cuda and width.dtype == torch.int32 and width.numel() == 1):
+                raise ValueError("width: expected a one-element CUDA int32 tensor")
+            self._width = width                      # keep it alive
+        else:
+            self._width = None
+        _lib.check(_lib.vg_verify_plan_set_width(self._h, _ptr(width) if width is not None
+                                                 else None), "vg_verify_plan_set_width")
+
     def check(self, stream=None) -> int:
         err = ctypes.c_int()
         s = _lib.vg_verify_plan_check(self._h, _stream(stream), ctypes.byref(err))

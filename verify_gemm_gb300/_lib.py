@@ -69,6 +69,7 @@ SIGNATURES = {
     "vg_verify_plan_create_ex": (st, [ctypes.POINTER(vg_matrix_desc), i32, i32,
                                       ctypes.POINTER(vg_plan_options), ctypes.POINTER(P)]),
     "vg_verify_pass": (st, [P, P]),
+    "vg_verify_plan_set_width": (st, [P, P]),
     "vg_verify_plan_check": (st, [P, P, ctypes.POINTER(i32)]),
     "vg_verify_plan_bytes": (st, [P, ctypes.POINTER(i64)]),
     "vg_verify_plan_grid": (st, [P, ctypes.POINTER(i32)]),

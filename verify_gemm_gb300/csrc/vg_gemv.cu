@@ -87,7 +87,8 @@ struct Params {
   const MatDev *mats;       // nullptr: use mat0 / phase0
   const PhaseDev *phases;
   int nphases;
-  int N;
+  int N;                    // columns of x and y (the most a width word may ask for)
+  const int *width;         // device word read at launch: the pass's width 1..N (or nullptr)
   int ordered;
   int hold_phase;
   int grid;
@@ -135,6 +136,7 @@ constexpr int kProducers = 2;
 static_assert(kSlots % kProducers == 0, "every producer owns its own ring slots");
 constexpr int kKernelThreads = kConsumers + 32 * kProducers;
 constexpr int kErrFullWait = 1, kErrEmptyWait = 2, kErrDepWait = 3, kErrPartialWait = 4;
+constexpr int kErrWidth = 5;   // the width word held a value outside 1..N
 // Header words of a workspace (GEMV) or plan state: error, finished blocks,
 // pass epoch; then, 256 bytes in, the per-phase counters (plans) and the
 // partial-sum slots.
@@ -427,7 +429,7 @@ constexpr int kBoundaryPf = VG_BPF;
 #endif
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0,
-                         const volatile int *dep_waiting, int which, int np) {
+                         const volatile int *dep_waiting, int which, int np, int N) {
   const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
   Seq q;
   q.init(mats, phases, p);
@@ -472,7 +474,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     // x: one tensor copy of 8 rows x the item's units (rows >= N and units
     // past K read as zeros), else one bulk copy per row (one-chunk items)
     const uint32_t x_bytes = tmap ? uint32_t(8 * iu * kUnitK * 2)
-                                  : uint32_t(min(iu * kUnitK, K - k0) * 2 * p.N);
+                                  : uint32_t(min(iu * kUnitK, K - k0) * 2 * N);
     const uint8_t *code_src = w + int64_t(q.rb) * rb_bytes + int64_t(q.c) * tiles * tile_item_bytes;
     const uint8_t *scale_src =
         sc ? sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * kNvScaleChunkBytes : nullptr;
@@ -515,8 +517,8 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     if (tmap) {
       bulk_tensor_3d(slot + kItemXOff, tmap, 0, 0, q.c * iu, full, pol_x);
     } else {
-      const uint32_t row_bytes = x_bytes / uint32_t(p.N);
-      for (int n = 0; n < p.N; ++n)
+      const uint32_t row_bytes = x_bytes / uint32_t(N);
+      for (int n = 0; n < N; ++n)
         bulk_g2s(slot + kItemXOff + n * kXRowBytes, xg + int64_t(n) * K + k0, row_bytes, full,
                  pol_x);
     }
@@ -613,7 +615,8 @@ __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_
 __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, int T, int G,
                                           int piece_start, bool full_piece, int rb, int ph,
                                           uint32_t tag, bool aborted, int tl, int cc,
-                                          uint32_t red, float a0, float a1, float a2, float a3) {
+                                          uint32_t red, int N, float a0, float a1, float a2,
+                                          float a3) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int mt = rb * m.rt + tl;
@@ -661,7 +664,7 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int nn = 2 * t + e;
-        if (nn < p.N) {
+        if (nn < N) {
           const __nv_bfloat16 v = __float2bfloat16_rn(accs[2 * h + e] * mult);
           m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
         }
@@ -698,21 +701,33 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     sflag[1] = int(ld_relaxed(p.epoch));
     sflag[2] = 0;
     sflag[3] = 0;   // consumers waiting on a group dependency
+    // the pass's width: fixed, or read from the width word at launch
+    int n = p.N;
+    if (p.width) {
+      n = ld_relaxed(reinterpret_cast<const uint32_t *>(p.width));
+      if (n < 1 || n > p.N) {
+        if (blockIdx.x == 0) set_error(p.error, kErrWidth);
+        n = 0;   // no work: every block goes straight to the end of the pass
+      }
+    }
+    sflag[4] = n;
   }
   __syncthreads();
   const uint32_t epoch = uint32_t(sflag[1]);
+  const int N = sflag[4];
 
-  if (warp >= kWarps) {
+  if (N == 0) {
+    // invalid width: nothing is read or written
+  } else if (warp >= kWarps) {
     // ================================================================ producer
     const int np = p.mats ? kProducers : 1;
     if (lane == 0 && warp - kWarps < np)
       producer(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots),
-               sflag + 3, warp - kWarps, np);
+               sflag + 3, warp - kWarps, np, N);
 
   } else {
     // =============================================================== consumers
     const int g = lane >> 2, t = lane & 3;
-    const int N = p.N;
     const bool on = g < N;
     const uint32_t ring = smem_addr(smem);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kSlots);
@@ -909,8 +924,8 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
       }
       if (!finish_piece(p, mats[cons.mi], cons.items, cons.G, piece_start,
-                        c0 == 0 && len == cons.KI, rb, ph, tag, aborted, tl, cc, red, accs[0],
-                        accs[1], accs[2], accs[3]))
+                        c0 == 0 && len == cons.KI, rb, ph, tag, aborted, tl, cc, red, N,
+                        accs[0], accs[1], accs[2], accs[3]))
         aborted = true;
       cons.skip(len, mats, phases, p);
     }
@@ -1327,6 +1342,13 @@ extern "C" vg_status vg_verify_pass(vg_verify_plan *plan, vg_stream_t stream) {
   VG_CUDA(cudaGetDevice(&dev));
   if (dev != plan->dev) return VG_ERR_INVALID_ARG;
   return launch(plan->params, stream);
+}
+
+extern "C" vg_status vg_verify_plan_set_width(vg_verify_plan *plan, const int32_t *d_width) {
+  if (!plan) return VG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(d_width) & 3u) != 0) return VG_ERR_ALIGNMENT;
+  plan->params.width = reinterpret_cast<const int *>(d_width);
+  return VG_OK;
 }
 
 extern "C" vg_status vg_verify_plan_check(vg_verify_plan *plan, vg_stream_t stream,

@@ -17,6 +17,8 @@ Recipe:
   * The 64-layer stack is too large to hold in FP32 at once: each matrix is
     drawn from its own generator seeded with seed*1000003 + layer*16 + idx,
     and each matrix gets its own x from seed*1000003 + layer*16 + 8 + idx.
+  * The draft step (one row-scaled FP8 layer + the NVFP4 head, N = 1) is
+    drawn the same way from seed 5, a seed of its own.
 """
 from __future__ import annotations
 
@@ -72,6 +74,25 @@ def stack_mats(layers: int = LAYERS, attn_fmt: str = "nvfp4", down_fmt: str = "f
         mats.append(Mat(f"L{layer}.down", down_fmt, HIDDEN, INTERMEDIATE, g, layer, 6))
         g += 1
     mats.append(Mat("head", "nvfp4", VOCAB, HIDDEN, g, layers, 0))
+    return mats
+
+
+DRAFT_SEED = 5
+
+
+def draft_mats(hidden: int = HIDDEN, inter: int = INTERMEDIATE, vocab: int = VOCAB):
+    """Matrices of one draft step (engine card, Model section: the drafting
+    layer re-encoded as row-scaled FP8, the output head as NVFP4; Measured
+    section: each draft step adds about 0.8 ms).  One layer's q, k, v, o,
+    gate, up and down, all row-scaled FP8, then the NVFP4 head; the same
+    groups as a stack layer.  Drawn like the stack (derived seeds, layer 0
+    and 1 for the head) from DRAFT_SEED."""
+    mats = [Mat(f"D.{nm}", "fp8", hidden, hidden, 0, 0, i) for i, nm in enumerate("qkv")]
+    mats.append(Mat("D.o", "fp8", hidden, hidden, 1, 0, 3))
+    mats.append(Mat("D.gate", "fp8", inter, hidden, 2, 0, 4))
+    mats.append(Mat("D.up", "fp8", inter, hidden, 2, 0, 5))
+    mats.append(Mat("D.down", "fp8", hidden, inter, 3, 0, 6))
+    mats.append(Mat("head", "nvfp4", vocab, hidden, 4, 1, 0))
     return mats
 
 
