@@ -70,6 +70,10 @@ def _declare(lib):
                                   P, i64, P, P, ctypes.c_int]),
         "vgo_gemv_fp8": (None, [P, P, P, ctypes.c_int, i64, i64, P, i64, P, P,
                                 ctypes.c_int]),
+        "vgo_bf16_round": (ctypes.c_uint16, [ctypes.c_double]),
+        "vgo_silu": (ctypes.c_double, [ctypes.c_double]),
+        "vgo_swiglu": (None, [P, P, P, P, i64, P, P]),
+        "vgo_rmsnorm": (None, [P, P, ctypes.c_int, i64, ctypes.c_double, P]),
         "vgo_check": (ctypes.c_int64, [P, P, P, i64, ctypes.c_double, ctypes.c_double,
                                        ctypes.POINTER(ctypes.c_double)]),
     }
@@ -214,6 +218,31 @@ class Oracle:
                               None if r is None else _ptr(r), nr, _ptr(y), _ptr(a),
                               int(threads))
         return y, a
+
+    # ----------------------------------------------------- fused neighbours
+    def bf16_round(self, v):
+        return self.lib.vgo_bf16_round(float(v))
+
+    def silu(self, g):
+        return self.lib.vgo_silu(float(g))
+
+    def swiglu(self, g, u, ag, au):
+        """h = SiLU(g) * u and its acceptance bound (FP64, same shapes)."""
+        g, u, ag, au = (np.ascontiguousarray(v, dtype=np.float64) for v in (g, u, ag, au))
+        h = np.empty_like(g)
+        b = np.empty_like(g)
+        self.lib.vgo_swiglu(_ptr(g), _ptr(u), _ptr(ag), _ptr(au), g.size, _ptr(h), _ptr(b))
+        return h, b
+
+    def rmsnorm(self, x_bits, gamma_bits, eps=1e-6):
+        """BF16 bits of RMSNorm(x) * gamma, x [N, K], gamma [K] as BF16 bits."""
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        gamma_bits = np.ascontiguousarray(gamma_bits, dtype=np.uint16)
+        N, K = x_bits.shape
+        assert gamma_bits.shape == (K,)
+        out = np.empty_like(x_bits)
+        self.lib.vgo_rmsnorm(_ptr(x_bits), _ptr(gamma_bits), N, K, float(eps), _ptr(out))
+        return out
 
     def check(self, y_bits, yref, a, rel=REL_TOL, abs_tol=ABS_TOL):
         """(number of elements out of tolerance, worst error / tolerance)."""

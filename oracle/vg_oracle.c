@@ -356,3 +356,63 @@ int64_t vgo_check(const uint16_t *y, const double *yref, const double *a,
         *worst = w;
     return bad;
 }
+
+/* ------------------------------------------------------ fused neighbours */
+
+uint16_t vgo_bf16_round(double v)
+{
+    int ex;
+    double a = fabs(v), q, r;
+    uint32_t u;
+    float f;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    if (isnan(v))
+        return 0x7FC0;
+    if (a == 0.0)
+        return sign;
+    frexp(a, &ex);                                /* a in [2^(ex-1), 2^ex) */
+    if (ex - 1 < -126)
+        ex = -125;                                /* subnormal spacing 2^-133 */
+    q = ldexp(1.0, ex - 1 - 7);                   /* 7 fraction bits */
+    r = nearbyint(a / q) * q;                     /* ties to the even multiple */
+    if (r > 3.3895313892515355e38)                /* past the largest finite BF16 */
+        return sign | 0x7F80;
+    f = (float)r;                                 /* exact: r has <= 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+double vgo_silu(double g)
+{
+    return g / (1.0 + exp(-g));
+}
+
+void vgo_swiglu(const double *g, const double *u, const double *ag, const double *au,
+                int64_t n, double *h, double *bound)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i) {
+        double s = vgo_silu(g[i]);
+        double eg = 4e-3 * ag[i] + 1e-6, eu = 4e-3 * au[i] + 1e-6;
+        h[i] = s * u[i];
+        bound[i] = 1.1 * eg * (fabs(u[i]) + eu) + fabs(s) * eu + ldexp(fabs(h[i]), -8) + 1e-6;
+    }
+}
+
+void vgo_rmsnorm(const uint16_t *x, const uint16_t *gamma, int N, int64_t K, double eps,
+                 uint16_t *out)
+{
+    int n;
+    int64_t k;
+    for (n = 0; n < N; ++n) {
+        double ss = 0.0, inv;
+        for (k = 0; k < K; ++k) {
+            double v = vgo_bf16_value(x[n * K + k]);
+            ss += v * v;
+        }
+        inv = 1.0 / sqrt(ss / (double)K + eps);
+        for (k = 0; k < K; ++k)
+            out[n * K + k] = vgo_bf16_round(vgo_bf16_value(x[n * K + k]) * inv
+                                            * vgo_bf16_value(gamma[k]));
+    }
+}

@@ -86,6 +86,39 @@ void vgo_gemv_fp8(const uint8_t *q, const float *rs,
                   const int64_t *rows, int64_t nrows,
                   double *y, double *a, int threads);
 
+/* ------------------------------------------------- fused neighbours
+ * Operations that sit next to the GEMV in a layer and that the verify pass
+ * can run in the same launch (engine card, Checks section: the operator
+ * checks cover row reductions next to the GEMVs; the card's Model section
+ * names the MLPs, whose gate and up projections feed a gated activation).
+ * The pages give no formulas; these are the plain definitions of the
+ * SiLU-gated MLP activation and of RMS normalisation used by the model
+ * family the card runs. */
+
+/* BF16 bit pattern nearest to v: round to nearest, ties to the even
+ * significand, with BF16's subnormals (spacing 2^-133); one rounding from
+ * the FP64 value.  |v| past the largest finite BF16 gives +-inf. */
+uint16_t vgo_bf16_round(double v);
+
+/* SiLU(g) = g * sigmoid(g) = g / (1 + exp(-g)), FP64. */
+double vgo_silu(double g);
+
+/* Gated activation of n gate/up pairs: h[i] = SiLU(g[i]) * u[i] (FP64),
+ * and the acceptance bound of a BF16 h computed from a gate and an up
+ * product that each carry the GEMV tolerance: with eg = 4e-3*ag + 1e-6 and
+ * eu = 4e-3*au + 1e-6 (ag, au = sum|w x| of the two products),
+ *   bound = 1.1*eg*(|u| + eu) + |SiLU(g)|*eu + 2^-8*|h| + 1e-6,
+ * where 1.1 bounds |SiLU'| everywhere and 2^-8*|h| covers the BF16
+ * rounding of h. */
+void vgo_swiglu(const double *g, const double *u, const double *ag, const double *au,
+                int64_t n, double *h, double *bound);
+
+/* RMS normalisation of N rows of K BF16 values with BF16 weights gamma[K]:
+ *   out[n][k] = bf16( x[n][k] * gamma[k] / sqrt(sum_k x[n][k]^2 / K + eps) )
+ * evaluated in FP64 with one rounding to BF16 at the end. */
+void vgo_rmsnorm(const uint16_t *x, const uint16_t *gamma, int N, int64_t K, double eps,
+                 uint16_t *out);
+
 /* Count elements with |y - yref| > rel*a + abs; *worst gets the largest
  * |y - yref| / (rel*a + abs).  y is BF16 bits. */
 int64_t vgo_check(const uint16_t *y, const double *yref, const double *a,

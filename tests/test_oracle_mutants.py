@@ -35,6 +35,13 @@ MUTANTS = {
     "block scale divisor": ("float s = t / 6.0f;", "float s = t / 4.0f;"),
     "fp8 row scale divisor": ("rs = ramax / 448.0f;", "rs = ramax / 447.0f;"),
     "fp8 scale dropped in gemv": ("* (double)j->rs[m];", ";"),
+    "silu sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    "swiglu gate and up swapped": ("h[i] = s * u[i];", "h[i] = vgo_silu(u[i]) * g[i];"),
+    "rmsnorm mean as sum": ("ss / (double)K + eps", "ss + eps"),
+    "rmsnorm weight dropped": ("* inv\n                                            * vgo_bf16_value(gamma[k]));",
+                               "* inv);"),
+    "bf16 round ties away": ("r = nearbyint(a / q) * q;", "r = floor(a / q + 0.5) * q;"),
+    "bf16 subnormal spacing": ("ex = -125;", "ex = -124;"),
     "e4m3 saturation": ("if (a >= 448.0)\n        return sign | 0x7E;",
                         "if (a >= 480.0)\n        return sign | 0x7F;"),
 }

@@ -439,3 +439,102 @@ def test_quantise_rows_with_given_gs_matches_whole_matrix(orc):
     rows = [0, 17, 39]
     nr, sr = orc.nvfp4_quantise_gs(W[rows], gs)
     assert np.array_equal(nr, nib[rows]) and np.array_equal(sr, sc[rows])
+
+
+# ------------------------------------------------------- fused neighbours
+
+def test_bf16_round_matches_torch_on_fp32_values(orc):
+    """For FP32 inputs one FP64 rounding equals torch's FP32 -> BF16 cast
+    (round to nearest even), across normal, subnormal and huge values."""
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([rng.standard_normal(4000).astype(np.float32),
+                           (rng.standard_normal(2000) * 1e-39).astype(np.float32),
+                           (rng.standard_normal(2000) * 1e37).astype(np.float32),
+                           np.float32([0.0, -0.0, 1.0, -2.5, 3e38, -3.3e38])])
+    want = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.bf16_round(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_round_midpoints_and_edges(orc):
+    """Midpoints between neighbouring BF16 values go to the even
+    significand; a hair above or below goes to the nearer one; the
+    subnormal spacing is 2^-133; past the largest finite value is inf."""
+    rng = np.random.default_rng(12)
+    for b in rng.integers(0x0001, 0x7F7E, 500):
+        lo, hi = orc.bf16_value(int(b)), orc.bf16_value(int(b) + 1)
+        mid = (lo + hi) / 2                       # exact in FP64
+        even = int(b) if int(b) % 2 == 0 else int(b) + 1
+        assert orc.bf16_round(mid) == even
+        assert orc.bf16_round(-mid) == even | 0x8000
+        assert orc.bf16_round(np.nextafter(mid, 0)) == int(b)
+        assert orc.bf16_round(np.nextafter(mid, np.inf)) == int(b) + 1
+    assert orc.bf16_round(2.0 ** -133) == 0x0001
+    assert orc.bf16_round(2.0 ** -134) == 0x0000        # tie with 0: even
+    assert orc.bf16_round(3 * 2.0 ** -134) == 0x0002    # tie between 1 and 2: even
+    assert orc.bf16_round(orc.bf16_value(0x7F7F)) == 0x7F7F
+    assert orc.bf16_round(2.0 ** 128) == 0x7F80
+    assert orc.bf16_round(-0.0) == 0x8000
+
+
+def test_silu_against_library_sigmoid(orc):
+    """SiLU(g) = g * sigmoid(g), with scipy's expit as the sigmoid, and the
+    identity SiLU(g) - SiLU(-g) = g."""
+    from scipy.special import expit
+
+    for g in np.linspace(-30, 30, 241):
+        want = g * expit(g)
+        assert abs(orc.silu(g) - want) <= 1e-15 * max(1.0, abs(want))
+        assert abs(orc.silu(g) - orc.silu(-g) - g) <= 1e-14 * max(1.0, abs(g))
+    assert orc.silu(0.0) == 0.0
+
+
+def test_swiglu_values_and_bound(orc):
+    """h = SiLU(gate) * up (the gate goes through SiLU, not the up), and
+    the bound grows with both products' scales and with |h|."""
+    from scipy.special import expit
+
+    g = np.array([2.0, 3.0, -1.5, 0.0, 10.0])
+    u = np.array([3.0, 2.0, 4.0, 7.0, -0.5])
+    zero = np.zeros_like(g)
+    h, b = orc.swiglu(g, u, zero, zero)
+    assert np.allclose(h, g * expit(g) * u, rtol=1e-15, atol=0)
+    assert h[0] != h[1]                                  # not symmetric in gate/up
+    assert np.allclose(b, np.abs(h) / 256 + 1.1e-6 * (np.abs(u) + 1e-6)
+                       + np.abs(g * expit(g)) * 1e-6 + 1e-6, rtol=1e-12)
+    _, b2 = orc.swiglu(g, u, zero + 1.0, zero)
+    _, b3 = orc.swiglu(g, u, zero, zero + 1.0)
+    assert np.all(b2 > b) and np.all(b3 >= b)
+
+
+def test_rmsnorm_against_library(orc):
+    """RMS normalisation against torch's rms_norm in FP64, rounded once to
+    BF16 (the rounding pinned above), at K of a layer and with outliers."""
+    rng = np.random.default_rng(13)
+    for N, K, scale in ((1, 5120, 1.0), (8, 512, 30.0), (3, 17408, 1e-3)):
+        x = torch.from_numpy(rng.standard_normal((N, K)) * scale).to(torch.bfloat16)
+        x[:, rng.integers(0, K, 4)] *= 20
+        gamma = torch.from_numpy(1 + 0.1 * rng.standard_normal(K)).to(torch.bfloat16)
+        ref = torch.nn.functional.rms_norm(x.double(), (K,), gamma.double(), eps=1e-6)
+        want = np.array([[orc.bf16_round(v) for v in row] for row in ref.numpy()],
+                        dtype=np.uint16)
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        gb = gamma.view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(orc.rmsnorm(xb, gb, 1e-6), want)
+
+
+def test_rmsnorm_closed_forms(orc):
+    """A constant row c gives gamma * c / sqrt(c^2 + eps); with eps = 0 a
+    power-of-two scale of x leaves the output unchanged."""
+    K = 256
+    gamma = torch.linspace(0.5, 2.0, K).to(torch.bfloat16)
+    gb = gamma.view(torch.int16).numpy().view(np.uint16)
+    x = torch.full((1, K), 3.0).to(torch.bfloat16)
+    out = orc.rmsnorm(x.view(torch.int16).numpy().view(np.uint16), gb, 1e-6)
+    want = [orc.bf16_round(orc.bf16_value(int(gv)) * 3.0 / np.sqrt(9.0 + 1e-6)) for gv in gb]
+    assert np.array_equal(out[0], np.array(want, dtype=np.uint16))
+    rng = np.random.default_rng(14)
+    x = torch.from_numpy(rng.standard_normal((2, K))).to(torch.bfloat16)
+    a = orc.rmsnorm(x.view(torch.int16).numpy().view(np.uint16), gb, 0.0)
+    b = orc.rmsnorm((x * 8).view(torch.int16).numpy().view(np.uint16), gb, 0.0)
+    assert np.array_equal(a, b)
