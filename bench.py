@@ -390,6 +390,31 @@ def run_ours(args, world, rank, local):
         del ds
         torch.cuda.empty_cache()
 
+    # the same stack with its neighbours fused in and real dependencies:
+    # RMS norm -> q,k,v (x = the norm's y); o; RMS norm -> gate+up with the
+    # gated activation -> down (x = the activation's y); final norm -> head
+    fused = None
+    if not args.no_configs and args.layers == 64:
+        from verify_gemm_gb300.workloads import build_fused_stack
+
+        fs = build_fused_stack(args.N, device=dev, attn_fmt=args.attn_fmt)
+        fplan = fs.plan()
+        ms, per_f = timed(fplan.run, args.steps, args.warmup)
+        if fplan.check() != 0:
+            raise RuntimeError("fused stack reported a device error")
+        fplan.close()
+        med = statistics.median(per_f)
+        fused = {"workload": "the verify stack with RMS norms before q,k,v and before the MLP, "
+                             "the gated activation fused into gate+up and written as down's x, "
+                             "a final norm before the head; every dependent x copied only after "
+                             "its producer group completes",
+                 "N": args.N, "bytes": fs.bytes, "phases": len({e.group for e in fs.entries}),
+                 "us_per_pass": round(1e3 * med, 1),
+                 "us_p10_p90": [round(1e3 * q, 1) for q in pcts(per_f, (10, 90))],
+                 "GBps": round(fs.bytes / (med / 1e3) / 1e9, 1)}
+        del fs
+        torch.cuda.empty_cache()
+
     e2e = None
     if not args.no_e2e:
         x_host = torch.empty(st.x_all.shape, dtype=st.x_all.dtype, pin_memory=True)
@@ -477,7 +502,8 @@ def run_ours(args, world, rank, local):
                                      == ("nvfp4", 8, 64) else None),
                          "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
             "per_width": widths, **extra,
-            "per_config": configs, "draft_step": draft, "sustained": sustained,
+            "per_config": configs, "draft_step": draft, "fused_stack": fused,
+            "sustained": sustained,
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
         }
         if cb is not None:

@@ -166,6 +166,26 @@ vg_status vg_nvfp4_from_canonical(const uint8_t *nib, const uint8_t *sc,
 vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t K, void *w_out,
                                 vg_stream_t stream);
 
+/* Gated pair packers for VG_OP_SWIGLU: the gate and up projections of an
+ * MLP (each [I][K], I % 8 == 0) packed as one matrix of M = 2*I rows whose
+ * every 16-row tile holds 8 gate rows and the same 8 up rows (tile j: gate
+ * rows 8j..8j+7, then up rows 8j..8j+7), so that the lane that finishes a
+ * gate output also holds the matching up output.  Each half is quantised
+ * exactly as vg_nvfp4_pack / vg_fp8_pack would quantise it alone (its own
+ * tensor scale or row scales).  Buffers: vg_nvfp4_sizes / vg_fp8_sizes of
+ * (2*I, K).  vg_nvfp4_unpack / vg_fp8_unpack of (2*I, K) give the canonical
+ * interleaved rows.
+ *   Wgate, Wup   device FP32 [I][K].
+ *   gscales_out  host float[2]: gate, up tensor scales.
+ *   rs_gate_out, rs_up_out  device FP32 [I].
+ * Synchronise once; NaN/Inf gives VG_ERR_INVALID_ARG. */
+vg_status vg_nvfp4_pack_gated(const float *Wgate, const float *Wup, int64_t I, int64_t K,
+                              void *w_out, void *scales_out, float *gscales_out,
+                              vg_stream_t stream);
+vg_status vg_fp8_pack_gated(const float *Wgate, const float *Wup, int64_t I, int64_t K,
+                            void *w_out, float *rs_gate_out, float *rs_up_out,
+                            vg_stream_t stream);
+
 /* ------------------------------------------------------------ the GEMV */
 
 /* Workspace bytes that vg_gemv_nvfp4 / vg_gemv_fp8_rowscale need for an
@@ -270,18 +290,53 @@ vg_status vg_hbm_read_probe(const void *buf, size_t bytes, int mode, int chunk, 
 
 /* -------------------------------------------------- fused verify pass */
 
-/* One matrix of a verify pass (a layer stack).  Matrices must be listed
- * with non-decreasing group; group g+1 depends on group g. */
+/* Operations of a verify pass entry (vg_matrix_desc.op). */
+enum {
+    VG_OP_GEMV = 0,      /* y = x . dequant(W)^T */
+    VG_OP_SWIGLU = 1,    /* gated MLP pair: y = SiLU(x . Wgate^T) * (x . Wup^T) */
+    VG_OP_RMSNORM = 2    /* y = x * gamma / sqrt(mean(x^2) + eps), no weights */
+};
+
+/* One entry of a verify pass (a layer stack).  Entries must be listed with
+ * non-decreasing group; group g+1 depends on group g.  Zero-initialise, then
+ * set: the fields after y default to a plain GEMV whose x does not depend
+ * on the pass.
+ *
+ * VG_OP_GEMV: y[N][M] = x[N][K] . dequant(W)[M][K]^T.
+ * VG_OP_SWIGLU, the gated activation fused into the epilogue of the MLP's
+ *   gate and up projections (engine card, Model section: the MLPs): W is a
+ *   gated pair packed by vg_nvfp4_pack_gated / vg_fp8_pack_gated, M = 2*I
+ *   (I gate rows and I up rows, I % 8 == 0), and
+ *     y[n][i] = bf16( SiLU(g) * u ),  g = x[n] . Wgate[i],  u = x[n] . Wup[i],
+ *   with g and u kept in FP32 (never rounded to BF16); y is [N][I].  NVFP4:
+ *   gscale is the gate half's tensor scale, gscale_up the up half's; FP8:
+ *   rowscale / rowscale_up are the halves' FP32 row scales [I].
+ * VG_OP_RMSNORM, the row reduction before a layer's projections (engine
+ *   card, Checks section: row reductions are checked next to the GEMVs):
+ *     y[n][k] = bf16( x[n][k] * gamma[k] / sqrt(sum_k x[n][k]^2 / K + eps) ),
+ *   sums and scaling in FP32; x and y [N][K], gamma BF16 [K]; format, M, w,
+ *   scales and rowscale are ignored.  It runs as one item of the pass.
+ * x_after_group = 1 says that x is written earlier in the same pass (by the
+ *   previous group, e.g. the down projection's x = the gated pair's y, or
+ *   q/k/v's x = an RMS norm's y): its copy into the kernel is then issued
+ *   only after the previous group has completed.  0 (default): x is ready
+ *   before the pass starts and is copied ahead of the group order. */
 typedef struct vg_matrix_desc {
     int32_t format;          /* VG_FMT_NVFP4 or VG_FMT_FP8_ROWSCALE */
     int32_t group;           /* dependency group */
     int64_t M, K;
     const void *w;           /* device, packed codes */
     const void *scales;      /* device, packed block scales (NVFP4), else NULL */
-    const float *rowscale;   /* device FP32 [M] (FP8), else NULL */
-    float gscale;            /* tensor scale (NVFP4) */
+    const float *rowscale;   /* device FP32 [M] (FP8; SWIGLU: gate rows [I]), else NULL */
+    float gscale;            /* tensor scale (NVFP4; SWIGLU: of the gate rows) */
     const uint16_t *x;       /* device BF16 [N][K] */
-    uint16_t *y;             /* device BF16 [N][M] */
+    uint16_t *y;             /* device BF16 [N][M] ([N][M/2] SWIGLU, [N][K] RMSNORM) */
+    int32_t op;              /* VG_OP_* (0: GEMV) */
+    int32_t x_after_group;   /* 1: x is written by the previous group of this pass */
+    float gscale_up;         /* SWIGLU, NVFP4: tensor scale of the up rows */
+    float eps;               /* RMSNORM */
+    const float *rowscale_up;/* SWIGLU, FP8: device FP32 row scales of the up rows [I] */
+    const uint16_t *gamma;   /* RMSNORM: device BF16 weights [K] */
 } vg_matrix_desc;
 
 typedef struct vg_verify_plan vg_verify_plan;

@@ -18,12 +18,14 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import VG_FMT_FP8_ROWSCALE, VG_FMT_NVFP4, VGError  # noqa: F401
+from ._lib import (VG_FMT_FP8_ROWSCALE, VG_FMT_NVFP4, VG_OP_GEMV, VG_OP_RMSNORM,  # noqa: F401
+                   VG_OP_SWIGLU, VGError)
 
 __all__ = [
     "NVFP4Weight", "FP8Weight", "nvfp4_pack", "fp8_pack", "nvfp4_unpack", "fp8_unpack",
     "nvfp4_from_canonical", "fp8_from_canonical", "gemv", "workspace_for", "VerifyPlan",
-    "VGError", "VG_FMT_NVFP4", "VG_FMT_FP8_ROWSCALE",
+    "VGError", "VG_FMT_NVFP4", "VG_FMT_FP8_ROWSCALE", "NVFP4GatedWeight", "FP8GatedWeight",
+    "nvfp4_pack_gated", "fp8_pack_gated", "RMSNorm",
 ]
 
 
@@ -75,6 +77,61 @@ class FP8Weight:
         return self.M * self.K + 4 * self.M
 
 
+@dataclass
+class NVFP4GatedWeight:
+    """A gate/up pair packed for the fused gated activation: M = 2*I rows,
+    each 16-row tile holding 8 gate rows and the same 8 up rows."""
+
+    w: torch.Tensor
+    scales: torch.Tensor
+    gscale: float            # tensor scale of the gate half
+    gscale_up: float         # tensor scale of the up half
+    I: int
+    K: int
+    fmt: int = VG_FMT_NVFP4
+    op: int = VG_OP_SWIGLU
+
+    @property
+    def M(self) -> int:
+        return 2 * self.I
+
+    @property
+    def nbytes(self) -> int:
+        """Both halves' codes and block scales, and their two tensor scales."""
+        return self.M * self.K // 2 + self.M * self.K // 16 + 8
+
+
+@dataclass
+class FP8GatedWeight:
+    """A gate/up pair of row-scaled FP8 weights packed like NVFP4GatedWeight."""
+
+    w: torch.Tensor
+    rowscale: torch.Tensor     # float32 [I], gate rows
+    rowscale_up: torch.Tensor  # float32 [I], up rows
+    I: int
+    K: int
+    fmt: int = VG_FMT_FP8_ROWSCALE
+    op: int = VG_OP_SWIGLU
+
+    @property
+    def M(self) -> int:
+        return 2 * self.I
+
+    @property
+    def nbytes(self) -> int:
+        return self.M * self.K + 4 * self.M
+
+
+@dataclass
+class RMSNorm:
+    """An RMS normalisation entry of a verify pass: y = x * gamma / rms(x)."""
+
+    gamma: torch.Tensor      # bfloat16 [K]
+    eps: float = 1e-6
+    op: int = VG_OP_RMSNORM
+    nbytes: int = 0          # no weights
+
+
 def nvfp4_sizes(M: int, K: int):
     wb, sb = ctypes.c_size_t(), ctypes.c_size_t()
     _lib.check(_lib.vg_nvfp4_sizes(M, K, ctypes.byref(wb), ctypes.byref(sb)), "vg_nvfp4_sizes")
@@ -108,6 +165,38 @@ def fp8_pack(W: torch.Tensor, stream=None) -> FP8Weight:
     rs = torch.empty(M, dtype=torch.float32, device=W.device)
     _lib.check(_lib.vg_fp8_pack(_ptr(W), M, K, _ptr(w), _ptr(rs), _stream(stream)), "vg_fp8_pack")
     return FP8Weight(w, rs, M, K)
+
+
+def nvfp4_pack_gated(Wgate: torch.Tensor, Wup: torch.Tensor, stream=None) -> NVFP4GatedWeight:
+    """NVFP4 gate/up pair for the fused gated activation (each half with its
+    own tensor scale, quantised exactly as nvfp4_pack would)."""
+    _dev_tensor(Wgate, torch.float32, "Wgate")
+    _dev_tensor(Wup, torch.float32, "Wup")
+    if Wgate.shape != Wup.shape:
+        raise ValueError("gate and up must have the same shape")
+    I, K = Wgate.shape
+    wb, sb = nvfp4_sizes(2 * I, K)
+    w = torch.empty(wb, dtype=torch.uint8, device=Wgate.device)
+    sc = torch.empty(sb, dtype=torch.uint8, device=Wgate.device)
+    gs = (ctypes.c_float * 2)()
+    _lib.check(_lib.vg_nvfp4_pack_gated(_ptr(Wgate), _ptr(Wup), I, K, _ptr(w), _ptr(sc), gs,
+                                        _stream(stream)), "vg_nvfp4_pack_gated")
+    return NVFP4GatedWeight(w, sc, gs[0], gs[1], I, K)
+
+
+def fp8_pack_gated(Wgate: torch.Tensor, Wup: torch.Tensor, stream=None) -> FP8GatedWeight:
+    """Row-scaled FP8 gate/up pair for the fused gated activation."""
+    _dev_tensor(Wgate, torch.float32, "Wgate")
+    _dev_tensor(Wup, torch.float32, "Wup")
+    if Wgate.shape != Wup.shape:
+        raise ValueError("gate and up must have the same shape")
+    I, K = Wgate.shape
+    w = torch.empty(fp8_sizes(2 * I, K), dtype=torch.uint8, device=Wgate.device)
+    rg = torch.empty(I, dtype=torch.float32, device=Wgate.device)
+    ru = torch.empty(I, dtype=torch.float32, device=Wgate.device)
+    _lib.check(_lib.vg_fp8_pack_gated(_ptr(Wgate), _ptr(Wup), I, K, _ptr(w), _ptr(rg), _ptr(ru),
+                                      _stream(stream)), "vg_fp8_pack_gated")
+    return FP8GatedWeight(w, rg, ru, I, K)
 
 
 def nvfp4_unpack(wt: NVFP4Weight, stream=None):
@@ -191,27 +280,45 @@ def workspace_error(workspace: torch.Tensor, stream=None) -> int:
 
 
 class VerifyPlan:
-    """A fused verify pass over a list of (weight, x, y, group) matrices."""
+    """A fused verify pass over a list of entries (op, x, y, group) or
+    (op, x, y, group, x_after_group): op is a packed weight (a GEMV, or a
+    gated pair's fused activation) or an RMSNorm; x_after_group marks an x
+    that the previous group of the same pass writes."""
 
     def __init__(self, entries, N: int, ordered: bool = True, max_ctas: int = 0,
                  wait_timeout_ns: int = 0, hold_group: int = -1):
         self.entries = list(entries)    # keep tensors alive
         arr = (_lib.vg_matrix_desc * len(self.entries))()
-        for i, (wt, x, y, group) in enumerate(self.entries):
+        for i, e in enumerate(self.entries):
+            wt, x, y, group = e[:4]
+            after = bool(e[4]) if len(e) > 4 else False
             _dev_tensor(x, torch.bfloat16, "x")
             _dev_tensor(y, torch.bfloat16, "y")
             d = arr[i]
-            d.format = wt.fmt
             d.group = group
+            d.x_after_group = int(after)
+            d.x = x.data_ptr()
+            d.y = y.data_ptr()
+            op = getattr(wt, "op", VG_OP_GEMV)
+            d.op = op
+            if op == VG_OP_RMSNORM:
+                _dev_tensor(wt.gamma, torch.bfloat16, "gamma")
+                d.M, d.K = 1, x.shape[1]
+                d.gamma = wt.gamma.data_ptr()
+                d.eps = wt.eps
+                continue
+            d.format = wt.fmt
             d.M, d.K = wt.M, wt.K
             d.w = wt.w.data_ptr()
             if wt.fmt == VG_FMT_NVFP4:
                 d.scales = wt.scales.data_ptr()
                 d.gscale = wt.gscale
+                if op == VG_OP_SWIGLU:
+                    d.gscale_up = wt.gscale_up
             else:
                 d.rowscale = wt.rowscale.data_ptr()
-            d.x = x.data_ptr()
-            d.y = y.data_ptr()
+                if op == VG_OP_SWIGLU:
+                    d.rowscale_up = wt.rowscale_up.data_ptr()
         opt = _lib.vg_plan_options(int(bool(ordered)), int(max_ctas), int(wait_timeout_ns),
                                    int(hold_group), 0)
         h = ctypes.c_void_p()

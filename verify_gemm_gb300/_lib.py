@@ -23,6 +23,9 @@ VG_ERR_TIMEOUT = 5
 VG_ERR_WORKSPACE = 6
 VG_FMT_NVFP4 = 0
 VG_FMT_FP8_ROWSCALE = 1
+VG_OP_GEMV = 0
+VG_OP_SWIGLU = 1
+VG_OP_RMSNORM = 2
 
 P = ctypes.c_void_p
 i64 = ctypes.c_int64
@@ -34,7 +37,9 @@ st = ctypes.c_int   # vg_status
 
 class vg_matrix_desc(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("group", ctypes.c_int32), ("M", i64), ("K", i64),
-                ("w", P), ("scales", P), ("rowscale", P), ("gscale", f32), ("x", P), ("y", P)]
+                ("w", P), ("scales", P), ("rowscale", P), ("gscale", f32), ("x", P), ("y", P),
+                ("op", ctypes.c_int32), ("x_after_group", ctypes.c_int32), ("gscale_up", f32),
+                ("eps", f32), ("rowscale_up", P), ("gamma", P)]
 
 
 class vg_plan_options(ctypes.Structure):
@@ -56,6 +61,8 @@ SIGNATURES = {
     "vg_fp8_rowscale_pack": (st, [P, i64, i64, P, P, P]),
     "vg_fp8_rowscale_unpack": (st, [P, i64, i64, P, P]),
     "vg_nvfp4_from_canonical": (st, [P, P, i64, i64, P, P, P]),
+    "vg_nvfp4_pack_gated": (st, [P, P, i64, i64, P, P, ctypes.POINTER(f32), P]),
+    "vg_fp8_pack_gated": (st, [P, P, i64, i64, P, P, P, P]),
     "vg_fp8_from_canonical": (st, [P, i64, i64, P, P]),
     "vg_gemv_workspace_size": (st, [i64, i64, i32, ctypes.POINTER(sz)]),
     "vg_gemv_nvfp4": (st, [P, P, f32, P, i32, i64, i64, P, P, sz, P]),

@@ -348,6 +348,13 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's earlier generic-proxy accesses of global memory
+// (an acquire of data other blocks wrote) before its later async-proxy
+// (bulk or tensor copy) accesses of the same memory, and the converse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // GPU-scope accesses for the cross-block protocol.
 __device__ __forceinline__ void red_add_release(uint32_t *p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

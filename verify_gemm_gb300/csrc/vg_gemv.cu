@@ -64,6 +64,11 @@ struct MatDev {
   uint16_t *y;
   float mult;        // epilogue multiplier (NVFP4: 256 * gscale)
   int fmt;
+  // fused neighbours: flags read at the end of every piece, so kept in the
+  // same cache line as the fields read there
+  int op;            // VG_OP_GEMV, VG_OP_SWIGLU or VG_OP_RMSNORM (then fmt is kFmtNorm)
+  int x_after;       // x is written by the previous phase: copy it after that phase completes
+  int y_async;       // y is read by a later phase through copies: fence before releasing it
   int M, K, MT, KU, KC, RB;
   int cu, ub;        // units per chunk, bytes per unit
   int rt, cpi;       // tiles per row block, chunks per item (16 / rt)
@@ -72,7 +77,14 @@ struct MatDev {
   int64_t rb_bytes;  // code bytes of a full row block (rt tiles x KU units)
   int item0;         // first item of this matrix within its phase
   const CUtensorMap *xmap;  // x as [K/64 units][N rows][64 columns], or nullptr
+  int Mo;            // rows of y (M, or M / 2 for a gated pair)
+  float mult2;       // SWIGLU, NVFP4: epilogue multiplier of the up rows
+  const float *rowscale2;  // SWIGLU, FP8: row scales of the up rows
+  const uint16_t *gamma;   // RMSNORM weights
+  float eps;
 };
+// Internal format of an RMS-norm item (no weights; one item, no copies).
+constexpr int kFmtNorm = 7;
 
 // Item counts fit 32 bits: a matrix has fewer than 2^40 / (256 x 512) items
 // and a plan's phase is checked on the host.
@@ -102,6 +114,7 @@ struct Params {
                             // slot that any call sharing this workspace may have written
   uint32_t m8, m64;         // 8 and 64: shift multipliers kept in registers
   int x0_tensor;
+  int fused;                // (host) the pass has fused operations or dependent x
   MatDev mat0;
   PhaseDev phase0;
 };
@@ -424,9 +437,51 @@ constexpr int kBoundaryPf = VG_BPF;
 // warp), is split over two sub-partitions.  A single product, a short
 // launch, runs one producer over both slots (np = 1): there the second
 // measured 1-2 us slower per launch.  `which` is the producer's index.
+// A producer's wait for the previous phase before it copies an x that phase
+// writes (bounded), bringing its next items into L2 meanwhile; then the
+// acquire is ordered before the x copies.  Returns
+// false if the wait ran out or another block failed.
+__device__ __forceinline__ bool producer_dep_wait(const Params &p, const MatDev *mats,
+                                               const PhaseDev *phases, const Seq &q, int np) {
+  const uint32_t *d = p.done + (q.ph - 1);
+  const uint32_t target = uint32_t(phases[q.ph - 1].rbs);
+  if (ld_acquire(d) < target) {
+    const uint64_t deadline = globaltimer() + p.timeout_ns;
+    Seq f = q;
+    int ahead = 0;
+    uint32_t it = 0;
+    while (ld_acquire(d) < target) {
+      if (ahead < kBoundaryPf && f.valid) {
+        const MatDev &fm = mats[f.mi];
+        if (fm.fmt != kFmtNorm) {
+          const int ft = min(fm.rt, fm.MT - f.rb * fm.rt);
+          const int fu = min(fm.iu, fm.KU - f.c * fm.iu);
+          bulk_prefetch_l2(fm.w + item_code_off(fm, f.rb, f.c, ft), uint32_t(ft * fu * fm.ub));
+          if (fm.fmt == VG_FMT_NVFP4)
+            bulk_prefetch_l2(fm.sc + item_scale_off(fm, f.rb, f.c, ft),
+                             uint32_t(ft * fm.cpi * kNvScaleChunkBytes));
+        }
+        for (int k = 0; k < np && f.valid; ++k) f.advance(mats, phases, p);
+        ++ahead;
+      }
+      if ((++it & 7u) == 0) {
+        if (globaltimer() > deadline) {
+          set_error(p.error, kErrDepWait);
+          return false;
+        }
+        if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
+      }
+      __nanosleep(32);
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
 #ifndef VG_PARK_NS
 #define VG_PARK_NS 2000
 #endif
+template <bool kFused>
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0,
                          const volatile int *dep_waiting, int which, int np, int N) {
@@ -440,7 +495,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   Seq pf = q;       // next item to bring into L2 during a dependency wait
   int pf_ahead = 0; // items between q and pf (pf is stale while 0)
   // the current matrix's fields, cached while the matrix does not change
-  int cur_mi = -1;
+  int cur_mi = -1, is_norm = 0, xdep = 0, dep_ok = -1;
   const uint8_t *w = nullptr, *sc = nullptr;
   const uint16_t *xg = nullptr;
   const CUtensorMap *tmap = nullptr;
@@ -451,6 +506,8 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     if (q.mi != cur_mi) {
       const MatDev &m = mats[q.mi];
       cur_mi = q.mi;
+      is_norm = m.fmt == kFmtNorm;
+      xdep = kFused && m.x_after && p.done && q.ph > 0;
       w = m.w;
       sc = m.fmt == VG_FMT_NVFP4 ? m.sc : nullptr;
       xg = m.x;
@@ -479,6 +536,14 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     const uint8_t *scale_src =
         sc ? sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * kNvScaleChunkBytes : nullptr;
     const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
+
+    // ---- x written by the previous phase of this pass: wait until that
+    // phase has completed (bounded), bringing this producer's next items
+    // into L2 meanwhile; then order the acquire before the x copies
+    if (kFused && xdep && dep_ok != q.ph) {
+      if (!producer_dep_wait(p, mats, phases, q, np)) break;
+      dep_ok = q.ph;
+    }
 
     // ---- wait for the slot
     if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
@@ -510,7 +575,10 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
       }
     }
 
-    // ---- issue
+    // ---- issue (an RMS-norm item carries no data: its slot completes at once)
+    if (is_norm) {
+      mbar_arrive_expect_tx(full, 0u);
+    } else {
     mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes);
     bulk_g2s(slot, code_src, code_bytes, full, pol_w);
     if (sc) bulk_g2s(slot + kItemScaleOff, scale_src, scale_bytes, full, pol_w);
@@ -521,6 +589,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
       for (int n = 0; n < N; ++n)
         bulk_g2s(slot + kItemXOff + n * kXRowBytes, xg + int64_t(n) * K + k0, row_bytes, full,
                  pol_x);
+    }
     }
     used |= 1u << s;
     last_par = (last_par & ~(1u << s)) | (par << s);
@@ -602,6 +671,28 @@ __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_
   return true;
 }
 
+// Epilogue of a gated pair: rows g (gate) and g + 8 (up) of tile mt are
+// gate and up row 8 mt + g; y = SiLU(gate) * up from the FP32 sums, rounded
+// once to BF16.  Out of line, like the other rarely taken paths.
+__device__ __noinline__ void swiglu_epilogue(const MatDev &m, int mt, int g, int t, int N,
+                                             const float (&accs)[4]) {
+  const int gi = mt * 8 + g;
+  if (gi >= m.Mo) return;
+  const bool nv = m.fmt == VG_FMT_NVFP4;
+  const float mg = nv ? m.mult : __ldg(m.rowscale + gi);
+  const float mu = nv ? m.mult2 : __ldg(m.rowscale2 + gi);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int nn = 2 * t + e;
+    if (nn < N) {
+      const float gate = accs[e] * mg, up = accs[2 + e] * mu;
+      const float h = gate / (1.0f + expf(-gate)) * up;
+      const __nv_bfloat16 v = __float2bfloat16_rn(h);
+      m.y[int64_t(nn) * m.Mo + gi] = *reinterpret_cast<const uint16_t *>(&v);
+    }
+  }
+}
+
 // End of a row-block piece.  With several chunks per item (cpi > 1) the
 // warps that share a tile first hand their sums to its first warp (cc == 0)
 // through shared memory, added in chunk order; only that warp goes on.
@@ -612,6 +703,7 @@ __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_
 // without waiting.  In ordered mode the completed row block is counted for
 // its phase.  It runs once per piece, outside the per-item loops.  Returns
 // false if the wait for partial sums failed.
+template <bool kFused>
 __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, int T, int G,
                                           int piece_start, bool full_piece, int rb, int ph,
                                           uint32_t tag, bool aborted, int tl, int cc,
@@ -655,7 +747,9 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
     // mma.sync needs whole warps: a failure anywhere in the warp stops it all
     ok = __all_sync(0xFFFFFFFFu, ok);
   }
-  if (ok && !aborted && lead && mt < m.MT) {
+  if (kFused && ok && !aborted && lead && mt < m.MT && m.op == VG_OP_SWIGLU) {
+    swiglu_epilogue(m, mt, g, t, N, accs);
+  } else if (ok && !aborted && lead && mt < m.MT) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = mt * kTileRows + g + 8 * h;
@@ -671,6 +765,8 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
       }
     }
   }
+  // y that a later phase copies in: order these stores before those copies
+  if (kFused && m.y_async && lead) fence_proxy_async_global();
   if (p.done) {
     named_bar(1, kConsumers);
     // releases the row block's y (written before the barrier)
@@ -679,6 +775,71 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
   return ok;
 }
 
+// An RMS-norm item, run by all consumer threads of one block:
+//   y[n][k] = bf16( x[n][k] * inv[n] * gamma[k] ),
+//   inv[n] = 1 / sqrt(sum_k x[n][k]^2 / K + eps),
+// sums in FP32 (per thread, then per warp, then across warps in `red`).
+// Every thread reaches every barrier; `active` false skips the work.  Kept
+// out of line: inlined, it costs the streaming loops registers.
+__device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, bool active) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K8 = m.K / 8;
+  for (int n = 0; n < N; ++n) {
+    float ss = 0.f;
+    if (active) {
+      const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
+      for (int k = tid; k < K8; k += kConsumers) {
+        const uint4 v = xr[k];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(wv[j] << 16), hi = __uint_as_float(wv[j] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if (lane == 0) red[n * kWarps + warp] = ss;
+  }
+  named_bar(1, kConsumers);
+  if (tid < N) {
+    float tot = 0.f;
+    for (int w = 0; w < kWarps; ++w) tot += red[tid * kWarps + w];
+    red[8 * kWarps + tid] = 1.0f / sqrtf(tot / float(m.K) + m.eps);
+  }
+  named_bar(1, kConsumers);
+  if (active) {
+    const uint4 *gr = reinterpret_cast<const uint4 *>(m.gamma);
+    for (int n = 0; n < N; ++n) {
+      const float inv = red[8 * kWarps + n];
+      const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
+      uint4 *yr = reinterpret_cast<uint4 *>(m.y + int64_t(n) * m.K);
+      for (int k = tid; k < K8; k += kConsumers) {
+        const uint4 v = xr[k], gv = __ldg(gr + k);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float x0 = __uint_as_float(wv[j] << 16), x1 = __uint_as_float(wv[j] & 0xFFFF0000u);
+          const float g0 = __uint_as_float(gw[j] << 16), g1 = __uint_as_float(gw[j] & 0xFFFF0000u);
+          const __nv_bfloat162 r = __floats2bfloat162_rn(x0 * inv * g0, x1 * inv * g1);
+          o[j] = *reinterpret_cast<const uint32_t *>(&r);
+        }
+        yr[k] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    // a later phase copies y in through the async proxy
+    fence_proxy_async_global();
+  }
+  named_bar(1, kConsumers);
+}
+
+// Two instantiations: kFused = false for passes of plain products (single
+// GEMVs and verify passes without fused operations or dependent x), which
+// then carry none of that code; kFused = true for the rest.
+template <bool kFused>
 __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzled tensor copies need 1024-byte alignment in shared memory
@@ -722,7 +883,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     // ================================================================ producer
     const int np = p.mats ? kProducers : 1;
     if (lane == 0 && warp - kWarps < np)
-      producer(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots),
+      producer<kFused>(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots),
                sflag + 3, warp - kWarps, np, N);
 
   } else {
@@ -811,6 +972,28 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         // the warp's chunk starts cc chunks into the item's x slice
         xoff_t = xoff_t0 + uint32_t(cc * mm.cu * 1024);
         xt = p.mats ? mm.xmap != nullptr : p.x0_tensor != 0;
+      }
+      if (kFused && fmt == kFmtNorm) {
+        // an RMS-norm item: its slot carries no data (take it and give it
+        // back), this block's consumers normalise x into y, and the item
+        // completes its phase
+        if (!aborted) {
+          const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
+          if (!__all_sync(0xFFFFFFFFu, ready)) {
+            if (lane == 0) set_error(p.error, kErrFullWait);
+            aborted = true;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (++s == kSlots) {
+          s = 0;
+          par ^= 1u;
+        }
+        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted);
+        if (tid == 0 && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
+        cons.skip(1, mats, phases, p);
+        continue;
       }
       // ------------------------------------------------- one row-block piece
       // the block's contiguous items of one row block: set up once, then a
@@ -923,7 +1106,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
 #pragma unroll
         for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
       }
-      if (!finish_piece(p, mats[cons.mi], cons.items, cons.G, piece_start,
+      if (!finish_piece<kFused>(p, mats[cons.mi], cons.items, cons.G, piece_start,
                         c0 == 0 && len == cons.KI, rb, ph, tag, aborted, tl, cc, red, N,
                         accs[0], accs[1], accs[2], accs[3]))
         aborted = true;
@@ -984,7 +1167,9 @@ vg_status device_info(int *dev_out, DeviceInfo **info) {
     VG_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
     d.cc = major * 10 + minor;
     if (d.cc != 103) return VG_ERR_UNSUPPORTED;
-    VG_CUDA(cudaFuncSetAttribute(stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    VG_CUDA(cudaFuncSetAttribute(stream_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes));
+    VG_CUDA(cudaFuncSetAttribute(stream_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes));
     d.attr_set = true;
   }
@@ -1056,12 +1241,39 @@ MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, co
   m.kfull = int(K / (int64_t(m.iu) * kUnitK));
   m.RB = int(ceil_div(m.MT, m.rt));
   m.rb_bytes = int64_t(m.rt) * m.KU * m.ub;
+  m.op = VG_OP_GEMV;
+  m.Mo = m.M;
+  return m;
+}
+
+// An RMS-norm entry: one item, no weights, no copies.
+MatDev make_norm_mat(int64_t K, const uint16_t *x, uint16_t *y, const uint16_t *gamma, float eps) {
+  MatDev m;
+  std::memset(&m, 0, sizeof m);
+  m.x = x;
+  m.y = y;
+  m.gamma = gamma;
+  m.eps = eps;
+  m.fmt = kFmtNorm;
+  m.op = VG_OP_RMSNORM;
+  m.M = 1;
+  m.Mo = int(K);
+  m.K = int(K);
+  m.MT = m.KU = m.KC = m.RB = m.KI = 1;
+  m.cu = kNvChunkUnits;
+  m.ub = kNvUnitBytes;
+  m.rt = kBlockTiles;
+  m.cpi = 1;
+  m.iu = kNvChunkUnits;
   return m;
 }
 
 int64_t algorithmic_bytes(const MatDev &m) {
+  if (m.fmt == kFmtNorm) return 0;                 // no weights
   const int64_t E = int64_t(m.M) * m.K;
-  return m.fmt == VG_FMT_NVFP4 ? E / 2 + E / 16 + 4 : E + 4 * int64_t(m.M);
+  // a gated pair carries the tensor scales of both halves
+  const int64_t gs_bytes = m.op == VG_OP_SWIGLU ? 8 : 4;
+  return m.fmt == VG_FMT_NVFP4 ? E / 2 + E / 16 + gs_bytes : E + 4 * int64_t(m.M);
 }
 
 // Single-GEMV workspace: [header words | partial slots].
@@ -1077,7 +1289,9 @@ void set_head(Params &p, uint8_t *head) {
 // other contributors), which a cooperative launch guarantees.
 vg_status launch(const Params &p, vg_stream_t stream) {
   void *args[] = {const_cast<Params *>(&p)};
-  VG_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&stream_kernel), dim3(p.grid),
+  const void *fn = p.fused ? reinterpret_cast<const void *>(&stream_kernel<true>)
+                           : reinterpret_cast<const void *>(&stream_kernel<false>);
+  VG_CUDA(cudaLaunchCooperativeKernel(fn, dim3(p.grid),
                                       dim3(kKernelThreads), args, kSmemBytes, as_cuda(stream)));
   return VG_OK;
 }
@@ -1086,7 +1300,8 @@ vg_status launch(const Params &p, vg_stream_t stream) {
 // what can be resident at once.
 vg_status max_grid(const DeviceInfo &d, int *grid) {
   int per_sm = 0;
-  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel, kKernelThreads,
+  // both instantiations have the same registers, threads and shared memory
+  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<true>, kKernelThreads,
                                                         kSmemBytes));
   if (per_sm < 1) return VG_ERR_UNSUPPORTED;
   *grid = std::min(d.sms, per_sm * d.sms);
@@ -1234,17 +1449,38 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   int hold_phase = -1;
   for (int i = 0; i < count; ++i) {
     const vg_matrix_desc &d = mats[i];
-    if (vg_status s = check_gemv_args(d.w, d.x, d.y, N, d.M, d.K)) return s;
     if (i > 0 && d.group < mats[i - 1].group) return VG_ERR_INVALID_ARG;
-    if (d.format == VG_FMT_NVFP4) {
-      if (!d.scales) return VG_ERR_INVALID_ARG;
-      if (!aligned16(d.scales)) return VG_ERR_ALIGNMENT;
-    } else if (d.format == VG_FMT_FP8_ROWSCALE) {
-      if (!d.rowscale) return VG_ERR_INVALID_ARG;
+    // fused operations and dependent x need the group order
+    if ((d.op != VG_OP_GEMV || d.x_after_group) && !o.ordered) return VG_ERR_INVALID_ARG;
+    if (d.x_after_group && (i == 0 || d.group == mats[0].group)) return VG_ERR_INVALID_ARG;
+    if (d.op == VG_OP_RMSNORM) {
+      if (vg_status s = check_mk(1, d.K)) return s;
+      if (!d.x || !d.y || !d.gamma || !(d.eps >= 0.0f) || N < 1 || N > 8)
+        return VG_ERR_INVALID_ARG;
+      if (!aligned16(d.x) || !aligned16(d.y) || !aligned16(d.gamma)) return VG_ERR_ALIGNMENT;
+      hm[i] = make_norm_mat(d.K, d.x, d.y, d.gamma, d.eps);
     } else {
-      return VG_ERR_INVALID_ARG;
+      if (d.op != VG_OP_GEMV && d.op != VG_OP_SWIGLU) return VG_ERR_INVALID_ARG;
+      if (vg_status s = check_gemv_args(d.w, d.x, d.y, N, d.M, d.K)) return s;
+      if (d.format == VG_FMT_NVFP4) {
+        if (!d.scales) return VG_ERR_INVALID_ARG;
+        if (!aligned16(d.scales)) return VG_ERR_ALIGNMENT;
+      } else if (d.format == VG_FMT_FP8_ROWSCALE) {
+        if (!d.rowscale) return VG_ERR_INVALID_ARG;
+        if (d.op == VG_OP_SWIGLU && !d.rowscale_up) return VG_ERR_INVALID_ARG;
+      } else {
+        return VG_ERR_INVALID_ARG;
+      }
+      hm[i] = make_mat(d.format, d.M, d.K, d.w, d.scales, d.rowscale, d.gscale, d.x, d.y);
+      if (d.op == VG_OP_SWIGLU) {
+        if (d.M % 16 != 0) return VG_ERR_INVALID_ARG;   // I % 8 == 0
+        hm[i].op = VG_OP_SWIGLU;
+        hm[i].Mo = int(d.M / 2);
+        hm[i].mult2 = kNvEpilogueScale * d.gscale_up;
+        hm[i].rowscale2 = d.rowscale_up;
+      }
     }
-    hm[i] = make_mat(d.format, d.M, d.K, d.w, d.scales, d.rowscale, d.gscale, d.x, d.y);
+    hm[i].x_after = d.x_after_group ? 1 : 0;
     const bool new_phase = hp.empty() || (o.ordered && d.group != mats[i - 1].group);
     if (new_phase) {
       PhaseDev ph;
@@ -1263,6 +1499,13 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
     ph.rbs += hm[i].RB;
     ph.mat_end = i + 1;
     bytes += algorithmic_bytes(hm[i]);
+  }
+  // a phase whose y a dependent x of the next phase copies in fences its stores
+  for (size_t ph = 0; ph + 1 < hp.size(); ++ph) {
+    bool next_dep = false;
+    for (int j = hp[ph + 1].mat_begin; j < hp[ph + 1].mat_end; ++j) next_dep |= hm[j].x_after != 0;
+    if (next_dep)
+      for (int j = hp[ph].mat_begin; j < hp[ph].mat_end; ++j) hm[j].y_async = 1;
   }
   int grid = 0;
   if (vg_status s = max_grid(*di, &grid)) return s;
@@ -1286,6 +1529,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   if (e == cudaSuccess) {
     std::vector<CUtensorMap> maps(hm.size());
     for (size_t i = 0; i < hm.size(); ++i) {
+      if (hm[i].fmt == kFmtNorm) continue;   // no copies
       hm[i].xmap = make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].iu) ? plan->d_xmaps + i : nullptr;
       if (!hm[i].xmap && hm[i].cpi > 1) untensored = true;
     }
@@ -1323,6 +1567,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   p.done = plan->ordered ? reinterpret_cast<uint32_t *>(plan->d_state + kWsHead) : nullptr;
   p.partials = reinterpret_cast<uint64_t *>(plan->d_state + kWsHead + done_bytes);
   p.clear_slots = grid;   // the plan's state is its own
+  for (const MatDev &m : hm) p.fused |= m.op != VG_OP_GEMV || m.x_after;
   *plan_out = plan;
   return VG_OK;
 }

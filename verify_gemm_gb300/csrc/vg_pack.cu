@@ -116,9 +116,13 @@ __global__ void f8_rowscale_kernel(const float *__restrict__ W, int64_t M, int64
 
 // --------------------------------------------------------- NVFP4 packing
 // One thread per (tile, unit, lane): the lane's 16 columns of rows g, g+8.
+// With W2 set the matrix is a gated pair of M = 2I rows: tile row g comes
+// from row 8*mt + g of W (gate, tensor scale gs) and tile row g + 8 from the
+// same row of W2 (up, tensor scale gs2).
 
 __global__ void nv_pack_kernel(const float *__restrict__ W, Geom G, float gs,
-                               uint8_t *__restrict__ w_out, uint8_t *__restrict__ sc_out) {
+                               uint8_t *__restrict__ w_out, uint8_t *__restrict__ sc_out,
+                               const float *__restrict__ W2 = nullptr, float gs2 = 0.0f) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= G.MT * G.KU * 32) return;
   const int lane = int(idx & 31);
@@ -128,9 +132,12 @@ __global__ void nv_pack_kernel(const float *__restrict__ W, Geom G, float gs,
   uint32_t words[4] = {0, 0, 0, 0};
   for (int ri = 0; ri < 2; ++ri) {
     const int64_t row = mt * kTileRows + g + 8 * ri;
+    const int64_t srow = W2 ? mt * 8 + g : row;          // row of the source matrix
+    const float *Ws = W2 && ri ? W2 : W;
+    const float gsr = W2 && ri ? gs2 : gs;
     uint32_t code = 0;
     if (row < G.M && k0 < G.K) {
-      const float *w = W + row * G.K + k0;
+      const float *w = Ws + srow * G.K + k0;
       float v[16];
       uint32_t bm = 0;
 #pragma unroll
@@ -139,8 +146,8 @@ __global__ void nv_pack_kernel(const float *__restrict__ W, Geom G, float gs,
         bm = max(bm, abs_bits(v[j]));
       }
       const float bamax = __uint_as_float(bm);
-      if (gs != 0.0f) code = e4m3_rn_sat(__fdiv_rn(__fdiv_rn(bamax, gs), 6.0f));
-      const float d = __fmul_rn(e4m3_to_float(code), gs);
+      if (gsr != 0.0f) code = e4m3_rn_sat(__fdiv_rn(__fdiv_rn(bamax, gsr), 6.0f));
+      const float d = __fmul_rn(e4m3_to_float(code), gsr);
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {
         const uint32_t c = d == 0.0f ? 0u : e2m1_rn_sat(__fdiv_rn(v[kk], d));
@@ -233,8 +240,11 @@ __global__ void nv_from_canonical_kernel(const uint8_t *__restrict__ nib,
 
 // ------------------------------------------------------------ FP8 packing
 
+// With W2 set, a gated pair as in nv_pack_kernel: tile row g + 8 comes from
+// W2 with row scales rs2.
 __global__ void f8_pack_kernel(const float *__restrict__ W, const float *__restrict__ rs, Geom G,
-                               uint8_t *__restrict__ w_out) {
+                               uint8_t *__restrict__ w_out, const float *__restrict__ W2 = nullptr,
+                               const float *__restrict__ rs2 = nullptr) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= G.MT * G.KU * 32) return;
   const int lane = int(idx & 31);
@@ -247,8 +257,9 @@ __global__ void f8_pack_kernel(const float *__restrict__ W, const float *__restr
   for (int ri = 0; ri < 2; ++ri) {
     const int64_t row = mt * kTileRows + g + 8 * ri;
     if (row >= G.M || k0 >= G.K) continue;
-    const float s = rs[row];
-    const float *w = W + row * G.K + k0;
+    const int64_t srow = W2 ? mt * 8 + g : row;
+    const float s = (W2 && ri ? rs2 : rs)[srow];
+    const float *w = (W2 && ri ? W2 : W) + srow * G.K + k0;
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       const uint32_t c = s == 0.0f ? 0u : e4m3_rn_sat(__fdiv_rn(w[kk], s));
@@ -483,4 +494,80 @@ extern "C" vg_status vg_fp8_rowscale_pack(const float *W, int64_t M, int64_t K, 
 extern "C" vg_status vg_fp8_rowscale_unpack(const void *w, int64_t M, int64_t K, uint8_t *q_out,
                                             vg_stream_t stream) {
   return vg_fp8_unpack(w, M, K, q_out, stream);
+}
+
+// ------------------------------------------------------------ gated pairs
+
+namespace {
+// Tensor scale of one FP32 matrix (amax / 2688), through a word of device
+// scratch; synchronises.
+vg_status nv_tensor_scale(const float *W, int64_t n, uint32_t *scratch, cudaStream_t st,
+                          float *gs) {
+  VG_CUDA(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st));
+  amax_kernel<<<reduce_blocks(n), 256, 0, st>>>(W, n, scratch);
+  VG_LAUNCH_CHECK();
+  uint32_t bits = 0;
+  VG_CUDA(cudaMemcpyAsync(&bits, scratch, sizeof bits, cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  if (bits >= 0x7F800000u) return VG_ERR_INVALID_ARG;
+  float amax;
+  std::memcpy(&amax, &bits, sizeof amax);
+  *gs = amax / 2688.0f;
+  return VG_OK;
+}
+}  // namespace
+
+extern "C" vg_status vg_nvfp4_pack_gated(const float *Wgate, const float *Wup, int64_t I,
+                                         int64_t K, void *w_out, void *scales_out,
+                                         float *gscales_out, vg_stream_t stream) {
+  if (I % 8 != 0) return VG_ERR_INVALID_ARG;
+  if (vg_status s = check_mk(2 * I, K)) return s;
+  if (!Wgate || !Wup || !w_out || !scales_out || !gscales_out) return VG_ERR_INVALID_ARG;
+  if (!aligned16(Wgate) || !aligned16(Wup) || !aligned16(w_out) || !aligned16(scales_out))
+    return VG_ERR_ALIGNMENT;
+  cudaStream_t st = as_cuda(stream);
+  const Geom G = nv_geom(2 * I, K);
+  uint32_t *scratch = static_cast<uint32_t *>(scales_out);   // rewritten below
+  float gs[2];
+  if (vg_status s = nv_tensor_scale(Wgate, I * K, scratch, st, &gs[0])) return s;
+  if (vg_status s = nv_tensor_scale(Wup, I * K, scratch, st, &gs[1])) return s;
+  VG_CUDA(cudaMemsetAsync(scales_out, 0, size_t(G.MT * G.KC * kNvScaleChunkBytes), st));
+  const int64_t threads = G.MT * G.KU * 32;
+  nv_pack_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
+      Wgate, G, gs[0], static_cast<uint8_t *>(w_out), static_cast<uint8_t *>(scales_out), Wup,
+      gs[1]);
+  VG_LAUNCH_CHECK();
+  gscales_out[0] = gs[0];
+  gscales_out[1] = gs[1];
+  return VG_OK;
+}
+
+extern "C" vg_status vg_fp8_pack_gated(const float *Wgate, const float *Wup, int64_t I, int64_t K,
+                                       void *w_out, float *rs_gate_out, float *rs_up_out,
+                                       vg_stream_t stream) {
+  if (I % 8 != 0) return VG_ERR_INVALID_ARG;
+  if (vg_status s = check_mk(2 * I, K)) return s;
+  if (!Wgate || !Wup || !w_out || !rs_gate_out || !rs_up_out) return VG_ERR_INVALID_ARG;
+  if (!aligned16(Wgate) || !aligned16(Wup) || !aligned16(w_out) || !aligned16(rs_gate_out) ||
+      !aligned16(rs_up_out))
+    return VG_ERR_ALIGNMENT;
+  cudaStream_t st = as_cuda(stream);
+  const Geom G = f8_geom(2 * I, K);
+  f8_rowscale_kernel<<<blocks_for(I, 8), 256, 0, st>>>(Wgate, I, K, rs_gate_out);
+  VG_LAUNCH_CHECK();
+  f8_rowscale_kernel<<<blocks_for(I, 8), 256, 0, st>>>(Wup, I, K, rs_up_out);
+  VG_LAUNCH_CHECK();
+  std::vector<float> rs(static_cast<size_t>(2 * I));
+  VG_CUDA(cudaMemcpyAsync(rs.data(), rs_gate_out, sizeof(float) * size_t(I),
+                          cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaMemcpyAsync(rs.data() + I, rs_up_out, sizeof(float) * size_t(I),
+                          cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  for (float v : rs)
+    if (!(v <= 3.4028234663852886e38f)) return VG_ERR_INVALID_ARG;   // NaN or Inf
+  const int64_t threads = G.MT * G.KU * 32;
+  f8_pack_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
+      Wgate, rs_gate_out, G, static_cast<uint8_t *>(w_out), Wup, rs_up_out);
+  VG_LAUNCH_CHECK();
+  return VG_OK;
 }

@@ -140,6 +140,17 @@ def draw_x(gen: torch.Generator, N: int, K: int, outliers: int = 0,
     return x.to(torch.bfloat16)
 
 
+def draw_norm_inputs(seed: int, layer: int, which: int, N: int, K: int, device="cpu"):
+    """x [N, K] BF16 ~ N(0, 1) and gamma [K] BF16 ~ 1 + 0.1 N(0, 1) of one
+    RMS normalisation of a fused layer (which: 0 before q/k/v, 1 before the
+    MLP), from the derived seeds of indices 12 + which and 14 + which."""
+    gx = generator(stack_seed(seed, layer, 12 + which), device)
+    x = torch.randn((N, K), generator=gx, dtype=torch.float32, device=device).to(torch.bfloat16)
+    gg = generator(stack_seed(seed, layer, 14 + which), device)
+    gamma = (1.0 + 0.1 * torch.randn((K,), generator=gg, dtype=torch.float32, device=device))
+    return x, gamma.to(torch.bfloat16)
+
+
 def bf16_bits(x: torch.Tensor):
     """BF16 tensor -> numpy uint16 bit patterns (host copy)."""
     return x.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

@@ -8,8 +8,10 @@ from dataclasses import dataclass
 
 import torch
 
-from . import FP8Weight, NVFP4Weight, VerifyPlan, fp8_pack, nvfp4_pack
-from .inputs import HIDDEN, INTERMEDIATE, LAYERS, VOCAB, Mat, draw_stack_matrix, stack_mats
+from . import (FP8Weight, NVFP4Weight, RMSNorm, VerifyPlan, fp8_pack, fp8_pack_gated, nvfp4_pack,
+               nvfp4_pack_gated)
+from .inputs import (HIDDEN, INTERMEDIATE, LAYERS, VOCAB, Mat, draw_norm_inputs, draw_stack_matrix,
+                     stack_mats)
 
 
 @dataclass
@@ -83,3 +85,94 @@ def build_stack(N: int, device="cuda", layers: int = LAYERS, seed: int = 4,
 def weight_bytes(w) -> int:
     assert isinstance(w, (NVFP4Weight, FP8Weight))
     return w.nbytes
+
+
+@dataclass
+class FusedEntry:
+    kind: str             # "norm", "gemv", "swiglu"
+    name: str
+    layer: int
+    op: object            # packed weight or RMSNorm
+    x: torch.Tensor
+    y: torch.Tensor
+    group: int
+    after: bool           # x is written by the previous group
+    mats: tuple = ()      # the stack matrices (Mat) behind a weight entry
+
+
+@dataclass
+class FusedStack:
+    entries: list
+    N: int
+
+    @property
+    def bytes(self) -> int:
+        return sum(e.op.nbytes for e in self.entries)
+
+    def plan(self, **kw) -> VerifyPlan:
+        return VerifyPlan([(e.op, e.x, e.y, e.group, e.after) for e in self.entries], self.N,
+                          ordered=True, **kw)
+
+
+def build_fused_stack(N: int, device="cuda", layers: int = LAYERS, seed: int = 4,
+                      attn_fmt: str = "nvfp4", mlp_fmt: str = "nvfp4", down_fmt: str = "fp8",
+                      hidden: int = HIDDEN, inter: int = INTERMEDIATE, vocab: int = VOCAB,
+                      eps: float = 1e-6) -> FusedStack:
+    """The layer stack with its GEMV neighbours fused into the pass and real
+    data dependencies.  Per layer: RMS norm -> {q, k, v} (x = the norm's y)
+    -> {o} (x drawn: the attention output is not part of this path) -> RMS
+    norm -> {gate+up, gated activation} (x = the norm's y) -> {down} (x = the
+    activation's y); after the layers an RMS norm -> head.  The weights are
+    the same draws as the plain stack's (same derived seeds); norm inputs and
+    weights come from their own derived seeds."""
+    def resize(m: Mat) -> Mat:
+        dims = {HIDDEN: hidden, INTERMEDIATE: inter, VOCAB: vocab}
+        return Mat(m.name, m.fmt, dims[m.M], dims[m.K], m.group, m.layer, m.idx)
+
+    base = [resize(m) for m in stack_mats(layers, attn_fmt, down_fmt)]
+    by_name = {m.name: m for m in base}
+    entries = []
+    g = 0
+
+    def bf16(shape):
+        return torch.zeros(shape, dtype=torch.bfloat16, device=device)
+
+    def norm(layer, which, name):
+        nonlocal g
+        x, gamma = draw_norm_inputs(seed, layer, which, N, hidden, device)
+        y = bf16((N, hidden))
+        entries.append(FusedEntry("norm", name, layer, RMSNorm(gamma.contiguous(), eps), x, y, g,
+                                  False))
+        g += 1
+        return y
+
+    def gemv(m: Mat, x, after):
+        W, xd = draw_stack_matrix(m, N, seed, device)
+        wt = nvfp4_pack(W) if m.fmt == "nvfp4" else fp8_pack(W)
+        del W
+        if x is None:
+            x = xd
+        return FusedEntry("gemv", m.name, m.layer, wt, x, bf16((N, m.M)), g, after, (m,))
+
+    for layer in range(layers):
+        xn = norm(layer, 0, f"L{layer}.norm1")
+        for nm in ("q", "k", "v"):
+            entries.append(gemv(by_name[f"L{layer}.{nm}"], xn, True))
+        g += 1
+        entries.append(gemv(by_name[f"L{layer}.o"], None, False))
+        g += 1
+        xn2 = norm(layer, 1, f"L{layer}.norm2")
+        mg, mu = by_name[f"L{layer}.gate"], by_name[f"L{layer}.up"]
+        Wg, _ = draw_stack_matrix(mg, N, seed, device)
+        Wu, _ = draw_stack_matrix(mu, N, seed, device)
+        pair = nvfp4_pack_gated(Wg, Wu) if mlp_fmt == "nvfp4" else fp8_pack_gated(Wg, Wu)
+        del Wg, Wu
+        h = bf16((N, inter))
+        entries.append(FusedEntry("swiglu", f"L{layer}.gate_up", layer, pair, xn2, h, g, True,
+                                  (mg, mu)))
+        g += 1
+        entries.append(gemv(by_name[f"L{layer}.down"], h, True))
+        g += 1
+    xf = norm(layers, 0, "final_norm")
+    entries.append(gemv(by_name["head"], xf, True))
+    return FusedStack(entries, N)
