@@ -70,6 +70,13 @@ def _declare(lib):
                                   P, i64, P, P, ctypes.c_int]),
         "vgo_gemv_fp8": (None, [P, P, P, ctypes.c_int, i64, i64, P, i64, P, P,
                                 ctypes.c_int]),
+        "vgo_e8m0_value": (ctypes.c_double, [ctypes.c_int]),
+        "vgo_mxfp8_quantise": (ctypes.c_int, [P, i64, i64, P, P]),
+        "vgo_int4g_quantise": (ctypes.c_int, [P, i64, i64, P, P]),
+        "vgo_mxfp8_dequant": (None, [P, P, i64, i64, P]),
+        "vgo_int4g_dequant": (None, [P, P, i64, i64, P]),
+        "vgo_gemv_mxfp8": (None, [P, P, P, ctypes.c_int, i64, i64, P, i64, P, P, ctypes.c_int]),
+        "vgo_gemv_int4g": (None, [P, P, P, ctypes.c_int, i64, i64, P, i64, P, P, ctypes.c_int]),
         "vgo_bf16_round": (ctypes.c_uint16, [ctypes.c_double]),
         "vgo_silu": (ctypes.c_double, [ctypes.c_double]),
         "vgo_swiglu": (None, [P, P, P, P, i64, P, P]),
@@ -217,6 +224,76 @@ class Oracle:
         self.lib.vgo_gemv_fp8(_ptr(q), _ptr(rs), _ptr(x_bits), N, M, K,
                               None if r is None else _ptr(r), nr, _ptr(y), _ptr(a),
                               int(threads))
+        return y, a
+
+    # --------------------------------------------------------- other formats
+    def e8m0_value(self, byte):
+        return self.lib.vgo_e8m0_value(int(byte))
+
+    def mxfp8_quantise(self, W):
+        """MXFP8: q [M, K] E4M3 bytes, sc [M, K/32] E8M0 bytes."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        M, K = W.shape
+        assert K % 32 == 0
+        q = np.zeros((M, K), np.uint8)
+        sc = np.zeros((M, K // 32), np.uint8)
+        if self.lib.vgo_mxfp8_quantise(_ptr(W), M, K, _ptr(q), _ptr(sc)) != 0:
+            raise ValueError("non-finite weight")
+        return q, sc
+
+    def int4g_quantise(self, W):
+        """Groupwise INT4: nib [M, K/2] codes, sc [M, K/128] BF16 bits."""
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        M, K = W.shape
+        assert K % 128 == 0
+        nib = np.zeros((M, K // 2), np.uint8)
+        sc = np.zeros((M, K // 128), np.uint16)
+        if self.lib.vgo_int4g_quantise(_ptr(W), M, K, _ptr(nib), _ptr(sc)) != 0:
+            raise ValueError("non-finite weight")
+        return nib, sc
+
+    def mxfp8_dequant(self, q, sc, M, K):
+        out = np.zeros((M, K), np.float64)
+        self.lib.vgo_mxfp8_dequant(_ptr(np.ascontiguousarray(q, dtype=np.uint8)),
+                                   _ptr(np.ascontiguousarray(sc, dtype=np.uint8)), M, K,
+                                   _ptr(out))
+        return out
+
+    def int4g_dequant(self, nib, sc, M, K):
+        out = np.zeros((M, K), np.float64)
+        self.lib.vgo_int4g_dequant(_ptr(np.ascontiguousarray(nib, dtype=np.uint8)),
+                                   _ptr(np.ascontiguousarray(sc, dtype=np.uint16)), M, K,
+                                   _ptr(out))
+        return out
+
+    def gemv_mxfp8(self, q, sc, x_bits, rows=None, threads=1):
+        q = np.ascontiguousarray(q, dtype=np.uint8)
+        sc = np.ascontiguousarray(sc, dtype=np.uint8)
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        M, K = q.shape
+        N = x_bits.shape[0]
+        assert x_bits.shape[1] == K and sc.shape == (M, K // 32)
+        r, nr = self._rows(rows, M)
+        y = np.zeros((N, nr), np.float64)
+        a = np.zeros((N, nr), np.float64)
+        self.lib.vgo_gemv_mxfp8(_ptr(q), _ptr(sc), _ptr(x_bits), N, M, K,
+                                None if r is None else _ptr(r), nr, _ptr(y), _ptr(a),
+                                int(threads))
+        return y, a
+
+    def gemv_int4g(self, nib, sc, x_bits, rows=None, threads=1):
+        nib = np.ascontiguousarray(nib, dtype=np.uint8)
+        sc = np.ascontiguousarray(sc, dtype=np.uint16)
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        M, K = nib.shape[0], nib.shape[1] * 2
+        N = x_bits.shape[0]
+        assert x_bits.shape[1] == K and sc.shape == (M, K // 128)
+        r, nr = self._rows(rows, M)
+        y = np.zeros((N, nr), np.float64)
+        a = np.zeros((N, nr), np.float64)
+        self.lib.vgo_gemv_int4g(_ptr(nib), _ptr(sc), _ptr(x_bits), N, M, K,
+                                None if r is None else _ptr(r), nr, _ptr(y), _ptr(a),
+                                int(threads))
         return y, a
 
     # ----------------------------------------------------- fused neighbours

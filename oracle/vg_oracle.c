@@ -228,8 +228,9 @@ void vgo_fp8_dequant(const uint8_t *q, const float *rs,
 /* ----------------------------------------------------------------- gemv */
 
 typedef struct {
-    int fp8;
+    int fp8;                                      /* 1 FP8 row-scaled, 2 MXFP8, 3 INT4 groups */
     const uint8_t *nib, *sc, *q;
+    const uint16_t *gsc;                          /* INT4 group scales (BF16) */
     const float *rs;
     float gs;
     const uint16_t *x;
@@ -249,8 +250,15 @@ static void gemv_row(const gemv_job *j, int64_t r, double *wrow)
     int64_t k;
     int n;
     for (k = 0; k < j->K; ++k) {
-        if (j->fp8) {
+        if (j->fp8 == 1) {
             wrow[k] = vgo_e4m3_value(j->q[m * j->K + k]) * (double)j->rs[m];
+        } else if (j->fp8 == 2) {
+            wrow[k] = vgo_e4m3_value(j->q[m * j->K + k])
+                    * vgo_e8m0_value(j->sc[m * (j->K / 32) + k / 32]);
+        } else if (j->fp8 == 3) {
+            uint8_t byte = j->nib[m * (j->K / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            wrow[k] = (double)(code - 8) * vgo_bf16_value(j->gsc[m * (j->K / 128) + k / 128]);
         } else {
             uint8_t byte = j->nib[m * (j->K / 2) + k / 2];
             int code = (k & 1) ? (byte >> 4) : (byte & 15);
@@ -324,6 +332,28 @@ void vgo_gemv_nvfp4(const uint8_t *nib, const uint8_t *sc, float gs,
     gemv_run(&j, threads);
 }
 
+void vgo_gemv_mxfp8(const uint8_t *q, const uint8_t *sc, const uint16_t *x, int N, int64_t M,
+                    int64_t K, const int64_t *rows, int64_t nrows, double *y, double *a,
+                    int threads)
+{
+    gemv_job j;
+    memset(&j, 0, sizeof j);
+    j.fp8 = 2; j.q = q; j.sc = sc; j.x = x; j.N = N; j.M = M; j.K = K;
+    j.rows = rows; j.nrows = rows ? nrows : M; j.y = y; j.a = a;
+    gemv_run(&j, threads);
+}
+
+void vgo_gemv_int4g(const uint8_t *nib, const uint16_t *sc, const uint16_t *x, int N, int64_t M,
+                    int64_t K, const int64_t *rows, int64_t nrows, double *y, double *a,
+                    int threads)
+{
+    gemv_job j;
+    memset(&j, 0, sizeof j);
+    j.fp8 = 3; j.nib = nib; j.gsc = sc; j.x = x; j.N = N; j.M = M; j.K = K;
+    j.rows = rows; j.nrows = rows ? nrows : M; j.y = y; j.a = a;
+    gemv_run(&j, threads);
+}
+
 void vgo_gemv_fp8(const uint8_t *q, const float *rs,
                   const uint16_t *x, int N, int64_t M, int64_t K,
                   const int64_t *rows, int64_t nrows,
@@ -355,6 +385,106 @@ int64_t vgo_check(const uint16_t *y, const double *yref, const double *a,
     if (worst)
         *worst = w;
     return bad;
+}
+
+/* --------------------------------------------------------- other formats */
+
+double vgo_e8m0_value(int byte)
+{
+    if (byte == 255)
+        return NAN;
+    return ldexp(1.0, byte - 127);
+}
+
+int vgo_mxfp8_quantise(const float *W, int64_t M, int64_t K, uint8_t *q, uint8_t *sc)
+{
+    int64_t m, b;
+    if (!all_finite(W, M * K))
+        return -1;
+    for (m = 0; m < M; ++m) {
+        for (b = 0; b < K / 32; ++b) {
+            const float *w = W + m * K + b * 32;
+            float amax = 0.0f, X;
+            int e, ex, j;
+            for (j = 0; j < 32; ++j)
+                if (fabsf(w[j]) > amax)
+                    amax = fabsf(w[j]);
+            if (amax == 0.0f) {
+                e = 127;
+            } else {
+                frexp((double)amax, &ex);         /* amax in [2^(ex-1), 2^ex) */
+                e = (ex - 1) - 8 + 127;           /* floor(log2 amax) - emax(E4M3) */
+                if (e < 10)
+                    e = 10;
+                if (e > 134)
+                    e = 134;
+            }
+            sc[m * (K / 32) + b] = (uint8_t)e;
+            X = (float)ldexp(1.0, e - 127);       /* exact */
+            for (j = 0; j < 32; ++j)
+                q[m * K + b * 32 + j] = (uint8_t)vgo_e4m3_encode(w[j] / X);
+        }
+    }
+    return 0;
+}
+
+int vgo_int4g_quantise(const float *W, int64_t M, int64_t K, uint8_t *nib, uint16_t *sc)
+{
+    int64_t m, b;
+    if (!all_finite(W, M * K))
+        return -1;
+    memset(nib, 0, (size_t)(M * (K / 2)));
+    for (m = 0; m < M; ++m) {
+        for (b = 0; b < K / 128; ++b) {
+            const float *w = W + m * K + b * 128;
+            float amax = 0.0f, s;
+            uint16_t sbits;
+            int j;
+            for (j = 0; j < 128; ++j)
+                if (fabsf(w[j]) > amax)
+                    amax = fabsf(w[j]);
+            sbits = vgo_bf16_round((double)(amax / 7.0f));   /* FP32 division, then BF16 */
+            sc[m * (K / 128) + b] = sbits;
+            s = (float)vgo_bf16_value(sbits);
+            for (j = 0; j < 128; ++j) {
+                int code = 8;
+                if (s != 0.0f) {
+                    float r = nearbyintf(w[j] / s);       /* ties to even */
+                    if (r < -8.0f)
+                        r = -8.0f;
+                    if (r > 7.0f)
+                        r = 7.0f;
+                    code = (int)r + 8;
+                }
+                {
+                    int64_t k = b * 128 + j;
+                    uint8_t *p = nib + m * (K / 2) + k / 2;
+                    *p = (uint8_t)(*p | ((k & 1) ? code << 4 : code));
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+void vgo_mxfp8_dequant(const uint8_t *q, const uint8_t *sc, int64_t M, int64_t K, double *What)
+{
+    int64_t m, k;
+    for (m = 0; m < M; ++m)
+        for (k = 0; k < K; ++k)
+            What[m * K + k] = vgo_e4m3_value(q[m * K + k]) * vgo_e8m0_value(sc[m * (K / 32) + k / 32]);
+}
+
+void vgo_int4g_dequant(const uint8_t *nib, const uint16_t *sc, int64_t M, int64_t K,
+                       double *What)
+{
+    int64_t m, k;
+    for (m = 0; m < M; ++m)
+        for (k = 0; k < K; ++k) {
+            uint8_t byte = nib[m * (K / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            What[m * K + k] = (double)(code - 8) * vgo_bf16_value(sc[m * (K / 128) + k / 128]);
+        }
 }
 
 /* ------------------------------------------------------ fused neighbours */

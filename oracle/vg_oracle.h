@@ -86,6 +86,49 @@ void vgo_gemv_fp8(const uint8_t *q, const float *rs,
                   const int64_t *rows, int64_t nrows,
                   double *y, double *a, int threads);
 
+/* ------------------------------------------------------ other formats
+ * Two more weight formats the pages name next to NVFP4 and FP8: MXFP8
+ * (crit README, Kernels section: cuBLASLt's block-scaled MXFP8) and
+ * groupwise integer weights (NInfer README, model table: "groupwise-int"
+ * artifacts; crit README, Kernels section: Marlin's 4-bit weights in
+ * GPTQ-style groups against 16-bit activations).  The pages define neither;
+ * the readings are the plain public ones:
+ *   MXFP8 (OCP Microscaling): E4M3 elements, one E8M0 scale 2^(e-127) per
+ *     32 consecutive K elements; quantisation takes the shared exponent
+ *     floor(log2(block amax)) - 8 (8 = the largest E4M3 exponent), scale
+ *     byte e = that + 127 limited to 10..134 (scales 2^-117..2^7, the range
+ *     in which every scaled element is a normal BF16 value), a zero block
+ *     gets e = 127; codes are E4M3(w / 2^(e-127)) rounded to nearest even
+ *     with saturation.
+ *   groupwise-int ("int4-g128"): 4-bit codes q in 0..15 with the zero point
+ *     8, one BF16 scale s per 128 consecutive K elements of a row,
+ *     w = (q - 8) * s; quantisation s = bf16(amax / 7) (FP32 division, one
+ *     rounding to BF16), q = clamp(rne(w / s), -8, 7) + 8 (all 8 when
+ *     s == 0). */
+
+/* Value of an E8M0 scale byte: 2^(e-127); 0xFF is NaN. */
+double vgo_e8m0_value(int byte);
+
+/* MXFP8 quantisation, K % 32 == 0: q[M][K] E4M3 bytes, sc[M][K/32] E8M0
+ * bytes.  Returns 0, or -1 if W holds a NaN/Inf. */
+int vgo_mxfp8_quantise(const float *W, int64_t M, int64_t K, uint8_t *q, uint8_t *sc);
+
+/* Groupwise INT4 quantisation, K % 128 == 0: nib[M][K/2] (low nibble =
+ * even k), sc[M][K/128] BF16 bits.  Returns 0, or -1 on NaN/Inf. */
+int vgo_int4g_quantise(const float *W, int64_t M, int64_t K, uint8_t *nib, uint16_t *sc);
+
+void vgo_mxfp8_dequant(const uint8_t *q, const uint8_t *sc, int64_t M, int64_t K, double *What);
+void vgo_int4g_dequant(const uint8_t *nib, const uint16_t *sc, int64_t M, int64_t K,
+                       double *What);
+
+/* The GEMV of vgo_gemv_nvfp4 for these formats (same outputs). */
+void vgo_gemv_mxfp8(const uint8_t *q, const uint8_t *sc, const uint16_t *x, int N, int64_t M,
+                    int64_t K, const int64_t *rows, int64_t nrows, double *y, double *a,
+                    int threads);
+void vgo_gemv_int4g(const uint8_t *nib, const uint16_t *sc, const uint16_t *x, int N, int64_t M,
+                    int64_t K, const int64_t *rows, int64_t nrows, double *y, double *a,
+                    int threads);
+
 /* ------------------------------------------------- fused neighbours
  * Operations that sit next to the GEMV in a layer and that the verify pass
  * can run in the same launch (engine card, Checks section: the operator

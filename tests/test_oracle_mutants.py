@@ -42,6 +42,14 @@ MUTANTS = {
                                "* inv);"),
     "bf16 round ties away": ("r = nearbyint(a / q) * q;", "r = floor(a / q + 0.5) * q;"),
     "bf16 subnormal spacing": ("ex = -125;", "ex = -124;"),
+    "e8m0 bias": ("return ldexp(1.0, byte - 127);", "return ldexp(1.0, byte - 126);"),
+    "mxfp8 element max exponent": ("e = (ex - 1) - 8 + 127;", "e = (ex - 1) - 7 + 127;"),
+    "mxfp8 block index": ("vgo_e8m0_value(j->sc[m * (j->K / 32) + k / 32])",
+                          "vgo_e8m0_value(j->sc[m * (j->K / 32) + k / 64])"),
+    "int4 zero point": ("(double)(code - 8) * vgo_bf16_value(j->gsc", "(double)(code - 7) * vgo_bf16_value(j->gsc"),
+    "int4 scale divisor": ("(double)(amax / 7.0f)", "(double)(amax / 8.0f)"),
+    "int4 group index": ("vgo_bf16_value(j->gsc[m * (j->K / 128) + k / 128])",
+                         "vgo_bf16_value(j->gsc[m * (j->K / 128) + k / 256])"),
     "e4m3 saturation": ("if (a >= 448.0)\n        return sign | 0x7E;",
                         "if (a >= 480.0)\n        return sign | 0x7F;"),
 }

@@ -538,3 +538,119 @@ def test_rmsnorm_closed_forms(orc):
     a = orc.rmsnorm(x.view(torch.int16).numpy().view(np.uint16), gb, 0.0)
     b = orc.rmsnorm((x * 8).view(torch.int16).numpy().view(np.uint16), gb, 0.0)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------- other formats
+
+def test_e8m0_values(orc):
+    """E8M0 is a bare exponent: 2^(e-127), 0xFF NaN (OCP Microscaling)."""
+    assert orc.e8m0_value(127) == 1.0
+    assert orc.e8m0_value(0) == 2.0 ** -127
+    assert orc.e8m0_value(254) == 2.0 ** 127
+    assert orc.e8m0_value(130) == 8.0
+    assert math.isnan(orc.e8m0_value(255))
+
+
+def test_mxfp8_quantiser_decisions(orc):
+    """Per 32-block: the scale puts the block amax in [256, 512) (shared
+    exponent floor(log2 amax) - 8) unless the scale range clamps it; every
+    code is the nearest E4M3 value to w / X by brute force over all finite
+    codes, ties to the even code, saturating at 448; a zero block gets
+    scale 1 and zero codes."""
+    rng = np.random.default_rng(21)
+    W = (rng.standard_normal((6, 256)) * rng.choice([1e-3, 0.02, 3.0, 1e3], (6, 1))) \
+        .astype(np.float32)
+    W[1, 32:64] = 0.0
+    q, sc = orc.mxfp8_quantise(W)
+    finite = [(orc.e4m3_value(c), c) for c in range(256) if not math.isnan(orc.e4m3_value(c))]
+    for m in range(6):
+        for b in range(8):
+            blk = W[m, 32 * b:32 * b + 32]
+            e = int(sc[m, b])
+            amax = float(np.abs(blk).max())
+            if amax == 0:
+                assert e == 127 and not q[m, 32 * b:32 * b + 32].any()
+                continue
+            X = 2.0 ** (e - 127)
+            if 10 < e < 134:
+                assert 256 <= amax / X < 512
+            for j in range(32):
+                v = float(np.float32(blk[j]) / np.float32(X))
+                best = min(finite, key=lambda t: (abs(t[0] - v), t[1] & 1))
+                want = best[1] if abs(v) < 448 else (0x7E | (0x80 if v < 0 else 0))
+                if best[0] == 0 and v < 0:
+                    want = 0x80
+                assert q[m, 32 * b + j] == want, (m, b, j, v)
+
+
+def test_mxfp8_textbook_reduction(orc):
+    """With every scale byte 127 (X = 1) the product is plain FP8: numpy
+    x @ e4m3(q).T in float64, exactly; other scale bytes multiply their
+    32-block by 2^(e-127)."""
+    rng = np.random.default_rng(22)
+    M, K, N = 5, 128, 3
+    q = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0
+    sc = np.full((M, K // 32), 127, np.uint8)
+    x = torch.from_numpy(rng.standard_normal((N, K))).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    y, _ = orc.gemv_mxfp8(q, sc, xb)
+    Wd = np.vectorize(orc.e4m3_value)(q)
+    assert np.array_equal(y, x.double().numpy() @ Wd.T)
+    assert np.array_equal(orc.mxfp8_dequant(q, sc, M, K), Wd)
+    pw = rng.integers(-4, 5, (M, K // 32))
+    sc = (127 + pw).astype(np.uint8)
+    Ws = Wd * np.repeat(2.0 ** pw, 32, axis=1)
+    assert np.array_equal(orc.mxfp8_dequant(q, sc, M, K), Ws)
+    y, _ = orc.gemv_mxfp8(q, sc, xb)
+    assert np.array_equal(y, x.double().numpy() @ Ws.T)
+
+
+def test_int4g_quantiser_decisions(orc):
+    """Per 128-group: the scale is BF16(amax / 7); each code is the integer
+    nearest to w / s (ties to even) clamped to -8..7, plus the zero point 8,
+    by brute force over the 16 codes; a zero group stores scale 0 and 8s."""
+    rng = np.random.default_rng(23)
+    W = (rng.standard_normal((4, 512)) * 0.02).astype(np.float32)
+    W[2, 128:256] = 0.0
+    W[3, 5] = 1.0                     # one large value: most of its group rounds to 0
+    nib, sc = orc.int4g_quantise(W)
+    codes = np.empty((4, 512), np.int64)
+    codes[:, 0::2] = nib & 15
+    codes[:, 1::2] = nib >> 4
+    for m in range(4):
+        for g in range(4):
+            blk = W[m, 128 * g:128 * g + 128]
+            s = orc.bf16_value(int(sc[m, g]))
+            amax = np.float32(np.abs(blk).max())
+            assert sc[m, g] == orc.bf16_round(float(amax / np.float32(7.0)))
+            for j in range(128):
+                if s == 0:
+                    assert codes[m, 128 * g + j] == 8
+                    continue
+                r = float(np.float32(blk[j]) / np.float32(s))
+                best = min(range(-8, 8), key=lambda c: (abs(c - r), c & 1))
+                assert codes[m, 128 * g + j] == best + 8, (m, g, j, r)
+
+
+def test_int4g_textbook_reduction(orc):
+    """With power-of-two group scales the weights are the integers q - 8
+    times each group's scale, and the product is numpy x @ W.T in float64,
+    exactly (a scale of 1 everywhere gives the plain integer product)."""
+    rng = np.random.default_rng(24)
+    M, K, N = 4, 512, 3
+    nib = rng.integers(0, 256, (M, K // 2)).astype(np.uint8)
+    x = torch.from_numpy(rng.standard_normal((N, K))).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    Wi = np.empty((M, K))
+    Wi[:, 0::2] = (nib & 15).astype(np.int64) - 8
+    Wi[:, 1::2] = (nib >> 4).astype(np.int64) - 8
+    sc = np.full((M, K // 128), 0x3F80, np.uint16)          # 1.0
+    y, _ = orc.gemv_int4g(nib, sc, xb)
+    assert np.array_equal(y, x.double().numpy() @ Wi.T)
+    pw = rng.integers(-3, 4, (M, K // 128))
+    sc = (0x3F80 + (pw << 7)).astype(np.uint16)             # 2^pw
+    Ws = Wi * np.repeat(2.0 ** pw, 128, axis=1)
+    assert np.array_equal(orc.int4g_dequant(nib, sc, M, K), Ws)
+    y, _ = orc.gemv_int4g(nib, sc, xb)
+    assert np.array_equal(y, x.double().numpy() @ Ws.T)
