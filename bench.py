@@ -390,6 +390,23 @@ def run_ours(args, world, rank, local):
         del ds
         torch.cuda.empty_cache()
 
+    # the same stack with every matrix in MXFP8, then in groupwise INT4
+    format_stacks = None
+    if not args.no_configs and args.layers == 64:
+        format_stacks = {}
+        for f in ("mxfp8", "int4g"):
+            fst = build_stack(args.N, device=dev, all_fmt=f)
+            fpl = fst.plan(ordered=True)
+            ms, per_s = timed(fpl.run, args.steps, args.warmup)
+            if fpl.check() != 0:
+                raise RuntimeError("format stack reported a device error")
+            fpl.close()
+            med = statistics.median(per_s)
+            format_stacks[f] = {"bytes": fst.bytes, "us_per_pass": round(1e3 * med, 1),
+                                "GBps": round(fst.bytes / (med / 1e3) / 1e9, 1)}
+            del fst
+            torch.cuda.empty_cache()
+
     # the same stack with its neighbours fused in and real dependencies:
     # RMS norm -> q,k,v (x = the norm's y); o; RMS norm -> gate+up with the
     # gated activation -> down (x = the activation's y); final norm -> head
@@ -503,6 +520,7 @@ def run_ours(args, world, rank, local):
                          "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
             "per_width": widths, **extra,
             "per_config": configs, "draft_step": draft, "fused_stack": fused,
+            "format_stacks": format_stacks,
             "sustained": sustained,
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
         }
@@ -519,15 +537,19 @@ SINGLE = {
     "down": ("row-scaled FP8 down 5120x17408, seed 3", ["down"]),
     "head": ("NVFP4 head 151936x5120, seed 3", ["head"]),
 }
-# the single-product configurations and the widths each is quoted at
+# the single-product configurations and the widths each is quoted at; the
+# last entries time the same shapes in the other weight formats
 PER_CONFIG = [("tiny", (1,)), ("proj", (1,)), ("gateup", (1, 2, 4, 8)), ("down", (1, 8)),
-              ("head", (1, 8))]
+              ("head", (1, 8)), ("proj", (8,), "mxfp8"), ("proj", (8,), "int4g"),
+              ("gateup", (8,), "mxfp8"), ("gateup", (8,), "int4g"), ("head", (8,), "mxfp8"),
+              ("head", (8,), "int4g")]
 
 
-def time_single(workload: str, N: int, steps: int, warmup: int, flush):
+def time_single(workload: str, N: int, steps: int, warmup: int, flush, fmt=None):
     """One configuration's product, timed alone: L2 flushed (a 512 MB write)
-    before every launch, CUDA events around each launch only.  Returns
-    (bytes, per-launch ms list, launches per step)."""
+    before every launch, CUDA events around each launch only; fmt: the
+    weights in that format instead of the configuration's.  Returns (bytes,
+    per-launch ms list)."""
     import torch
 
     import verify_gemm_gb300 as vg
@@ -540,7 +562,9 @@ def time_single(workload: str, N: int, steps: int, warmup: int, flush):
     for m, W in zip(WORKLOADS[key].mats, Ws):
         if m.name not in names:
             continue
-        wt = vg.nvfp4_pack(W) if m.fmt == "nvfp4" else vg.fp8_pack(W)
+        from verify_gemm_gb300.workloads import pack
+
+        wt = pack(W, fmt or m.fmt)
         y = torch.empty((N, m.M), dtype=torch.bfloat16, device="cuda")
         entries.append((wt, xs[m.K], y, 0))
     del Ws
@@ -616,11 +640,11 @@ def per_config(steps: int, warmup: int):
 
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     out = {}
-    for wl, widths in PER_CONFIG:
+    for wl, widths, *fmt in PER_CONFIG:
         for N in widths:
-            nbytes, ms = time_single(wl, N, steps, warmup, flush)
+            nbytes, ms = time_single(wl, N, steps, warmup, flush, *fmt)
             med = statistics.median(ms)
-            out[f"{wl} N={N}"] = {"us": round(1e3 * med, 2),
+            out[f"{wl}{' ' + fmt[0] if fmt else ''} N={N}"] = {"us": round(1e3 * med, 2),
                                   "us_p10_p90": [round(1e3 * q, 2) for q in pcts(ms, (10, 90))],
                                   "GBps": round(nbytes / (med / 1e3) / 1e9, 1), "bytes": nbytes}
             torch.cuda.empty_cache()

@@ -83,8 +83,13 @@ typedef enum vg_status {
     VG_ERR_WORKSPACE = 6      /* workspace missing or too small */
 } vg_status;
 
-/* Weight formats of vg_matrix_desc.format. */
-enum { VG_FMT_NVFP4 = 0, VG_FMT_FP8_ROWSCALE = 1 };
+/* Weight formats of vg_matrix_desc.format.
+ *   VG_FMT_MXFP8: E4M3 codes, one E8M0 scale 2^(e-127) per 32 elements along
+ *     K (e limited to 10..134), K % 256 == 0.
+ *   VG_FMT_INT4G: 4-bit codes q with zero point 8 and one BF16 scale s per
+ *     128 elements along K of a row, w = (q - 8) * s, K % 512 == 0.
+ * These two take x by tensor copy only (see vg_gemv_nvfp4). */
+enum { VG_FMT_NVFP4 = 0, VG_FMT_FP8_ROWSCALE = 1, VG_FMT_MXFP8 = 2, VG_FMT_INT4G = 3 };
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *vg_status_string(vg_status s);
@@ -166,6 +171,48 @@ vg_status vg_nvfp4_from_canonical(const uint8_t *nib, const uint8_t *sc,
 vg_status vg_fp8_from_canonical(const uint8_t *q, int64_t M, int64_t K, void *w_out,
                                 vg_stream_t stream);
 
+/* ------------------------------------------- MXFP8 and groupwise INT4
+ * Two more weight formats next to NVFP4 and row-scaled FP8: MXFP8, the OCP
+ * Microscaling FP8 format that cuBLASLt takes block-scaled (crit README,
+ * Kernels section), and groupwise 4-bit integers, the "groupwise-int"
+ * artifacts of the NInfer README (model table) and the 4-bit GPTQ-style
+ * groups of Marlin (crit README, Kernels section).
+ * Canonical forms:
+ *   MXFP8: q[M][K] E4M3 bytes, sc[M][K/32] E8M0 bytes (2^(e-127)).
+ *   INT4G: nib[M][K/2] codes 0..15 (low nibble = even k),
+ *          sc[M][K/128] BF16 bits; w = (q - 8) * s.
+ * Quantisation (FP32 IEEE steps):
+ *   MXFP8: per 32-block e = floor(log2(amax)) - 8 + 127 limited to
+ *          10..134 (a zero block: 127); q = E4M3(w / 2^(e-127)), nearest
+ *          even, saturating.
+ *   INT4G: per 128-group s = BF16(amax / 7) (nearest even); q =
+ *          clamp(nearest-even integer of w / s, -8, 7) + 8 (8 when s == 0).
+ * Sizes of the packed code and scale buffers for any format. */
+vg_status vg_weight_sizes(int format, int64_t M, int64_t K, size_t *w_bytes,
+                          size_t *scale_bytes);
+
+/* Quantise an FP32 matrix (device [M][K]) into the packed layout.
+ * Synchronises once; NaN/Inf gives VG_ERR_INVALID_ARG; K not a multiple of
+ * 256 (MXFP8) or 512 (INT4G) gives VG_ERR_UNSUPPORTED. */
+vg_status vg_mxfp8_pack(const float *W, int64_t M, int64_t K, void *w_out, void *scales_out,
+                        vg_stream_t stream);
+vg_status vg_int4g_pack(const float *W, int64_t M, int64_t K, void *w_out, void *scales_out,
+                        vg_stream_t stream);
+
+/* Packed -> canonical (device). */
+vg_status vg_mxfp8_unpack(const void *w, const void *scales, int64_t M, int64_t K,
+                          uint8_t *q_out, uint8_t *sc_out, vg_stream_t stream);
+vg_status vg_int4g_unpack(const void *w, const void *scales, int64_t M, int64_t K,
+                          uint8_t *nib_out, uint16_t *sc_out, vg_stream_t stream);
+
+/* Canonical -> packed (device).  MXFP8 scale bytes outside 10..134 give
+ * VG_ERR_UNSUPPORTED, NaN codes VG_ERR_INVALID_ARG; INT4G scales must be
+ * finite (else VG_ERR_INVALID_ARG).  Synchronise once. */
+vg_status vg_mxfp8_from_canonical(const uint8_t *q, const uint8_t *sc, int64_t M, int64_t K,
+                                  void *w_out, void *scales_out, vg_stream_t stream);
+vg_status vg_int4g_from_canonical(const uint8_t *nib, const uint16_t *sc, int64_t M, int64_t K,
+                                  void *w_out, void *scales_out, vg_stream_t stream);
+
 /* Gated pair packers for VG_OP_SWIGLU: the gate and up projections of an
  * MLP (each [I][K], I % 8 == 0) packed as one matrix of M = 2*I rows whose
  * every 16-row tile holds 8 gate rows and the same 8 up rows (tile j: gate
@@ -227,6 +274,18 @@ vg_status vg_gemv_nvfp4(const void *w, const void *scales, float gscale,
 vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale,
                                const uint16_t *x, int N, int64_t M, int64_t K, uint16_t *y,
                                void *workspace, size_t workspace_bytes, vg_stream_t stream);
+
+/* The GEMV for MXFP8 and groupwise-INT4 weights (arguments as
+ * vg_gemv_nvfp4, minus the tensor scale).  Every block scale is applied
+ * exactly: MXFP8 weights are decoded to BF16 with their power-of-two scale,
+ * INT4 weights q - 8 go through the MMAs unscaled and each group's FP32 sum
+ * is multiplied by its BF16 scale. */
+vg_status vg_gemv_mxfp8(const void *w, const void *scales, const uint16_t *x, int N, int64_t M,
+                        int64_t K, uint16_t *y, void *workspace, size_t workspace_bytes,
+                        vg_stream_t stream);
+vg_status vg_gemv_int4g(const void *w, const void *scales, const uint16_t *x, int N, int64_t M,
+                        int64_t K, uint16_t *y, void *workspace, size_t workspace_bytes,
+                        vg_stream_t stream);
 
 /* Largest workspace, in bytes, that vg_gemv_nvfp4_noalloc can serve. */
 #define VG_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
@@ -322,11 +381,11 @@ enum {
  *   only after the previous group has completed.  0 (default): x is ready
  *   before the pass starts and is copied ahead of the group order. */
 typedef struct vg_matrix_desc {
-    int32_t format;          /* VG_FMT_NVFP4 or VG_FMT_FP8_ROWSCALE */
+    int32_t format;          /* VG_FMT_* */
     int32_t group;           /* dependency group */
     int64_t M, K;
     const void *w;           /* device, packed codes */
-    const void *scales;      /* device, packed block scales (NVFP4), else NULL */
+    const void *scales;      /* device, packed block scales (NVFP4, MXFP8, INT4G), else NULL */
     const float *rowscale;   /* device FP32 [M] (FP8; SWIGLU: gate rows [I]), else NULL */
     float gscale;            /* tensor scale (NVFP4; SWIGLU: of the gate rows) */
     const uint16_t *x;       /* device BF16 [N][K] */

@@ -18,14 +18,16 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (VG_FMT_FP8_ROWSCALE, VG_FMT_NVFP4, VG_OP_GEMV, VG_OP_RMSNORM,  # noqa: F401
-                   VG_OP_SWIGLU, VGError)
+from ._lib import (VG_FMT_FP8_ROWSCALE, VG_FMT_INT4G, VG_FMT_MXFP8, VG_FMT_NVFP4,  # noqa: F401
+                   VG_OP_GEMV, VG_OP_RMSNORM, VG_OP_SWIGLU, VGError)
 
 __all__ = [
     "NVFP4Weight", "FP8Weight", "nvfp4_pack", "fp8_pack", "nvfp4_unpack", "fp8_unpack",
     "nvfp4_from_canonical", "fp8_from_canonical", "gemv", "workspace_for", "VerifyPlan",
     "VGError", "VG_FMT_NVFP4", "VG_FMT_FP8_ROWSCALE", "NVFP4GatedWeight", "FP8GatedWeight",
-    "nvfp4_pack_gated", "fp8_pack_gated", "RMSNorm",
+    "nvfp4_pack_gated", "fp8_pack_gated", "RMSNorm", "BlockScaledWeight", "mxfp8_pack",
+    "int4g_pack", "mxfp8_unpack", "int4g_unpack", "mxfp8_from_canonical",
+    "int4g_from_canonical", "VG_FMT_MXFP8", "VG_FMT_INT4G",
 ]
 
 
@@ -130,6 +132,96 @@ class RMSNorm:
     eps: float = 1e-6
     op: int = VG_OP_RMSNORM
     nbytes: int = 0          # no weights
+
+
+@dataclass
+class BlockScaledWeight:
+    """Packed MXFP8 (fmt VG_FMT_MXFP8) or groupwise INT4 (VG_FMT_INT4G) weight."""
+
+    w: torch.Tensor          # uint8, opaque packed codes
+    scales: torch.Tensor     # uint8, opaque packed block scales
+    M: int
+    K: int
+    fmt: int
+
+    @property
+    def nbytes(self) -> int:
+        """Algorithmic bytes: MXFP8 M*K codes + M*K/32 scales; INT4 M*K/2 codes +
+        2*M*K/128 scales."""
+        E = self.M * self.K
+        return E + E // 32 if self.fmt == VG_FMT_MXFP8 else E // 2 + 2 * (E // 128)
+
+
+def weight_sizes(fmt: int, M: int, K: int):
+    wb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _lib.check(_lib.vg_weight_sizes(fmt, M, K, ctypes.byref(wb), ctypes.byref(sb)),
+               "vg_weight_sizes")
+    return wb.value, sb.value
+
+
+def _block_pack(fmt, fn, W, stream):
+    _dev_tensor(W, torch.float32, "W")
+    M, K = W.shape
+    wb, sb = weight_sizes(fmt, M, K)
+    w = torch.empty(wb, dtype=torch.uint8, device=W.device)
+    sc = torch.empty(sb, dtype=torch.uint8, device=W.device)
+    _lib.check(fn(_ptr(W), M, K, _ptr(w), _ptr(sc), _stream(stream)), fn.__name__)
+    return BlockScaledWeight(w, sc, M, K, fmt)
+
+
+def mxfp8_pack(W: torch.Tensor, stream=None) -> BlockScaledWeight:
+    """MXFP8 quantisation (E4M3 codes, E8M0 scale per 32 along K; K % 256 == 0)."""
+    return _block_pack(VG_FMT_MXFP8, _lib.vg_mxfp8_pack, W, stream)
+
+
+def int4g_pack(W: torch.Tensor, stream=None) -> BlockScaledWeight:
+    """Groupwise INT4 quantisation (BF16 scale per 128 along K; K % 512 == 0)."""
+    return _block_pack(VG_FMT_INT4G, _lib.vg_int4g_pack, W, stream)
+
+
+def mxfp8_unpack(wt: BlockScaledWeight, stream=None):
+    """Packed -> canonical (q uint8 [M, K], sc uint8 [M, K/32]) on the device."""
+    q = torch.empty((wt.M, wt.K), dtype=torch.uint8, device=wt.w.device)
+    sc = torch.empty((wt.M, wt.K // 32), dtype=torch.uint8, device=wt.w.device)
+    _lib.check(_lib.vg_mxfp8_unpack(_ptr(wt.w), _ptr(wt.scales), wt.M, wt.K, _ptr(q), _ptr(sc),
+                                    _stream(stream)), "vg_mxfp8_unpack")
+    return q, sc
+
+
+def int4g_unpack(wt: BlockScaledWeight, stream=None):
+    """Packed -> canonical (nib uint8 [M, K/2], sc BF16 bits as int16 [M, K/128])."""
+    nib = torch.empty((wt.M, wt.K // 2), dtype=torch.uint8, device=wt.w.device)
+    sc = torch.empty((wt.M, wt.K // 128), dtype=torch.int16, device=wt.w.device)
+    _lib.check(_lib.vg_int4g_unpack(_ptr(wt.w), _ptr(wt.scales), wt.M, wt.K, _ptr(nib), _ptr(sc),
+                                    _stream(stream)), "vg_int4g_unpack")
+    return nib, sc
+
+
+def mxfp8_from_canonical(q: torch.Tensor, sc: torch.Tensor, stream=None) -> BlockScaledWeight:
+    _dev_tensor(q, torch.uint8, "q")
+    _dev_tensor(sc, torch.uint8, "sc")
+    M, K = q.shape
+    wb, sb = weight_sizes(VG_FMT_MXFP8, M, K)
+    w = torch.empty(wb, dtype=torch.uint8, device=q.device)
+    s = torch.empty(sb, dtype=torch.uint8, device=q.device)
+    _lib.check(_lib.vg_mxfp8_from_canonical(_ptr(q), _ptr(sc), M, K, _ptr(w), _ptr(s),
+                                            _stream(stream)), "vg_mxfp8_from_canonical")
+    return BlockScaledWeight(w, s, M, K, VG_FMT_MXFP8)
+
+
+def int4g_from_canonical(nib: torch.Tensor, sc: torch.Tensor, stream=None) -> BlockScaledWeight:
+    """sc: BF16 scale bits [M, K/128] as an int16 (or bfloat16) tensor."""
+    _dev_tensor(nib, torch.uint8, "nib")
+    if sc.dtype == torch.bfloat16:
+        sc = sc.view(torch.int16)
+    _dev_tensor(sc, torch.int16, "sc")
+    M, K = nib.shape[0], nib.shape[1] * 2
+    wb, sb = weight_sizes(VG_FMT_INT4G, M, K)
+    w = torch.empty(wb, dtype=torch.uint8, device=nib.device)
+    s = torch.empty(sb, dtype=torch.uint8, device=nib.device)
+    _lib.check(_lib.vg_int4g_from_canonical(_ptr(nib), _ptr(sc), M, K, _ptr(w), _ptr(s),
+                                            _stream(stream)), "vg_int4g_from_canonical")
+    return BlockScaledWeight(w, s, M, K, VG_FMT_INT4G)
 
 
 def nvfp4_sizes(M: int, K: int):
@@ -261,6 +353,11 @@ def gemv(wt, x: torch.Tensor, y: torch.Tensor | None = None, workspace=None, str
         s = _lib.vg_gemv_nvfp4(_ptr(wt.w), _ptr(wt.scales), wt.gscale, _ptr(x), N, wt.M, wt.K,
                                _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream))
         _lib.check(s, "vg_gemv_nvfp4")
+    elif wt.fmt in (VG_FMT_MXFP8, VG_FMT_INT4G):
+        fn = _lib.vg_gemv_mxfp8 if wt.fmt == VG_FMT_MXFP8 else _lib.vg_gemv_int4g
+        s = fn(_ptr(wt.w), _ptr(wt.scales), _ptr(x), N, wt.M, wt.K, _ptr(y), _ptr(workspace),
+               workspace.numel(), _stream(stream))
+        _lib.check(s, fn.__name__)
     else:
         s = _lib.vg_gemv_fp8_rowscale(_ptr(wt.w), _ptr(wt.rowscale), _ptr(x), N, wt.M, wt.K,
                                       _ptr(y), _ptr(workspace), workspace.numel(),
@@ -315,6 +412,8 @@ class VerifyPlan:
                 d.gscale = wt.gscale
                 if op == VG_OP_SWIGLU:
                     d.gscale_up = wt.gscale_up
+            elif wt.fmt in (VG_FMT_MXFP8, VG_FMT_INT4G):
+                d.scales = wt.scales.data_ptr()
             else:
                 d.rowscale = wt.rowscale.data_ptr()
                 if op == VG_OP_SWIGLU:

@@ -23,6 +23,8 @@ VG_ERR_TIMEOUT = 5
 VG_ERR_WORKSPACE = 6
 VG_FMT_NVFP4 = 0
 VG_FMT_FP8_ROWSCALE = 1
+VG_FMT_MXFP8 = 2
+VG_FMT_INT4G = 3
 VG_OP_GEMV = 0
 VG_OP_SWIGLU = 1
 VG_OP_RMSNORM = 2
@@ -64,6 +66,15 @@ SIGNATURES = {
     "vg_nvfp4_pack_gated": (st, [P, P, i64, i64, P, P, ctypes.POINTER(f32), P]),
     "vg_fp8_pack_gated": (st, [P, P, i64, i64, P, P, P, P]),
     "vg_fp8_from_canonical": (st, [P, i64, i64, P, P]),
+    "vg_weight_sizes": (st, [i32, i64, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+    "vg_mxfp8_pack": (st, [P, i64, i64, P, P, P]),
+    "vg_int4g_pack": (st, [P, i64, i64, P, P, P]),
+    "vg_mxfp8_unpack": (st, [P, P, i64, i64, P, P, P]),
+    "vg_int4g_unpack": (st, [P, P, i64, i64, P, P, P]),
+    "vg_mxfp8_from_canonical": (st, [P, P, i64, i64, P, P, P]),
+    "vg_int4g_from_canonical": (st, [P, P, i64, i64, P, P, P]),
+    "vg_gemv_mxfp8": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
+    "vg_gemv_int4g": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_workspace_size": (st, [i64, i64, i32, ctypes.POINTER(sz)]),
     "vg_gemv_nvfp4": (st, [P, P, f32, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_fp8_rowscale": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),

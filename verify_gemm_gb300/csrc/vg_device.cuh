@@ -116,13 +116,34 @@ __host__ __device__ inline int64_t code_offset(int64_t mt, int64_t u, int64_t MT
   return rb * rt * KU * ub + ci * tiles * iu * ub + (tl * cpi + cc) * (nui / cpi) * ub + uu * ub;
 }
 // Byte offset of the scales of chunk c of tile mt (same grouping; every
-// tile-chunk has kNvScaleChunkBytes of scales, also a K tail).
+// tile-chunk has scb bytes of scales, also a K tail).
 __host__ __device__ inline int64_t scale_offset(int64_t mt, int64_t c, int64_t MT, int64_t KC,
-                                                int64_t rt) {
+                                                int64_t rt, int64_t scb = kNvScaleChunkBytes) {
   const int64_t cpi = kBlockTiles / rt;
   const int64_t rb = mt / rt, tl = mt % rt, ci = c / cpi, cc = c % cpi;
   const int64_t tiles = (MT - rb * rt) < rt ? (MT - rb * rt) : rt;
-  return (rb * rt * KC + ci * tiles * cpi + tl * cpi + cc) * kNvScaleChunkBytes;
+  return (rb * rt * KC + ci * tiles * cpi + tl * cpi + cc) * scb;
+}
+
+// ------------------------------------------------ MXFP8 and groupwise INT4
+// MXFP8 codes use the FP8 units and chunks; its E8M0 scales (one per 32
+// columns) take 128 bytes per tile-chunk: for each (g, t / 2) eight bytes
+// [unit 0..3][row g, row g + 8], the block that lane (g, t) covers in
+// each unit.  Groupwise INT4 codes use the NVFP4 units and chunks (4 bits
+// per weight) with their own bit placement; its BF16 scales (one per 128
+// columns = 2 units) take 128 bytes per tile-chunk: for each g sixteen
+// bytes [group 0..3][row g, row g + 8].
+constexpr int kMxScaleChunkBytes = 128;
+constexpr int kI4ScaleChunkBytes = 128;
+constexpr int kI4GroupK = 128;
+// MXFP8 scale bytes that give normal BF16 weights in one multiply: the
+// decode multiplies the placed FP8 bits (e4m3 * 2^-120) by the BF16 value
+// 2^(e - 7), whose exponent field e + 120 must stay below 255.
+constexpr int kMxScaleMin = 10, kMxScaleMax = 134;
+// INT4 nibble of (row half ri, column ii of an MMA step) in a packed word:
+// register r = ri + 2 * (ii >> 1) holds it at bit 4 r of its ii & 1 half.
+__host__ __device__ constexpr int i4_bitpos(int ri, int ii) {
+  return 4 * (ri + 2 * (ii >> 1)) + 16 * (ii & 1);
 }
 
 // ------------------------------------------------------ decode constants
@@ -418,6 +439,42 @@ __device__ __forceinline__ void nv_decode(uint32_t w, uint32_t fg, uint32_t fg8,
 __device__ __forceinline__ uint32_t nv_scale_pair(uint32_t word, uint32_t byte) {
   const uint32_t dup = prmt(word, 0u, 0x4040u | (byte * 0x0101u));
   return dup * 16u + kScaleBias2;
+}
+
+// BF16x2 {2^(e-7), 2^(e-7)} of the MXFP8 scale byte e number `byte` of
+// `word`: exponent field e + 120.
+__device__ __forceinline__ uint32_t mx_scale_pair(uint32_t word, uint32_t byte) {
+  const uint32_t dup = prmt(word, 0u, 0x4040u | (byte * 0x0101u));
+  return dup * 128u + 0x3C003C00u;
+}
+
+// Two BF16x2 registers of one MXFP8 word: the FP8 placement, multiplied by
+// the block scale of row g (sg) and of row g + 8 (sg8); exact.
+__device__ __forceinline__ void mx_decode(uint32_t w, uint32_t sg, uint32_t sg8, uint32_t &ra,
+                                          uint32_t &rb) {
+  const uint32_t pa = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
+  const uint32_t pb = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
+  ra = bmul2(pa, sg);
+  rb = bmul2(pb, sg8);
+}
+
+// (a + b) on BF16x2 as a fused multiply-add by 1.0 (exact here).
+__device__ __forceinline__ uint32_t badd2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(b));
+  return d;
+}
+
+// Four BF16x2 A registers of one INT4 word: the nibbles of register r sit at
+// bits 4 r and 4 r + 16; OR-ed into 0x4300 (the BF16 128) they give 128 + q,
+// and adding -136 gives q - 8, exactly.
+__device__ __forceinline__ void i4_decode(uint32_t w, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                          uint32_t &a3) {
+  constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u, kMinus136 = 0xC308C308u;
+  a0 = badd2((w & kMask) | kMagic, kMinus136);
+  a1 = badd2(((w >> 4) & kMask) | kMagic, kMinus136);
+  a2 = badd2(((w >> 8) & kMask) | kMagic, kMinus136);
+  a3 = badd2(((w >> 12) & kMask) | kMagic, kMinus136);
 }
 
 // Two BF16x2 registers of one FP8 word (bytes 0,2 -> ra; bytes 1,3 -> rb).

@@ -74,6 +74,7 @@ struct MatDev {
   int rt, cpi;       // tiles per row block, chunks per item (16 / rt)
   int iu, KI;        // units per item (cpi * cu), items per row block
   int kfull;         // items wholly inside K
+  int scb;           // block-scale bytes per tile-chunk (0: none)
   int64_t rb_bytes;  // code bytes of a full row block (rt tiles x KU units)
   int item0;         // first item of this matrix within its phase
   const CUtensorMap *xmap;  // x as [K/64 units][N rows][64 columns], or nullptr
@@ -401,13 +402,79 @@ __device__ __forceinline__ void f8_chunk(uint32_t slot, int lane, uint32_t xs, i
   }
 }
 
+// A whole MXFP8 chunk (4 units of 1024 bytes, tensor-copied x) of this
+// lane's tile: the FP8 decode with each unit's block scales of rows g and
+// g + 8 in place of the FP8 restore constant.  scl: the lane's 8 scale bytes
+// [unit][row g, row g + 8].
+__device__ __forceinline__ void mx_chunk(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                         int xd, float (&acc)[kAcc][4]) {
+  const uint2 sw = lds64(scl);
+#pragma unroll
+  for (int u = 0; u < kF8ChunkUnits; ++u) {
+    const uint32_t word = u < 2 ? sw.x : sw.y;
+    const uint32_t sg = mx_scale_pair(word, uint32_t(u & 1) * 2u);
+    const uint32_t sg8 = mx_scale_pair(word, uint32_t(u & 1) * 2u + 1u);
+    const uint4 w0 = lds128(slot + u * kF8UnitBytes + lane * 32);
+    const uint4 w1 = lds128(slot + u * kF8UnitBytes + lane * 32 + 16);
+    const uint4 xa = lds128(xs + u * 1024), xb = lds128(xs + u * 1024 + xd);
+    uint32_t a0, a1, a2, a3;
+    mx_decode(w0.x, sg, sg8, a0, a1);
+    mx_decode(w0.y, sg, sg8, a2, a3);
+    mma_bf16(acc[0], a0, a1, a2, a3, xa.x, xa.y);
+    mx_decode(w0.z, sg, sg8, a0, a1);
+    mx_decode(w0.w, sg, sg8, a2, a3);
+    mma_bf16(acc[1 % kAcc], a0, a1, a2, a3, xa.z, xa.w);
+    mx_decode(w1.x, sg, sg8, a0, a1);
+    mx_decode(w1.y, sg, sg8, a2, a3);
+    mma_bf16(acc[2 % kAcc], a0, a1, a2, a3, xb.x, xb.y);
+    mx_decode(w1.z, sg, sg8, a0, a1);
+    mx_decode(w1.w, sg, sg8, a2, a3);
+    mma_bf16(acc[3 % kAcc], a0, a1, a2, a3, xb.z, xb.w);
+  }
+}
+
+// A whole groupwise-INT4 chunk (8 units = 4 groups of 128 columns,
+// tensor-copied x): per group the 8 MMAs of its two units run on integer
+// weights q - 8 (exact in BF16) into a fresh FP32 sum, which is then scaled
+// by the group's BF16 scales of rows g and g + 8 and added in.  scl: the
+// lane's 16 scale bytes [group][row g, row g + 8].
+__device__ __forceinline__ void i4_chunk(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                         int xd, float (&acc)[kAcc][4]) {
+  const uint4 sv = lds128(scl);
+  const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+  for (int grp = 0; grp < kNvChunkUnits / 2; ++grp) {
+    float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int u = 2 * grp + h;
+      const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
+      const uint4 xa = lds128(xs + u * 1024), xb = lds128(xs + u * 1024 + xd);
+      uint32_t a0, a1, a2, a3;
+      i4_decode(wv.x, a0, a1, a2, a3);
+      mma_bf16(t4, a0, a1, a2, a3, xa.x, xa.y);
+      i4_decode(wv.y, a0, a1, a2, a3);
+      mma_bf16(t4, a0, a1, a2, a3, xa.z, xa.w);
+      i4_decode(wv.z, a0, a1, a2, a3);
+      mma_bf16(t4, a0, a1, a2, a3, xb.x, xb.y);
+      i4_decode(wv.w, a0, a1, a2, a3);
+      mma_bf16(t4, a0, a1, a2, a3, xb.z, xb.w);
+    }
+    const float sg = __uint_as_float(sw[grp] << 16), sg8 = __uint_as_float(sw[grp] & 0xFFFF0000u);
+    acc[0][0] = fmaf(sg, t4[0], acc[0][0]);
+    acc[0][1] = fmaf(sg, t4[1], acc[0][1]);
+    acc[0][2] = fmaf(sg8, t4[2], acc[0][2]);
+    acc[0][3] = fmaf(sg8, t4[3], acc[0][3]);
+  }
+}
+
 // Byte offsets of item (rb, ci)'s codes and scales in m (of `tiles` tiles);
 // its tile-chunks follow one another in warp order.
 __device__ __forceinline__ int64_t item_code_off(const MatDev &m, int rb, int ci, int tiles) {
   return int64_t(rb) * m.rb_bytes + int64_t(ci) * tiles * m.iu * m.ub;
 }
 __device__ __forceinline__ int64_t item_scale_off(const MatDev &m, int rb, int ci, int tiles) {
-  return (int64_t(rb) * m.rt * m.KC + int64_t(ci) * tiles * m.cpi) * kNvScaleChunkBytes;
+  return (int64_t(rb) * m.rt * m.KC + int64_t(ci) * tiles * m.cpi) * m.scb;
 }
 
 // Items beyond the ring that the producer brings into L2 while the consumers
@@ -457,9 +524,9 @@ __device__ __forceinline__ bool producer_dep_wait(const Params &p, const MatDev 
           const int ft = min(fm.rt, fm.MT - f.rb * fm.rt);
           const int fu = min(fm.iu, fm.KU - f.c * fm.iu);
           bulk_prefetch_l2(fm.w + item_code_off(fm, f.rb, f.c, ft), uint32_t(ft * fu * fm.ub));
-          if (fm.fmt == VG_FMT_NVFP4)
+          if (fm.scb)
             bulk_prefetch_l2(fm.sc + item_scale_off(fm, f.rb, f.c, ft),
-                             uint32_t(ft * fm.cpi * kNvScaleChunkBytes));
+                             uint32_t(ft * fm.cpi * fm.scb));
         }
         for (int k = 0; k < np && f.valid; ++k) f.advance(mats, phases, p);
         ++ahead;
@@ -500,6 +567,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
   const uint16_t *xg = nullptr;
   const CUtensorMap *tmap = nullptr;
   int rt = 0, MT = 0, KU = 0, K = 0, iu = 0, tile_item_bytes = 0, rb_scale_chunks = 0, cpi = 0, ub = 0;
+  int scb = 0;
   int64_t rb_bytes = 0;
   while (q.valid) {
     // ---- the item's copies, worked out before its slot is free
@@ -509,7 +577,8 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
       is_norm = m.fmt == kFmtNorm;
       xdep = kFused && m.x_after && p.done && q.ph > 0;
       w = m.w;
-      sc = m.fmt == VG_FMT_NVFP4 ? m.sc : nullptr;
+      sc = m.scb ? m.sc : nullptr;
+      scb = m.scb;
       xg = m.x;
       tmap = p.mats ? m.xmap : (p.x0_tensor ? &p.xmap0 : nullptr);
       rt = m.rt;
@@ -526,7 +595,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     const int tiles = min(rt, MT - q.rb * rt);
     const int nu = min(iu, KU - q.c * iu);   // units per tile in this item
     const uint32_t code_bytes = uint32_t(tiles * nu * ub);
-    const uint32_t scale_bytes = sc ? uint32_t(tiles * cpi * kNvScaleChunkBytes) : 0u;
+    const uint32_t scale_bytes = sc ? uint32_t(tiles * cpi * scb) : 0u;
     const int k0 = q.c * iu * kUnitK;
     // x: one tensor copy of 8 rows x the item's units (rows >= N and units
     // past K read as zeros), else one bulk copy per row (one-chunk items)
@@ -534,7 +603,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
                                   : uint32_t(min(iu * kUnitK, K - k0) * 2 * N);
     const uint8_t *code_src = w + int64_t(q.rb) * rb_bytes + int64_t(q.c) * tiles * tile_item_bytes;
     const uint8_t *scale_src =
-        sc ? sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * kNvScaleChunkBytes : nullptr;
+        sc ? sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * scb : nullptr;
     const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
 
     // ---- x written by the previous phase of this pass: wait until that
@@ -557,9 +626,9 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
             const int ft = min(fm.rt, fm.MT - pf.rb * fm.rt);
             const int fu = min(fm.iu, fm.KU - pf.c * fm.iu);
             bulk_prefetch_l2(fm.w + item_code_off(fm, pf.rb, pf.c, ft), uint32_t(ft * fu * fm.ub));
-            if (fm.fmt == VG_FMT_NVFP4)
+            if (fm.scb)
               bulk_prefetch_l2(fm.sc + item_scale_off(fm, pf.rb, pf.c, ft),
-                               uint32_t(ft * fm.cpi * kNvScaleChunkBytes));
+                               uint32_t(ft * fm.cpi * fm.scb));
             pf.advance(mats, phases, p);
             ++pf_ahead;
           }
@@ -754,7 +823,7 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
     for (int h = 0; h < 2; ++h) {
       const int row = mt * kTileRows + g + 8 * h;
       if (row >= m.M) continue;
-      const float mult = m.fmt == VG_FMT_NVFP4 ? m.mult : __ldg(m.rowscale + row);
+      const float mult = m.fmt == VG_FMT_FP8_ROWSCALE ? __ldg(m.rowscale + row) : m.mult;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int nn = 2 * t + e;
@@ -1029,6 +1098,32 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
               par ^= 1u;
             }
           }
+        } else if (fmt == VG_FMT_MXFP8 || fmt == VG_FMT_INT4G) {
+          // these formats take whole chunks and tensor-copied x only, so
+          // this loop does all of their work
+          const bool mx = fmt == VG_FMT_MXFP8;
+          const uint32_t scl_l = kItemScaleOff + warp * kMxScaleChunkBytes +
+                                 (mx ? uint32_t(g * 2 + (t >> 1)) * 8u : uint32_t(g) * 16u);
+          for (; c < c_full; ++c) {
+            const uint32_t item = ring + s * kItemSlotBytes;
+            if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+              break;
+            if (mx)
+              mx_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc);
+            else
+              i4_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (++s == kSlots) {
+              s = 0;
+              par ^= 1u;
+            }
+          }
+          if (c < c_full) {          // a wait ran out: nothing else computes them
+            if (lane == 0) set_error(p.error, kErrFullWait);
+            aborted = true;
+          }
         } else {
           for (; c < c_full; ++c) {
             const uint32_t item = ring + s * kItemSlotBytes;
@@ -1059,7 +1154,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
             aborted = true;
           }
         }
-        if (!aborted && work) {
+        if (!aborted && work && fmt <= VG_FMT_FP8_ROWSCALE) {
           const uint32_t xs = xt ? item + xoff_t : (on ? item + xoff_r : xzero);
           const int xd = xt ? xd_t : 16, xu = xt ? 1024 : kUnitK * 2;
           // item c's first column; items past kfull (a K tail) have one chunk
@@ -1231,8 +1326,13 @@ MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, co
   m.K = int(K);
   m.MT = int(ceil_div(M, kTileRows));
   m.KU = int(ceil_div(K, kUnitK));
-  m.cu = fmt == VG_FMT_NVFP4 ? kNvChunkUnits : kF8ChunkUnits;
-  m.ub = fmt == VG_FMT_NVFP4 ? kNvUnitBytes : kF8UnitBytes;
+  // 4-bit formats: NVFP4 units and chunks; 8-bit formats: FP8 ones
+  const bool nib4 = fmt == VG_FMT_NVFP4 || fmt == VG_FMT_INT4G;
+  m.cu = nib4 ? kNvChunkUnits : kF8ChunkUnits;
+  m.ub = nib4 ? kNvUnitBytes : kF8UnitBytes;
+  m.scb = fmt == VG_FMT_NVFP4 ? kNvScaleChunkBytes
+        : fmt == VG_FMT_MXFP8 ? kMxScaleChunkBytes
+        : fmt == VG_FMT_INT4G ? kI4ScaleChunkBytes : 0;
   m.KC = int(ceil_div(m.KU, m.cu));
   m.rt = layout_rt(M, K, m.cu);
   m.cpi = kBlockTiles / m.rt;
@@ -1273,7 +1373,12 @@ int64_t algorithmic_bytes(const MatDev &m) {
   const int64_t E = int64_t(m.M) * m.K;
   // a gated pair carries the tensor scales of both halves
   const int64_t gs_bytes = m.op == VG_OP_SWIGLU ? 8 : 4;
-  return m.fmt == VG_FMT_NVFP4 ? E / 2 + E / 16 + gs_bytes : E + 4 * int64_t(m.M);
+  switch (m.fmt) {
+    case VG_FMT_NVFP4: return E / 2 + E / 16 + gs_bytes;
+    case VG_FMT_MXFP8: return E + E / 32;
+    case VG_FMT_INT4G: return E / 2 + 2 * (E / kI4GroupK);
+    default: return E + 4 * int64_t(m.M);
+  }
 }
 
 // Single-GEMV workspace: [header words | partial slots].
@@ -1338,8 +1443,9 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
                              int64_t((workspace_bytes - kWsHead) / (kPartialWords * sizeof(uint64_t)))));
   p.mat0 = m0;
   p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu) ? 1 : 0;
-  // items of several chunks take x by tensor copy only
-  if (!p.x0_tensor && m0.cpi > 1) return VG_ERR_UNSUPPORTED;
+  // items of several chunks, and the block-scaled formats, take x by tensor
+  // copy only
+  if (!p.x0_tensor && (m0.cpi > 1 || m0.fmt >= VG_FMT_MXFP8)) return VG_ERR_UNSUPPORTED;
   p.phase0.items = int(T);
   p.phase0.rbs = m0.RB;
   p.phase0.mat_begin = 0;
@@ -1369,7 +1475,7 @@ struct vg_verify_plan {
 
 extern "C" vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes) {
   if (vg_status s = check_mk(M, K)) return s;
-  if (!bytes || (format != VG_FMT_NVFP4 && format != VG_FMT_FP8_ROWSCALE)) return VG_ERR_INVALID_ARG;
+  if (!bytes || format < VG_FMT_NVFP4 || format > VG_FMT_INT4G) return VG_ERR_INVALID_ARG;
   int dev;
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
@@ -1406,6 +1512,39 @@ extern "C" vg_status vg_gemv_fp8_rowscale(const void *w, const float *rowscale, 
   if (!rowscale) return VG_ERR_INVALID_ARG;
   const MatDev m = make_mat(VG_FMT_FP8_ROWSCALE, M, K, w, nullptr, rowscale, 0.f, x, y);
   return gemv_common(m, N, workspace, workspace_bytes, stream);
+}
+
+// K of the block-scaled formats: whole chunks only, so that their items are
+// whole and run in the streaming loops (which also need the x tensor copy).
+static vg_status check_block_format(int fmt, int64_t K) {
+  if (fmt == VG_FMT_MXFP8 && K % (kF8ChunkUnits * kUnitK) != 0) return VG_ERR_UNSUPPORTED;
+  if (fmt == VG_FMT_INT4G && K % (kNvChunkUnits * kUnitK) != 0) return VG_ERR_UNSUPPORTED;
+  return VG_OK;
+}
+
+static vg_status gemv_block_scaled(int fmt, const void *w, const void *scales, const uint16_t *x,
+                                   int N, int64_t M, int64_t K, uint16_t *y, void *workspace,
+                                   size_t workspace_bytes, vg_stream_t stream) {
+  if (vg_status s = check_gemv_args(w, x, y, N, M, K)) return s;
+  if (vg_status s = check_block_format(fmt, K)) return s;
+  if (!scales) return VG_ERR_INVALID_ARG;
+  if (!aligned16(scales)) return VG_ERR_ALIGNMENT;
+  const MatDev m = make_mat(fmt, M, K, w, scales, nullptr, 1.0f, x, y);
+  return gemv_common(m, N, workspace, workspace_bytes, stream);
+}
+
+extern "C" vg_status vg_gemv_mxfp8(const void *w, const void *scales, const uint16_t *x, int N,
+                                   int64_t M, int64_t K, uint16_t *y, void *workspace,
+                                   size_t workspace_bytes, vg_stream_t stream) {
+  return gemv_block_scaled(VG_FMT_MXFP8, w, scales, x, N, M, K, y, workspace, workspace_bytes,
+                           stream);
+}
+
+extern "C" vg_status vg_gemv_int4g(const void *w, const void *scales, const uint16_t *x, int N,
+                                   int64_t M, int64_t K, uint16_t *y, void *workspace,
+                                   size_t workspace_bytes, vg_stream_t stream) {
+  return gemv_block_scaled(VG_FMT_INT4G, w, scales, x, N, M, K, y, workspace, workspace_bytes,
+                           stream);
 }
 
 extern "C" vg_status vg_gemv_workspace_check(void *workspace, size_t workspace_bytes,
@@ -1468,6 +1607,10 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
       } else if (d.format == VG_FMT_FP8_ROWSCALE) {
         if (!d.rowscale) return VG_ERR_INVALID_ARG;
         if (d.op == VG_OP_SWIGLU && !d.rowscale_up) return VG_ERR_INVALID_ARG;
+      } else if (d.format == VG_FMT_MXFP8 || d.format == VG_FMT_INT4G) {
+        if (!d.scales || d.op != VG_OP_GEMV) return VG_ERR_INVALID_ARG;
+        if (!aligned16(d.scales)) return VG_ERR_ALIGNMENT;
+        if (vg_status s = check_block_format(d.format, d.K)) return s;
       } else {
         return VG_ERR_INVALID_ARG;
       }
@@ -1531,7 +1674,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
     for (size_t i = 0; i < hm.size(); ++i) {
       if (hm[i].fmt == kFmtNorm) continue;   // no copies
       hm[i].xmap = make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].iu) ? plan->d_xmaps + i : nullptr;
-      if (!hm[i].xmap && hm[i].cpi > 1) untensored = true;
+      if (!hm[i].xmap && (hm[i].cpi > 1 || hm[i].fmt >= VG_FMT_MXFP8)) untensored = true;
     }
     e = cudaMemcpy(plan->d_xmaps, maps.data(), sizeof(CUtensorMap) * maps.size(),
                    cudaMemcpyHostToDevice);

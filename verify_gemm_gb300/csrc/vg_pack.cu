@@ -9,6 +9,7 @@
 // step is one IEEE operation (explicit _rn intrinsics, no contraction), so
 // the codes are bit-identical to any other correct implementation of the
 // same recipe.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -329,6 +330,245 @@ __global__ void f8_from_canonical_kernel(const uint8_t *__restrict__ q, Geom G,
   dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
 }
 
+// ------------------------------------------- MXFP8 and groupwise INT4
+// One thread per (tile, unit, lane), as above.  MXFP8 codes sit in the FP8
+// layout; a lane with even t also writes the E8M0 bytes of the 32-block its
+// 16 columns belong to (rows g and g + 8).  INT4 codes sit in NVFP4 units
+// at i4_bitpos (padding codes are 8, the zero); the lane with t == 0 of an
+// even unit writes the group's BF16 scales.
+
+// Byte of the MXFP8 scale of (row half ri) for lane (g, t) in unit u of a
+// tile-chunk whose scales start at `base`.
+__device__ __forceinline__ int64_t mx_scale_at(int64_t base, int g, int t, int64_t u, int ri) {
+  return base + (g * 2 + (t >> 1)) * 8 + (u % kF8ChunkUnits) * 2 + ri;
+}
+// Byte of the INT4 group scale (2 bytes, BF16) of (row half ri) for row
+// group g in unit u of a tile-chunk whose scales start at `base`.
+__device__ __forceinline__ int64_t i4_scale_at(int64_t base, int g, int64_t u, int ri) {
+  return base + g * 16 + ((u % kNvChunkUnits) / 2) * 4 + ri * 2;
+}
+
+// floor(log2(amax)) - 8 + 127 from the FP32 exponent field, limited to the
+// supported scale bytes; a zero block gets 127.
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+  if (amax == 0.0f) return 127u;
+  const int E = int((__float_as_uint(amax) >> 23) & 0xFFu);   // 0 for subnormal amax
+  const int e = E == 0 ? kMxScaleMin : E - 8;
+  return uint32_t(min(max(e, kMxScaleMin), kMxScaleMax));
+}
+
+__global__ void mx_pack_kernel(const float *__restrict__ W, Geom G, uint8_t *__restrict__ w_out,
+                               uint8_t *__restrict__ sc_out) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= G.MT * G.KU * 32) return;
+  const int lane = int(idx & 31);
+  const int64_t u = (idx >> 5) % G.KU, mt = (idx >> 5) / G.KU;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t k0 = u * kUnitK + 16 * t;
+  const int64_t sbase = scale_offset(mt, u / kF8ChunkUnits, G.MT, G.KC, G.rt, kMxScaleChunkBytes);
+  uint8_t out[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) out[i] = 0;
+  for (int ri = 0; ri < 2; ++ri) {
+    const int64_t row = mt * kTileRows + g + 8 * ri;
+    if (row >= G.M || k0 >= G.K) continue;
+    const float *blk = W + row * G.K + (k0 & ~int64_t(31));
+    uint32_t bm = 0;
+    for (int j = 0; j < 32; ++j) bm = max(bm, abs_bits(blk[j]));
+    const uint32_t e = mx_scale_byte(__uint_as_float(bm));
+    const float X = __uint_as_float(e << 23);                // 2^(e - 127), exact
+    const float *w = W + row * G.K + k0;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk)
+      out[f8_byte(ri, kk >> 2, kk & 3)] = uint8_t(e4m3_rn_sat(__fdiv_rn(w[kk], X)));
+    if ((t & 1) == 0) sc_out[mx_scale_at(sbase, g, t, u, ri)] = uint8_t(e);
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(
+      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes, G.rt) + lane * 32);
+  dst[0] = *reinterpret_cast<const uint4 *>(out);
+  dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
+}
+
+__global__ void mx_unpack_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sc,
+                                 Geom G, uint8_t *__restrict__ q, uint8_t *__restrict__ scc) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= G.MT * G.KU * 32) return;
+  const int lane = int(idx & 31);
+  const int64_t u = (idx >> 5) % G.KU, mt = (idx >> 5) / G.KU;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t k0 = u * kUnitK + 16 * t;
+  if (k0 >= G.K) return;
+  const int64_t sbase = scale_offset(mt, u / kF8ChunkUnits, G.MT, G.KC, G.rt, kMxScaleChunkBytes);
+  uint8_t in[32];
+  const uint4 *src = reinterpret_cast<const uint4 *>(
+      w + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes, G.rt) + lane * 32);
+  *reinterpret_cast<uint4 *>(in) = src[0];
+  *reinterpret_cast<uint4 *>(in + 16) = src[1];
+  for (int ri = 0; ri < 2; ++ri) {
+    const int64_t row = mt * kTileRows + g + 8 * ri;
+    if (row >= G.M) continue;
+    uint8_t o[16];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) o[kk] = in[f8_byte(ri, kk >> 2, kk & 3)];
+    *reinterpret_cast<uint4 *>(q + row * G.K + k0) = *reinterpret_cast<const uint4 *>(o);
+    if ((t & 1) == 0) scc[row * (G.K / 32) + k0 / 32] = sc[mx_scale_at(sbase, g, t, u, ri)];
+  }
+}
+
+__global__ void mx_from_canonical_kernel(const uint8_t *__restrict__ q,
+                                         const uint8_t *__restrict__ scc, Geom G,
+                                         uint8_t *__restrict__ w_out,
+                                         uint8_t *__restrict__ sc_out) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= G.MT * G.KU * 32) return;
+  const int lane = int(idx & 31);
+  const int64_t u = (idx >> 5) % G.KU, mt = (idx >> 5) / G.KU;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t k0 = u * kUnitK + 16 * t;
+  const int64_t sbase = scale_offset(mt, u / kF8ChunkUnits, G.MT, G.KC, G.rt, kMxScaleChunkBytes);
+  uint8_t out[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) out[i] = 0;
+  for (int ri = 0; ri < 2; ++ri) {
+    const int64_t row = mt * kTileRows + g + 8 * ri;
+    if (row >= G.M || k0 >= G.K) continue;
+    uint8_t in[16];
+    *reinterpret_cast<uint4 *>(in) = *reinterpret_cast<const uint4 *>(q + row * G.K + k0);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) out[f8_byte(ri, kk >> 2, kk & 3)] = in[kk];
+    if ((t & 1) == 0) sc_out[mx_scale_at(sbase, g, t, u, ri)] = scc[row * (G.K / 32) + k0 / 32];
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(
+      w_out + code_offset(mt, u, G.MT, G.KU, kF8ChunkUnits, kF8UnitBytes, G.rt) + lane * 32);
+  dst[0] = *reinterpret_cast<const uint4 *>(out);
+  dst[1] = *reinterpret_cast<const uint4 *>(out + 16);
+}
+
+// Counts E8M0 bytes outside the supported range (in *bad) and NaN codes
+// (in bad[1]).
+__global__ void mx_check_canonical_kernel(const uint8_t *__restrict__ q, int64_t nq,
+                                          const uint8_t *__restrict__ sc, int64_t ns,
+                                          uint32_t *bad) {
+  uint32_t bs = 0, bq = 0;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < ns; i += stride)
+    bs += sc[i] < kMxScaleMin || sc[i] > kMxScaleMax;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq; i += stride)
+    bq += (q[i] & 0x7Fu) == 0x7Fu;
+  bs = __reduce_add_sync(0xFFFFFFFFu, bs);
+  bq = __reduce_add_sync(0xFFFFFFFFu, bq);
+  if ((threadIdx.x & 31) == 0) {
+    if (bs) atomicAdd(bad, bs);
+    if (bq) atomicAdd(bad + 1, bq);
+  }
+}
+
+__global__ void i4_pack_kernel(const float *__restrict__ W, Geom G, uint8_t *__restrict__ w_out,
+                               uint8_t *__restrict__ sc_out) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= G.MT * G.KU * 32) return;
+  const int lane = int(idx & 31);
+  const int64_t u = (idx >> 5) % G.KU, mt = (idx >> 5) / G.KU;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t k0 = u * kUnitK + 16 * t;
+  const int64_t sbase = scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC, G.rt, kI4ScaleChunkBytes);
+  uint32_t words[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};
+  for (int ri = 0; ri < 2; ++ri) {
+    const int64_t row = mt * kTileRows + g + 8 * ri;
+    if (row >= G.M || k0 >= G.K) continue;
+    const float *grp = W + row * G.K + (k0 & ~int64_t(kI4GroupK - 1));
+    uint32_t bm = 0;
+    for (int j = 0; j < kI4GroupK; ++j) bm = max(bm, abs_bits(grp[j]));
+    const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__uint_as_float(bm), 7.0f));
+    const float sv = __bfloat162float(sb);
+    const float *w = W + row * G.K + k0;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      uint32_t c = 8u;
+      if (sv != 0.0f) c = uint32_t(int(fminf(fmaxf(rintf(__fdiv_rn(w[kk], sv)), -8.0f), 7.0f)) + 8);
+      const int pos = i4_bitpos(ri, kk & 3);
+      words[kk >> 2] = (words[kk >> 2] & ~(0xFu << pos)) | (c << pos);
+    }
+    if (t == 0 && (u & 1) == 0)
+      *reinterpret_cast<__nv_bfloat16 *>(sc_out + i4_scale_at(sbase, g, u, ri)) = sb;
+  }
+  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes, G.rt) +
+                             lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+__global__ void i4_unpack_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sc,
+                                 Geom G, uint8_t *__restrict__ nib, uint16_t *__restrict__ scc) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= G.MT * G.KU * 32) return;
+  const int lane = int(idx & 31);
+  const int64_t u = (idx >> 5) % G.KU, mt = (idx >> 5) / G.KU;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t k0 = u * kUnitK + 16 * t;
+  if (k0 >= G.K) return;
+  const int64_t sbase = scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC, G.rt, kI4ScaleChunkBytes);
+  const uint4 v = *reinterpret_cast<const uint4 *>(
+      w + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes, G.rt) + lane * 16);
+  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+  for (int ri = 0; ri < 2; ++ri) {
+    const int64_t row = mt * kTileRows + g + 8 * ri;
+    if (row >= G.M) continue;
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint32_t c = (words[kk >> 2] >> i4_bitpos(ri, kk & 3)) & 15u;
+      if (kk < 8)
+        lo |= c << (4 * kk);
+      else
+        hi |= c << (4 * (kk - 8));
+    }
+    *reinterpret_cast<uint2 *>(nib + row * (G.K / 2) + k0 / 2) = make_uint2(lo, hi);
+    if (t == 0 && (u & 1) == 0)
+      scc[row * (G.K / kI4GroupK) + k0 / kI4GroupK] =
+          *reinterpret_cast<const uint16_t *>(sc + i4_scale_at(sbase, g, u, ri));
+  }
+}
+
+__global__ void i4_from_canonical_kernel(const uint8_t *__restrict__ nib,
+                                         const uint16_t *__restrict__ scc, Geom G,
+                                         uint8_t *__restrict__ w_out,
+                                         uint8_t *__restrict__ sc_out) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= G.MT * G.KU * 32) return;
+  const int lane = int(idx & 31);
+  const int64_t u = (idx >> 5) % G.KU, mt = (idx >> 5) / G.KU;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t k0 = u * kUnitK + 16 * t;
+  const int64_t sbase = scale_offset(mt, u / kNvChunkUnits, G.MT, G.KC, G.rt, kI4ScaleChunkBytes);
+  uint32_t words[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};
+  for (int ri = 0; ri < 2; ++ri) {
+    const int64_t row = mt * kTileRows + g + 8 * ri;
+    if (row >= G.M || k0 >= G.K) continue;
+    const uint2 c2 = *reinterpret_cast<const uint2 *>(nib + row * (G.K / 2) + k0 / 2);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint32_t c = ((kk < 8 ? c2.x : c2.y) >> (4 * (kk & 7))) & 15u;
+      const int pos = i4_bitpos(ri, kk & 3);
+      words[kk >> 2] = (words[kk >> 2] & ~(0xFu << pos)) | (c << pos);
+    }
+    if (t == 0 && (u & 1) == 0)
+      *reinterpret_cast<uint16_t *>(sc_out + i4_scale_at(sbase, g, u, ri)) =
+          scc[row * (G.K / kI4GroupK) + k0 / kI4GroupK];
+  }
+  *reinterpret_cast<uint4 *>(w_out + code_offset(mt, u, G.MT, G.KU, kNvChunkUnits, kNvUnitBytes, G.rt) +
+                             lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+// Counts BF16 scales that are Inf or NaN.
+__global__ void i4_check_canonical_kernel(const uint16_t *__restrict__ sc, int64_t n,
+                                          uint32_t *bad) {
+  uint32_t cnt = 0;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    cnt += (sc[i] & 0x7F80u) == 0x7F80u;
+  cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+  if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(bad, cnt);
+}
+
 inline unsigned blocks_for(int64_t threads, int per_block) {
   return unsigned(ceil_div(threads, per_block));
 }
@@ -568,6 +808,168 @@ extern "C" vg_status vg_fp8_pack_gated(const float *Wgate, const float *Wup, int
   const int64_t threads = G.MT * G.KU * 32;
   f8_pack_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
       Wgate, rs_gate_out, G, static_cast<uint8_t *>(w_out), Wup, rs_up_out);
+  VG_LAUNCH_CHECK();
+  return VG_OK;
+}
+
+// ------------------------------------------- MXFP8 and groupwise INT4
+
+namespace {
+inline Geom block_geom(int fmt, int64_t M, int64_t K) {
+  return fmt == VG_FMT_MXFP8 ? f8_geom(M, K) : nv_geom(M, K);
+}
+inline size_t block_scale_bytes(const Geom &G) { return size_t(G.MT * G.KC * 128); }
+
+vg_status block_args(int fmt, int64_t M, int64_t K, const void *a, const void *b, const void *c,
+                     const void *d) {
+  if (vg_status s = check_mk(M, K)) return s;
+  if (!a || !b || !c || !d) return VG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d)) return VG_ERR_ALIGNMENT;
+  if (fmt == VG_FMT_MXFP8 && K % (kF8ChunkUnits * kUnitK) != 0) return VG_ERR_UNSUPPORTED;
+  if (fmt == VG_FMT_INT4G && K % (kNvChunkUnits * kUnitK) != 0) return VG_ERR_UNSUPPORTED;
+  return VG_OK;
+}
+
+// Largest |W| through a word of device scratch; NaN/Inf -> VG_ERR_INVALID_ARG.
+vg_status check_finite(const float *W, int64_t n, uint32_t *scratch, cudaStream_t st) {
+  VG_CUDA(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st));
+  amax_kernel<<<reduce_blocks(n), 256, 0, st>>>(W, n, scratch);
+  VG_LAUNCH_CHECK();
+  uint32_t bits = 0;
+  VG_CUDA(cudaMemcpyAsync(&bits, scratch, sizeof bits, cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  return bits >= 0x7F800000u ? VG_ERR_INVALID_ARG : VG_OK;
+}
+
+vg_status block_pack(int fmt, const float *W, int64_t M, int64_t K, void *w_out, void *scales_out,
+                     vg_stream_t stream) {
+  if (vg_status s = block_args(fmt, M, K, W, w_out, scales_out, W)) return s;
+  cudaStream_t st = as_cuda(stream);
+  const Geom G = block_geom(fmt, M, K);
+  if (vg_status s = check_finite(W, M * K, static_cast<uint32_t *>(scales_out), st)) return s;
+  VG_CUDA(cudaMemsetAsync(scales_out, 0, block_scale_bytes(G), st));
+  const int64_t threads = G.MT * G.KU * 32;
+  if (fmt == VG_FMT_MXFP8)
+    mx_pack_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
+        W, G, static_cast<uint8_t *>(w_out), static_cast<uint8_t *>(scales_out));
+  else
+    i4_pack_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
+        W, G, static_cast<uint8_t *>(w_out), static_cast<uint8_t *>(scales_out));
+  VG_LAUNCH_CHECK();
+  return VG_OK;
+}
+}  // namespace
+
+extern "C" vg_status vg_weight_sizes(int format, int64_t M, int64_t K, size_t *w_bytes,
+                                     size_t *scale_bytes) {
+  if (vg_status s = check_mk(M, K)) return s;
+  size_t w = 0, sc = 0;
+  switch (format) {
+    case VG_FMT_NVFP4: {
+      const Geom G = nv_geom(M, K);
+      w = size_t(G.MT * G.KU * kNvUnitBytes);
+      sc = size_t(G.MT * G.KC * kNvScaleChunkBytes);
+      break;
+    }
+    case VG_FMT_FP8_ROWSCALE: {
+      const Geom G = f8_geom(M, K);
+      w = size_t(G.MT * G.KU * kF8UnitBytes);
+      break;
+    }
+    case VG_FMT_MXFP8: {
+      const Geom G = f8_geom(M, K);
+      w = size_t(G.MT * G.KU * kF8UnitBytes);
+      sc = block_scale_bytes(G);
+      break;
+    }
+    case VG_FMT_INT4G: {
+      const Geom G = nv_geom(M, K);
+      w = size_t(G.MT * G.KU * kNvUnitBytes);
+      sc = block_scale_bytes(G);
+      break;
+    }
+    default:
+      return VG_ERR_INVALID_ARG;
+  }
+  if (w_bytes) *w_bytes = w;
+  if (scale_bytes) *scale_bytes = sc;
+  return VG_OK;
+}
+
+extern "C" vg_status vg_mxfp8_pack(const float *W, int64_t M, int64_t K, void *w_out,
+                                   void *scales_out, vg_stream_t stream) {
+  return block_pack(VG_FMT_MXFP8, W, M, K, w_out, scales_out, stream);
+}
+
+extern "C" vg_status vg_int4g_pack(const float *W, int64_t M, int64_t K, void *w_out,
+                                   void *scales_out, vg_stream_t stream) {
+  return block_pack(VG_FMT_INT4G, W, M, K, w_out, scales_out, stream);
+}
+
+extern "C" vg_status vg_mxfp8_unpack(const void *w, const void *scales, int64_t M, int64_t K,
+                                     uint8_t *q_out, uint8_t *sc_out, vg_stream_t stream) {
+  if (vg_status s = block_args(VG_FMT_MXFP8, M, K, w, scales, q_out, sc_out)) return s;
+  const Geom G = f8_geom(M, K);
+  const int64_t threads = G.MT * G.KU * 32;
+  mx_unpack_kernel<<<blocks_for(threads, 256), 256, 0, as_cuda(stream)>>>(
+      static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(scales), G, q_out, sc_out);
+  VG_LAUNCH_CHECK();
+  return VG_OK;
+}
+
+extern "C" vg_status vg_int4g_unpack(const void *w, const void *scales, int64_t M, int64_t K,
+                                     uint8_t *nib_out, uint16_t *sc_out, vg_stream_t stream) {
+  if (vg_status s = block_args(VG_FMT_INT4G, M, K, w, scales, nib_out, sc_out)) return s;
+  const Geom G = nv_geom(M, K);
+  const int64_t threads = G.MT * G.KU * 32;
+  i4_unpack_kernel<<<blocks_for(threads, 256), 256, 0, as_cuda(stream)>>>(
+      static_cast<const uint8_t *>(w), static_cast<const uint8_t *>(scales), G, nib_out, sc_out);
+  VG_LAUNCH_CHECK();
+  return VG_OK;
+}
+
+extern "C" vg_status vg_mxfp8_from_canonical(const uint8_t *q, const uint8_t *sc, int64_t M,
+                                             int64_t K, void *w_out, void *scales_out,
+                                             vg_stream_t stream) {
+  if (vg_status s = block_args(VG_FMT_MXFP8, M, K, q, sc, w_out, scales_out)) return s;
+  cudaStream_t st = as_cuda(stream);
+  const Geom G = f8_geom(M, K);
+  uint32_t *bad = static_cast<uint32_t *>(scales_out);   // scratch, rewritten below
+  VG_CUDA(cudaMemsetAsync(bad, 0, 2 * sizeof(uint32_t), st));
+  mx_check_canonical_kernel<<<reduce_blocks(M * K), 256, 0, st>>>(q, M * K, sc, M * (K / 32), bad);
+  VG_LAUNCH_CHECK();
+  uint32_t nbad[2] = {0, 0};
+  VG_CUDA(cudaMemcpyAsync(nbad, bad, sizeof nbad, cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  if (nbad[1]) return VG_ERR_INVALID_ARG;
+  if (nbad[0]) return VG_ERR_UNSUPPORTED;
+  VG_CUDA(cudaMemsetAsync(scales_out, 0, block_scale_bytes(G), st));
+  const int64_t threads = G.MT * G.KU * 32;
+  mx_from_canonical_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
+      q, sc, G, static_cast<uint8_t *>(w_out), static_cast<uint8_t *>(scales_out));
+  VG_LAUNCH_CHECK();
+  return VG_OK;
+}
+
+extern "C" vg_status vg_int4g_from_canonical(const uint8_t *nib, const uint16_t *sc, int64_t M,
+                                             int64_t K, void *w_out, void *scales_out,
+                                             vg_stream_t stream) {
+  if (vg_status s = block_args(VG_FMT_INT4G, M, K, nib, sc, w_out, scales_out)) return s;
+  cudaStream_t st = as_cuda(stream);
+  const Geom G = nv_geom(M, K);
+  uint32_t *bad = static_cast<uint32_t *>(scales_out);   // scratch, rewritten below
+  VG_CUDA(cudaMemsetAsync(bad, 0, sizeof(uint32_t), st));
+  i4_check_canonical_kernel<<<reduce_blocks(M * (K / kI4GroupK)), 256, 0, st>>>(
+      sc, M * (K / kI4GroupK), bad);
+  VG_LAUNCH_CHECK();
+  uint32_t nbad = 0;
+  VG_CUDA(cudaMemcpyAsync(&nbad, bad, sizeof nbad, cudaMemcpyDeviceToHost, st));
+  VG_CUDA(cudaStreamSynchronize(st));
+  if (nbad) return VG_ERR_INVALID_ARG;
+  VG_CUDA(cudaMemsetAsync(scales_out, 0, block_scale_bytes(G), st));
+  const int64_t threads = G.MT * G.KU * 32;
+  i4_from_canonical_kernel<<<blocks_for(threads, 256), 256, 0, st>>>(
+      nib, sc, G, static_cast<uint8_t *>(w_out), static_cast<uint8_t *>(scales_out));
   VG_LAUNCH_CHECK();
   return VG_OK;
 }

@@ -8,8 +8,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (FP8Weight, NVFP4Weight, RMSNorm, VerifyPlan, fp8_pack, fp8_pack_gated, nvfp4_pack,
-               nvfp4_pack_gated)
+from . import (FP8Weight, NVFP4Weight, RMSNorm, VerifyPlan, fp8_pack, fp8_pack_gated, int4g_pack,
+               mxfp8_pack, nvfp4_pack, nvfp4_pack_gated)
 from .inputs import (HIDDEN, INTERMEDIATE, LAYERS, VOCAB, Mat, draw_norm_inputs, draw_stack_matrix,
                      stack_mats)
 
@@ -46,16 +46,23 @@ class StackSetup:
         return VerifyPlan(entries, self.N, ordered=ordered, **kw)
 
 
+PACKERS = {"nvfp4": nvfp4_pack, "fp8": fp8_pack, "mxfp8": mxfp8_pack, "int4g": int4g_pack}
+
+
 def pack(W: torch.Tensor, fmt: str):
-    return nvfp4_pack(W) if fmt == "nvfp4" else fp8_pack(W)
+    return PACKERS[fmt](W)
 
 
 def build_stack(N: int, device="cuda", layers: int = LAYERS, seed: int = 4,
                 attn_fmt: str = "nvfp4", down_fmt: str = "fp8", hidden: int = HIDDEN,
-                inter: int = INTERMEDIATE, vocab: int = VOCAB, mats=None) -> StackSetup:
-    """Quantised layer stack (+ head) with x drawn per matrix (BF16 N(0,1))."""
+                inter: int = INTERMEDIATE, vocab: int = VOCAB, mats=None,
+                all_fmt: str | None = None) -> StackSetup:
+    """Quantised layer stack (+ head) with x drawn per matrix (BF16 N(0,1)).
+    all_fmt: every matrix in that format instead."""
     if mats is None:
         mats = stack_mats(layers, attn_fmt, down_fmt)
+        if all_fmt is not None:
+            mats = [Mat(m.name, all_fmt, m.M, m.K, m.group, m.layer, m.idx) for m in mats]
         if (hidden, inter, vocab) != (HIDDEN, INTERMEDIATE, VOCAB):
             def resize(m: Mat) -> Mat:
                 dims = {HIDDEN: hidden, INTERMEDIATE: inter, VOCAB: vocab}
