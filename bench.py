@@ -357,7 +357,7 @@ def run_ours(args, world, rank, local):
     width = torch.zeros(1, dtype=torch.int32, device=dev)
     plan.set_width(width)
     for w in [int(v) for v in args.widths.split(",") if v]:
-        if w == args.N:
+        if w == args.N or w > args.N:
             continue
         width.fill_(w)
         ms, _ = timed(plan.run, max(3, args.steps // 2), 2)
@@ -388,6 +388,22 @@ def run_ours(args, world, rank, local):
                  "us_p10_p90": [round(1e3 * q, 1) for q in pcts(per_d, (10, 90))],
                  "GBps": round(ds.bytes / (med / 1e3) / 1e9, 1)}
         del ds
+        torch.cuda.empty_cache()
+
+    # the same stack verified 16 columns wide (e.g. four requests' rounds of
+    # one token and three drafts) in one pass
+    wide = None
+    if not args.no_configs and args.layers == 64 and args.N <= 8:
+        wst = build_stack(16, device=dev, attn_fmt=args.attn_fmt)
+        wpl = wst.plan(ordered=True)
+        ms, per_w = timed(wpl.run, args.steps, args.warmup)
+        if wpl.check() != 0:
+            raise RuntimeError("wide stack reported a device error")
+        wpl.close()
+        med = statistics.median(per_w)
+        wide = {"N": 16, "bytes": wst.bytes, "us_per_pass": round(1e3 * med, 1),
+                "GBps": round(wst.bytes / (med / 1e3) / 1e9, 1)}
+        del wst
         torch.cuda.empty_cache()
 
     # the same stack with every matrix in MXFP8, then in groupwise INT4
@@ -520,7 +536,7 @@ def run_ours(args, world, rank, local):
                          "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs, copy)"},
             "per_width": widths, **extra,
             "per_config": configs, "draft_step": draft, "fused_stack": fused,
-            "format_stacks": format_stacks,
+            "format_stacks": format_stacks, "wide_stack": wide,
             "sustained": sustained,
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
         }
@@ -539,8 +555,9 @@ SINGLE = {
 }
 # the single-product configurations and the widths each is quoted at; the
 # last entries time the same shapes in the other weight formats
-PER_CONFIG = [("tiny", (1,)), ("proj", (1,)), ("gateup", (1, 2, 4, 8)), ("down", (1, 8)),
-              ("head", (1, 8)), ("proj", (8,), "mxfp8"), ("proj", (8,), "int4g"),
+PER_CONFIG = [("tiny", (1,)), ("proj", (1,)), ("gateup", (1, 2, 4, 8, 16, 32)),
+              ("down", (1, 8, 16)), ("head", (1, 8, 16, 32)), ("proj", (8,), "mxfp8"),
+              ("proj", (8,), "int4g"),
               ("gateup", (8,), "mxfp8"), ("gateup", (8,), "int4g"), ("head", (8,), "mxfp8"),
               ("head", (8,), "int4g")]
 

@@ -31,7 +31,15 @@
  *    legacy default stream) and runs asynchronously, except where a
  *    function says it synchronises.
  *  - BF16 values travel as uint16_t bit patterns.
- *  - Limits: 1 <= N <= 8, M >= 1, K >= 16, K % 16 == 0, M * K < 2^40.
+ *  - Limits: 1 <= N <= 32, M >= 1, K >= 16, K % 16 == 0, M * K < 2^40.
+ *    Passes wider than 8 columns (batched verification of several requests'
+ *    drafts: the NInfer README's one to eight execution lanes, each
+ *    verifying its MTP drafts) need whole chunks along K (K % 512 for the
+ *    4-bit formats, K % 256 for the 8-bit ones) and x by tensor copy, and
+ *    their x slice must fit the kernel's staging: 16 columns for every
+ *    layout, 32 for matrices packed in row blocks of 16 tiles (most rows or
+ *    K not a multiple of the chunk); otherwise VG_ERR_UNSUPPORTED.  Fused
+ *    operations (see vg_matrix_desc) take 8 columns at most.
  *
  * Device weight layout (the "packed" form; canonical forms are below):
  *  NVFP4 codes are stored in 16-row tiles cut into 64-column units of 512
@@ -248,6 +256,10 @@ vg_status vg_fp8_pack_gated(const float *Wgate, const float *Wup, int64_t I, int
  * a workspace must not overlap on the GPU. */
 vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, size_t *bytes);
 
+/* The same for a GEMV of N columns (N > 8 needs 2x (N <= 16) or 4x the
+ * partial-sum space). */
+vg_status vg_gemv_workspace_size_n(int64_t M, int64_t K, int format, int N, size_t *bytes);
+
 /* y[n][m] = bf16( sum_k x[n][k] * dequant(W)[m][k] ), NVFP4 weights.
  * One cooperative launch of up to one thread block per SM (all resident at
  * once: the block that sums a split row block waits, bounded, for the
@@ -299,8 +311,9 @@ vg_status vg_gemv_int4g(const void *w, const void *scales, const uint16_t *x, in
  *   Arguments and results are those of vg_gemv_nvfp4, minus the workspace.
  *   The workspace is one fixed device array of VG_NOALLOC_SCRATCH_BYTES
  *   (4 MiB) inside the library, created on each device when the library's
- *   module is first used there and held until the process exits.  A matrix
- *   that needs more (vg_gemv_workspace_size) gives VG_ERR_UNSUPPORTED.
+ *   module is first used there and held until the process exits.  A call
+ *   that needs more (vg_gemv_workspace_size_n; any N <= 8 fits on devices of
+ *   up to 255 SMs) gives VG_ERR_UNSUPPORTED.
  *   Nothing is allocated: the call looks up the array's device address
  *   (cudaGetSymbolAddress, on every call, so a device reset is harmless),
  *   clears the array's error word (4 bytes, cudaMemsetAsync on `stream`),

@@ -82,7 +82,7 @@ def test_gemv_argument_validation_happens_on_the_host(lib):
     p8 = ctypes.c_void_p(0x10008)
     # N out of range, null pointers, K % 16, misalignment: no CUDA call is made
     assert lib.vg_gemv_nvfp4(p16, p16, 1.0, p16, 0, 64, 64, p16, p16, 1 << 20, None) == 1
-    assert lib.vg_gemv_nvfp4(p16, p16, 1.0, p16, 9, 64, 64, p16, p16, 1 << 20, None) == 1
+    assert lib.vg_gemv_nvfp4(p16, p16, 1.0, p16, 33, 64, 64, p16, p16, 1 << 20, None) == 1
     assert lib.vg_gemv_nvfp4(None, p16, 1.0, p16, 1, 64, 64, p16, p16, 1 << 20, None) == 1
     assert lib.vg_gemv_nvfp4(p16, None, 1.0, p16, 1, 64, 64, p16, p16, 1 << 20, None) == 1
     assert lib.vg_gemv_nvfp4(p16, p16, 1.0, p16, 1, 64, 40, p16, p16, 1 << 20, None) == 1

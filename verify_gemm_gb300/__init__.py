@@ -330,11 +330,12 @@ def fp8_from_canonical(q: torch.Tensor, rowscale: torch.Tensor, stream=None) -> 
     return FP8Weight(w, rowscale, M, K)
 
 
-def workspace_for(wt, device=None) -> torch.Tensor:
-    """A zero-filled workspace large enough for GEMVs with this weight."""
+def workspace_for(wt, device=None, N: int = 8) -> torch.Tensor:
+    """A zero-filled workspace large enough for GEMVs of up to N columns
+    (N <= 8 by default) with this weight."""
     n = ctypes.c_size_t()
-    _lib.check(_lib.vg_gemv_workspace_size(wt.M, wt.K, wt.fmt, ctypes.byref(n)),
-               "vg_gemv_workspace_size")
+    _lib.check(_lib.vg_gemv_workspace_size_n(wt.M, wt.K, wt.fmt, max(N, 1), ctypes.byref(n)),
+               "vg_gemv_workspace_size_n")
     return torch.zeros(n.value, dtype=torch.uint8, device=device or wt.w.device)
 
 
@@ -348,7 +349,7 @@ def gemv(wt, x: torch.Tensor, y: torch.Tensor | None = None, workspace=None, str
         y = torch.empty((N, wt.M), dtype=torch.bfloat16, device=x.device)
     _dev_tensor(y, torch.bfloat16, "y")
     if workspace is None:
-        workspace = workspace_for(wt, x.device)
+        workspace = workspace_for(wt, x.device, N)
     if wt.fmt == VG_FMT_NVFP4:
         s = _lib.vg_gemv_nvfp4(_ptr(wt.w), _ptr(wt.scales), wt.gscale, _ptr(x), N, wt.M, wt.K,
                                _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream))

@@ -76,6 +76,7 @@ SIGNATURES = {
     "vg_gemv_mxfp8": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_int4g": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_workspace_size": (st, [i64, i64, i32, ctypes.POINTER(sz)]),
+    "vg_gemv_workspace_size_n": (st, [i64, i64, i32, i32, ctypes.POINTER(sz)]),
     "vg_gemv_nvfp4": (st, [P, P, f32, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_fp8_rowscale": (st, [P, P, P, i32, i64, i64, P, P, sz, P]),
     "vg_gemv_workspace_check": (st, [P, sz, ctypes.POINTER(i32), P]),

@@ -110,9 +110,13 @@ struct Params {
   uint32_t *ctas_done;      // blocks finished in this pass (left at 0)
   uint32_t *epoch;          // pass counter: tags partial sums
   uint32_t *done;           // per-phase completed row blocks (ordered only)
-  uint64_t *partials;       // [grid][kPartialWords]: tagged FP32 partial sums
-  int clear_slots;          // slots cleared when the pass counter wraps (>= grid): every
-                            // slot that any call sharing this workspace may have written
+  uint64_t *partials;       // [grid][nb * kPartialWords]: tagged FP32 partial sums
+  int64_t clear_words;      // 64-bit words cleared when the pass counter wraps: every slot
+                            // that any call sharing this workspace may have written
+  // (host) column blocks of 8: 1, 2 or 4 (N up to 8, 16, 32).  Kept here: placed
+  // where it would pad the descriptors below, it changed the register
+  // allocation of the kernels (more spills, slower passes).
+  int nb;
   uint32_t m8, m64;         // 8 and 64: shift multipliers kept in registers
   int x0_tensor;
   int fused;                // (host) the pass has fused operations or dependent x
@@ -548,7 +552,7 @@ __device__ __forceinline__ bool producer_dep_wait(const Params &p, const MatDev 
 #ifndef VG_PARK_NS
 #define VG_PARK_NS 2000
 #endif
-template <bool kFused>
+template <bool kFused, int NB = 1>
 __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *phases,
                          uint32_t ring, uint32_t full0, uint32_t empty0,
                          const volatile int *dep_waiting, int which, int np, int N) {
@@ -599,7 +603,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     const int k0 = q.c * iu * kUnitK;
     // x: one tensor copy of 8 rows x the item's units (rows >= N and units
     // past K read as zeros), else one bulk copy per row (one-chunk items)
-    const uint32_t x_bytes = tmap ? uint32_t(8 * iu * kUnitK * 2)
+    const uint32_t x_bytes = tmap ? uint32_t(8 * NB * iu * kUnitK * 2)
                                   : uint32_t(min(iu * kUnitK, K - k0) * 2 * N);
     const uint8_t *code_src = w + int64_t(q.rb) * rb_bytes + int64_t(q.c) * tiles * tile_item_bytes;
     const uint8_t *scale_src =
@@ -740,6 +744,58 @@ __device__ __forceinline__ bool collect(const Params &p, int b0, int bl, uint32_
   return true;
 }
 
+// collect() for slots of NB column blocks (slot_words 64-bit words each).
+template <int NB>
+__device__ __forceinline__ bool collect_wide(const Params &p, int b0, int bl, uint32_t tag, int at,
+                                             float (&accs)[4]) {
+  constexpr int64_t slot_words = int64_t(NB) * kPartialWords;
+  uint64_t deadline = 0;
+  uint32_t polls = 0;
+  for (int bb = b0; bb <= bl; bb += kCollectW) {
+    uint64_t v[kCollectW][4];
+    uint32_t pending = 0;
+#pragma unroll
+    for (int j = 0; j < kCollectW; ++j) {
+      if (bb + j <= bl) {
+        const uint64_t *src = p.partials + int64_t(bb + j) * slot_words + at;
+        ld_relaxed_v2u64(src, v[j][0], v[j][1]);
+        ld_relaxed_v2u64(src + 64, v[j][2], v[j][3]);
+        pending |= 1u << j;
+      }
+    }
+    for (;;) {
+#pragma unroll
+      for (int j = 0; j < kCollectW; ++j)
+        if (((pending >> j) & 1u) && tags_match(v[j], tag)) pending &= ~(1u << j);
+      if (pending == 0) break;
+      if ((++polls & 7u) == 0) {   // clock and error word every 8th poll
+        const uint64_t now = globaltimer();
+        if (deadline == 0) {
+          deadline = now + p.timeout_ns;
+        } else if (now > deadline) {
+          set_error(p.error, kErrPartialWait);
+          return false;
+        }
+        if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) return false;
+      }
+#pragma unroll
+      for (int j = 0; j < kCollectW; ++j) {
+        if ((pending >> j) & 1u) {
+          const uint64_t *src = p.partials + int64_t(bb + j) * slot_words + at;
+          ld_relaxed_v2u64(src, v[j][0], v[j][1]);
+          ld_relaxed_v2u64(src + 64, v[j][2], v[j][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kCollectW; ++j)
+      if (bb + j <= bl)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accs[e] += __uint_as_float(uint32_t(v[j][e]));
+  }
+  return true;
+}
+
 // Epilogue of a gated pair: rows g (gate) and g + 8 (up) of tile mt are
 // gate and up row 8 mt + g; y = SiLU(gate) * up from the FP32 sums, rounded
 // once to BF16.  Out of line, like the other rarely taken paths.
@@ -839,6 +895,211 @@ __device__ __forceinline__ bool finish_piece(const Params &p, const MatDev &m, i
   if (p.done) {
     named_bar(1, kConsumers);
     // releases the row block's y (written before the barrier)
+    if (tid == 0 && ok && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
+  }
+  return ok;
+}
+
+// --------------------------------------------------------- wider passes
+// N = 9..32 columns: NB blocks of 8 (NB = 2 or 4).  The item's x slice is
+// one tensor copy of 8 NB rows per unit, [unit][8 NB rows][128 B] with the
+// same 128-byte swizzle (rows 8b + g read like rows g), so column block b of
+// unit u sits at u * 1024 NB + b * 1024.  Every decoded A fragment feeds NB
+// MMAs.  Only whole chunks and tensor-copied x take this path.
+
+// Wide units: per half unit (k16 steps 0-1, then 2-3) every column block's
+// x fragment is loaded (one 16-byte load per block), then each step's A
+// fragment is decoded once and fed to the NB MMAs, so that at most NB x
+// fragments and one A fragment are live.
+template <int NB>
+__device__ __forceinline__ void mma_wide(float (&acc)[NB][4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, const uint4 (&x)[NB], bool hi) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+    mma_bf16(acc[b], a0, a1, a2, a3, hi ? x[b].z : x[b].x, hi ? x[b].w : x[b].y);
+}
+
+template <int NB>
+__device__ __forceinline__ void load_x_half(uint32_t xs, uint4 (&x)[NB]) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b) x[b] = lds128(xs + b * 1024);
+}
+
+template <int NB>
+__device__ __forceinline__ void nv_chunk_wide(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                              int xd, uint32_t m8, uint32_t m64,
+                                              float (&acc)[NB][4]) {
+  uint32_t scw[kNvChunkUnits / 2];
+  load_scale_words(scl + lane * kNvScaleLaneBytes, scw);
+#pragma unroll
+  for (int u = 0; u < kNvChunkUnits; ++u) {
+    const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
+    const uint32_t fg = nv_scale_pair(scw[u >> 1], uint32_t(u & 1) * 2u);
+    const uint32_t fg8 = nv_scale_pair(scw[u >> 1], uint32_t(u & 1) * 2u + 1u);
+    const uint32_t xu = xs + u * 1024 * NB;
+    uint4 xv[NB];
+    uint32_t a0, a1, a2, a3;
+    load_x_half<NB>(xu, xv);
+    nv_decode(wv.x, fg, fg8, m8, m64, a0, a1, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, false);
+    nv_decode(wv.y, fg, fg8, m8, m64, a0, a1, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, true);
+    load_x_half<NB>(xu + xd, xv);
+    nv_decode(wv.z, fg, fg8, m8, m64, a0, a1, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, false);
+    nv_decode(wv.w, fg, fg8, m8, m64, a0, a1, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, true);
+  }
+}
+
+// FP8 (kMx false: the row scale comes in the epilogue) or MXFP8 (kMx: the
+// lane's 8 block-scale bytes at scl).
+template <int NB, bool kMx>
+__device__ __forceinline__ void f8_chunk_wide(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                              int xd, float (&acc)[NB][4]) {
+  uint2 sw = make_uint2(0u, 0u);
+  if (kMx) sw = lds64(scl);
+#pragma unroll
+  for (int u = 0; u < kF8ChunkUnits; ++u) {
+    const uint4 w0 = lds128(slot + u * kF8UnitBytes + lane * 32);
+    const uint4 w1 = lds128(slot + u * kF8UnitBytes + lane * 32 + 16);
+    const uint32_t word = u < 2 ? sw.x : sw.y;
+    const uint32_t sg = kMx ? mx_scale_pair(word, uint32_t(u & 1) * 2u) : kF8Restore2;
+    const uint32_t sg8 = kMx ? mx_scale_pair(word, uint32_t(u & 1) * 2u + 1u) : kF8Restore2;
+    const uint32_t xu = xs + u * 1024 * NB;
+    uint4 xv[NB];
+    uint32_t a0, a1, a2, a3;
+    load_x_half<NB>(xu, xv);
+    mx_decode(w0.x, sg, sg8, a0, a1);
+    mx_decode(w0.y, sg, sg8, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, false);
+    mx_decode(w0.z, sg, sg8, a0, a1);
+    mx_decode(w0.w, sg, sg8, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, true);
+    load_x_half<NB>(xu + xd, xv);
+    mx_decode(w1.x, sg, sg8, a0, a1);
+    mx_decode(w1.y, sg, sg8, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, false);
+    mx_decode(w1.z, sg, sg8, a0, a1);
+    mx_decode(w1.w, sg, sg8, a2, a3);
+    mma_wide<NB>(acc, a0, a1, a2, a3, xv, true);
+  }
+}
+
+template <int NB>
+__device__ __forceinline__ void i4_chunk_wide(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
+                                              int xd, float (&acc)[NB][4]) {
+  const uint4 sv = lds128(scl);
+  const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+  for (int grp = 0; grp < kNvChunkUnits / 2; ++grp) {
+    float t4[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) t4[b][0] = t4[b][1] = t4[b][2] = t4[b][3] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int u = 2 * grp + h;
+      const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
+      const uint32_t xu = xs + u * 1024 * NB;
+      uint4 xv[NB];
+      uint32_t a0, a1, a2, a3;
+      load_x_half<NB>(xu, xv);
+      i4_decode(wv.x, a0, a1, a2, a3);
+      mma_wide<NB>(t4, a0, a1, a2, a3, xv, false);
+      i4_decode(wv.y, a0, a1, a2, a3);
+      mma_wide<NB>(t4, a0, a1, a2, a3, xv, true);
+      load_x_half<NB>(xu + xd, xv);
+      i4_decode(wv.z, a0, a1, a2, a3);
+      mma_wide<NB>(t4, a0, a1, a2, a3, xv, false);
+      i4_decode(wv.w, a0, a1, a2, a3);
+      mma_wide<NB>(t4, a0, a1, a2, a3, xv, true);
+    }
+    const float sg = __uint_as_float(sw[grp] << 16), sg8 = __uint_as_float(sw[grp] & 0xFFFF0000u);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      acc[b][0] = fmaf(sg, t4[b][0], acc[b][0]);
+      acc[b][1] = fmaf(sg, t4[b][1], acc[b][1]);
+      acc[b][2] = fmaf(sg8, t4[b][2], acc[b][2]);
+      acc[b][3] = fmaf(sg8, t4[b][3], acc[b][3]);
+    }
+  }
+}
+
+// finish_piece for NB column blocks: the tile-sum hand-off and the
+// partial-sum collection run once per block of 8 columns; a thread block's
+// partial-sum slot holds NB blocks' words.
+template <int NB>
+__device__ __forceinline__ bool finish_piece_wide(const Params &p, const MatDev &m, int T, int G,
+                                                  int piece_start, bool full_piece, int rb, int ph,
+                                                  uint32_t tag, bool aborted, int tl, int cc,
+                                                  uint32_t red, int N, float (&acc)[NB][4]) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int mt = rb * m.rt + tl;
+  const int at = ((warp * 2) * 32 + lane) * 2;
+  constexpr int64_t kSlot = int64_t(NB) * kPartialWords;
+  if (m.cpi > 1) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (cc != 0) sts128(red + uint32_t(warp * 32 + lane) * 16u, acc[b][0], acc[b][1], acc[b][2],
+                          acc[b][3]);
+      named_bar(3 + tl, m.cpi * 32);
+      if (cc == 0) {
+        for (int j = 1; j < m.cpi; ++j) {
+          const uint4 q = lds128(red + uint32_t((warp + j) * 32 + lane) * 16u);
+          acc[b][0] += __uint_as_float(q.x);
+          acc[b][1] += __uint_as_float(q.y);
+          acc[b][2] += __uint_as_float(q.z);
+          acc[b][3] += __uint_as_float(q.w);
+        }
+      }
+      named_bar(3 + tl, m.cpi * 32);
+    }
+  }
+  const bool lead = cc == 0;
+  bool ok = true;
+  if (!full_piece) {
+    const int first = m.item0 + rb * m.KI;
+    if (piece_start != first) {
+      if (!aborted && lead) {
+        const uint64_t hi = uint64_t(tag) << 32;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          uint64_t *dst = p.partials + int64_t(blockIdx.x) * kSlot + b * kPartialWords + at;
+          st_relaxed_v2u64(dst, hi | __float_as_uint(acc[b][0]), hi | __float_as_uint(acc[b][1]));
+          st_relaxed_v2u64(dst + 64, hi | __float_as_uint(acc[b][2]), hi | __float_as_uint(acc[b][3]));
+        }
+      }
+      return true;
+    }
+    if (!aborted && lead) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        if (ok) ok = collect_wide<NB>(p, int(blockIdx.x) + 1, owner(T, G, first + m.KI - 1), tag,
+                                      at + b * kPartialWords, acc[b]);
+    }
+    ok = __all_sync(0xFFFFFFFFu, ok);
+  }
+  if (ok && !aborted && lead && mt < m.MT) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = mt * kTileRows + g + 8 * h;
+      if (row >= m.M) continue;
+      const float mult = m.fmt == VG_FMT_FP8_ROWSCALE ? __ldg(m.rowscale + row) : m.mult;
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int nn = 8 * b + 2 * t + e;
+          if (nn < N) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(acc[b][2 * h + e] * mult);
+            m.y[int64_t(nn) * m.M + row] = *reinterpret_cast<const uint16_t *>(&v);
+          }
+        }
+    }
+  }
+  if (p.done) {
+    named_bar(1, kConsumers);
     if (tid == 0 && ok && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
   }
   return ok;
@@ -1231,7 +1492,387 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
     __syncthreads();
     if (sflag[0]) {
       uint4 *dst = reinterpret_cast<uint4 *>(p.partials);
-      const int64_t n = int64_t(p.clear_slots) * kPartialWords / 2;
+      const int64_t n = p.clear_words / 2;
+      for (int64_t k = tid; k < n; k += kKernelThreads) dst[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+// Passes of 9..32 columns (NB = 2 or 4 blocks of 8): the kernel above with
+// wider accumulators and x slices, for plain products whose items are whole
+// in K and take x by tensor copy, so that the streaming loop does all of the
+// work.  A kernel of its own: folding it into the one above changes how that
+// one's registers are allocated, which costs the 8-column passes measurably.
+template <int NB>
+__global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel_wide(const __grid_constant__ Params p) {
+  static_assert(NB > 1 && kAcc == 1, "wide passes: one accumulator chain per column block");
+  constexpr bool kFused = false;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tensor copies need 1024-byte alignment in shared memory
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
+  volatile int *sflag = reinterpret_cast<volatile int *>(smem + kBarOff + kBarBytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const MatDev *mats = p.mats ? p.mats : &p.mat0;
+  const PhaseDev *phases = p.mats ? p.phases : &p.phase0;
+
+  if (tid * 16 < kXRowBytes)
+    *reinterpret_cast<uint4 *>(smem + kZeroRowOff + tid * 16) = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_addr(bars + i), 1);                       // full: the slot's producer
+      mbar_init(smem_addr(bars + kSlots + i), kWarps);         // empty: every consumer warp
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    sflag[0] = 0;
+    sflag[1] = int(ld_relaxed(p.epoch));
+    sflag[2] = 0;
+    sflag[3] = 0;   // consumers waiting on a group dependency
+    // the pass's width: fixed, or read from the width word at launch
+    int n = p.N;
+    if (p.width) {
+      n = ld_relaxed(reinterpret_cast<const uint32_t *>(p.width));
+      if (n < 1 || n > p.N) {
+        if (blockIdx.x == 0) set_error(p.error, kErrWidth);
+        n = 0;   // no work: every block goes straight to the end of the pass
+      }
+    }
+    sflag[4] = n;
+  }
+  __syncthreads();
+  const uint32_t epoch = uint32_t(sflag[1]);
+  const int N = sflag[4];
+
+  if (N == 0) {
+    // invalid width: nothing is read or written
+  } else if (warp >= kWarps) {
+    // ================================================================ producer
+    const int np = p.mats ? kProducers : 1;
+    if (lane == 0 && warp - kWarps < np)
+      producer<false, NB>(p, mats, phases, smem_addr(smem), smem_addr(bars), smem_addr(bars + kSlots),
+               sflag + 3, warp - kWarps, np, N);
+
+  } else {
+    // =============================================================== consumers
+    const int g = lane >> 2, t = lane & 3;
+    const bool on = g < N;
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kSlots);
+    // This lane's x columns inside an item slot.  Tensor-copied slices are
+    // [unit][row][128 B] with the 16-byte chunks of row r at chunk ^ (r % 8)
+    // (128-byte swizzle), so a unit is 1024 bytes and the lane's two chunks
+    // 2t, 2t+1 of row g sit at (2t ^ g) and next to it.  Row-copied slices
+    // are padded rows of kXRowBytes, and a column g >= N reads a zero row.
+    const uint32_t xoff_t0 = uint32_t(kItemXOff + g * 128 + ((2 * t) ^ g) * 16);
+    const int xd_t = (g & 1) ? -16 : 16;
+    const uint32_t xoff_r = uint32_t(kItemXOff + g * kXRowBytes + t * 32);
+    const uint32_t xzero = smem_addr(smem + kZeroRowOff) + t * 32;
+    Seq cons;
+    cons.init(mats, phases, p);
+    bool aborted = false;
+    int s = 0;                     // ring slot of the current item
+    uint32_t par = 0;              // parity of that slot's current phase
+    int cur_ph = -1, cur_mi = -1;
+    uint32_t tag = 0;              // tag of this pass and phase
+    float acc[NB * kAcc][4];
+    // matrix fields cached while the matrix does not change
+    int K = 0, KU = 0, MT = 0, fmt = 0, rt = kBlockTiles, kfull = 0, iu = 0;
+    int tl = warp, cc = 0;         // this warp's tile and chunk within an item
+    uint32_t xoff_t = xoff_t0;     // ... and its x columns (tensor-copied x)
+    bool xt = false;               // the matrix's x slice is tensor-copied
+    const uint32_t red = smem_addr(smem + kRedOff);   // tile-sum scratch
+    while (cons.valid) {
+      const int ph = cons.ph;
+      // -------------------------------------- ordered: wait for group ph-1
+      if (ph != cur_ph) {
+        if (p.ordered && ph > 0) {
+          if (tid == 0) {
+            int ok = 1;
+            if (!aborted) {
+              const uint32_t *d = p.done + (ph - 1);
+              sflag[3] = 1;
+              const uint32_t target = uint32_t(phases[ph - 1].rbs);
+              if (ld_acquire(d) < target) {
+                const uint64_t deadline = globaltimer() + p.timeout_ns;
+                uint32_t it = 0;
+                // one L2 round trip per poll: the clock and the error word
+                // are looked at every 8th poll only
+                while (ld_acquire(d) < target) {
+                  if ((++it & 7u) == 0) {
+                    if (globaltimer() > deadline) {
+                      ok = 0;
+                      set_error(p.error, kErrDepWait);
+                      break;
+                    }
+                    if (ld_relaxed(reinterpret_cast<const uint32_t *>(p.error)) != 0) {
+                      ok = 0;   // another block has failed: results are void
+                      break;
+                    }
+                  }
+                  __nanosleep(32);
+                }
+              }
+            }
+            sflag[3] = 0;
+            sflag[0] = ok ? 0 : 1;
+          }
+          named_bar(1, kConsumers);
+          if (sflag[0]) aborted = true;
+          named_bar(1, kConsumers);
+        }
+        cur_ph = ph;
+        tag = epoch * uint32_t(p.nphases) + uint32_t(ph) + 1u;
+      }
+      if (cons.mi != cur_mi) {
+        const MatDev &mm = mats[cons.mi];
+        cur_mi = cons.mi;
+        K = mm.K;
+        KU = mm.KU;
+        MT = mm.MT;
+        fmt = mm.fmt;
+        rt = mm.rt;
+        iu = mm.iu;
+        kfull = mm.kfull;
+        tl = warp / mm.cpi;
+        cc = warp - tl * mm.cpi;
+        // the warp's chunk starts cc chunks into the item's x slice
+        xoff_t = xoff_t0 + uint32_t(cc * mm.cu * 1024 * NB);
+        xt = p.mats ? mm.xmap != nullptr : p.x0_tensor != 0;
+      }
+      if (kFused && fmt == kFmtNorm) {
+        // an RMS-norm item: its slot carries no data (take it and give it
+        // back), this block's consumers normalise x into y, and the item
+        // completes its phase
+        if (!aborted) {
+          const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
+          if (!__all_sync(0xFFFFFFFFu, ready)) {
+            if (lane == 0) set_error(p.error, kErrFullWait);
+            aborted = true;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (++s == kSlots) {
+          s = 0;
+          par ^= 1u;
+        }
+        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted);
+        if (tid == 0 && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
+        cons.skip(1, mats, phases, p);
+        continue;
+      }
+      // ------------------------------------------------- one row-block piece
+      // the block's contiguous items of one row block: set up once, then a
+      // tight loop over its chunks
+      const int rb = cons.rb, c0 = cons.c;
+      const int len = min(cons.KI - c0, cons.i1 - cons.i);
+      const int piece_start = cons.i;
+#pragma unroll
+      for (int a = 0; a < NB * kAcc; ++a)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+      const int mt = rb * rt + tl;
+      const bool work = mt < MT;
+      int c = c0;
+      const int c_end = c0 + len;
+      // Fast loop: the common case (tensor-copied x, chunks wholly inside K,
+      // the warp's tile inside M) with nothing decided per item but the wait.
+      if (!aborted && work && xt) {
+        if constexpr (NB > 1) {
+          // wider passes: whole chunks only, so this loop does all the work
+          const uint32_t code0 = warp * kSlotCodeBytes;
+          const uint32_t scl_nv = kItemScaleOff + warp * kNvScaleChunkBytes;
+          const uint32_t scl_b = kItemScaleOff + warp * kMxScaleChunkBytes +
+                                 (fmt == VG_FMT_MXFP8 ? uint32_t(g * 2 + (t >> 1)) * 8u
+                                                      : uint32_t(g) * 16u);
+          const int c_full = min(c_end, kfull);
+          for (; c < c_full; ++c) {
+            const uint32_t item = ring + s * kItemSlotBytes;
+            if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+              break;
+            if (fmt == VG_FMT_NVFP4)
+              nv_chunk_wide<NB>(item + code0, item + scl_nv, lane, item + xoff_t, xd_t, p.m8, p.m64,
+                                acc);
+            else if (fmt == VG_FMT_FP8_ROWSCALE)
+              f8_chunk_wide<NB, false>(item + code0, 0u, lane, item + xoff_t, xd_t, acc);
+            else if (fmt == VG_FMT_MXFP8)
+              f8_chunk_wide<NB, true>(item + code0, item + scl_b, lane, item + xoff_t, xd_t, acc);
+            else
+              i4_chunk_wide<NB>(item + code0, item + scl_b, lane, item + xoff_t, xd_t, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (++s == kSlots) {
+              s = 0;
+              par ^= 1u;
+            }
+          }
+          if (c < c_full) {
+            if (lane == 0) set_error(p.error, kErrFullWait);
+            aborted = true;
+          }
+        } else {
+          const uint32_t scl0 = kItemScaleOff + warp * kNvScaleChunkBytes;
+          const uint32_t code0 = warp * kSlotCodeBytes;
+          const int c_full = min(c_end, kfull);
+          if (fmt == VG_FMT_NVFP4) {
+            for (; c < c_full; ++c) {
+              const uint32_t item = ring + s * kItemSlotBytes;
+              if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                  !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+                break;   // the general loop below records the failure
+              // releases the slot itself, before computing its last two units
+              nv_chunk_full<true>(item + code0, item + scl0, lane, item + xoff_t, xd_t, p.m8, p.m64,
+                                  acc, empty0 + 8 * s);
+              if (++s == kSlots) {
+                s = 0;
+                par ^= 1u;
+              }
+            }
+          } else if (fmt == VG_FMT_MXFP8 || fmt == VG_FMT_INT4G) {
+            // these formats take whole chunks and tensor-copied x only, so
+            // this loop does all of their work
+            const bool mx = fmt == VG_FMT_MXFP8;
+            const uint32_t scl_l = kItemScaleOff + warp * kMxScaleChunkBytes +
+                                   (mx ? uint32_t(g * 2 + (t >> 1)) * 8u : uint32_t(g) * 16u);
+            for (; c < c_full; ++c) {
+              const uint32_t item = ring + s * kItemSlotBytes;
+              if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                  !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+                break;
+              if (mx)
+                mx_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc);
+              else
+                i4_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(empty0 + 8 * s);
+              if (++s == kSlots) {
+                s = 0;
+                par ^= 1u;
+              }
+            }
+            if (c < c_full) {          // a wait ran out: nothing else computes them
+              if (lane == 0) set_error(p.error, kErrFullWait);
+              aborted = true;
+            }
+          } else {
+            for (; c < c_full; ++c) {
+              const uint32_t item = ring + s * kItemSlotBytes;
+              if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
+                  !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
+                break;
+              f8_chunk<true>(item + code0, lane, item + xoff_t, xd_t, true, true, kF8ChunkUnits, 0,
+                             acc);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(empty0 + 8 * s);
+              if (++s == kSlots) {
+                s = 0;
+                par ^= 1u;
+              }
+            }
+          }
+        }
+      }
+      // General loop: the rest of the piece (K tails, row-copied x, tiles past
+      // M, a failed wait).
+      for (; c < c_end; ++c) {
+        const uint32_t item = ring + s * kItemSlotBytes;
+        if (!aborted) {
+          // every lane polls; a lane whose wait ran out stops the whole
+          // warp, since mma.sync needs all of it
+          const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
+          if (!__all_sync(0xFFFFFFFFu, ready)) {
+            if (lane == 0) set_error(p.error, kErrFullWait);
+            aborted = true;
+          }
+        }
+        if constexpr (NB == 1) {
+          if (!aborted && work && fmt <= VG_FMT_FP8_ROWSCALE) {
+            const uint32_t xs = xt ? item + xoff_t : (on ? item + xoff_r : xzero);
+            const int xd = xt ? xd_t : 16, xu = xt ? 1024 : kUnitK * 2;
+            // item c's first column; items past kfull (a K tail) have one chunk
+            const int kc = c * iu * kUnitK;
+            if (fmt == VG_FMT_NVFP4) {
+              const uint32_t scl = item + kItemScaleOff + warp * kNvScaleChunkBytes;
+              // warp-uniform test (mma.sync needs the whole warp): the item's
+              // whole column range lies inside K
+              if (c < kfull) {
+                const uint32_t code = item + warp * kSlotCodeBytes;
+                if (xt)
+                  nv_chunk_full<true>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
+                else
+                  nv_chunk_full<false>(code, scl, lane, xs, xd, p.m8, p.m64, acc);
+              } else {
+                const int nu = min(kNvChunkUnits, KU - c * kNvChunkUnits);
+                nv_chunk_tail(item + warp * nu * kNvUnitBytes, scl, lane, xs, xu, xd, on, nu,
+                              K - kc - 16 * t, p.m8, p.m64, acc);
+              }
+            } else {
+              const bool full = c < kfull;
+              const int nu = full ? kF8ChunkUnits : min(kF8ChunkUnits, KU - c * kF8ChunkUnits);
+              const uint32_t code = item + warp * nu * kF8UnitBytes;
+              if (xt)
+                f8_chunk<true>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
+              else
+                f8_chunk<false>(code, lane, xs, xd, on, full, nu, K - kc - 16 * t, acc);
+            }
+          }
+        }
+        // release the slot to the producer once every warp has read it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (++s == kSlots) {
+          s = 0;
+          par ^= 1u;
+        }
+      }
+
+      // ---------------------------------------------- end of the piece
+      if constexpr (NB > 1) {
+        if (!finish_piece_wide<NB>(p, mats[cons.mi], cons.items, cons.G, piece_start,
+                                   c0 == 0 && len == cons.KI, rb, ph, tag, aborted, tl, cc, red, N,
+                                   acc))
+          aborted = true;
+      } else {
+        float accs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          accs[e] = acc[0][e];
+#pragma unroll
+          for (int a = 1; a < kAcc; ++a) accs[e] += acc[a][e];
+        }
+        if (!finish_piece<kFused>(p, mats[cons.mi], cons.items, cons.G, piece_start,
+                          c0 == 0 && len == cons.KI, rb, ph, tag, aborted, tl, cc, red, N,
+                          accs[0], accs[1], accs[2], accs[3]))
+          aborted = true;
+      }
+      cons.skip(len, mats, phases, p);
+    }
+  }
+
+  // The last block out resets the per-phase completion counters and
+  // advances the pass epoch, so that the next pass's partial sums carry new
+  // tags.  Before the tags would overflow 32 bits the epoch restarts at 0
+  // and every slot that a call sharing this workspace may have written is
+  // cleared (tag 0 never matches): a slot written by an earlier call with a
+  // larger grid would otherwise carry a tag that becomes valid again.
+  __syncthreads();
+  if (tid == 0) sflag[2] = atom_add_relaxed(p.ctas_done, 1u) == uint32_t(p.grid - 1) ? 1 : 0;
+  __syncthreads();
+  if (sflag[2]) {
+    if (tid == 0) {
+      fence_acq_rel_gpu();    // every other block has finished with the state
+      if (p.done)
+        for (int ph = 0; ph < p.nphases; ++ph) p.done[ph] = 0u;
+      const bool wrap = (uint64_t(epoch) + 2u) * uint64_t(p.nphases) > 0xFFFFFFFFull;
+      *p.epoch = wrap ? 0u : epoch + 1u;
+      *p.ctas_done = 0u;
+      sflag[0] = wrap ? 1 : 0;
+    }
+    __syncthreads();
+    if (sflag[0]) {
+      uint4 *dst = reinterpret_cast<uint4 *>(p.partials);
+      const int64_t n = p.clear_words / 2;
       for (int64_t k = tid; k < n; k += kKernelThreads) dst[k] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -1249,6 +1890,20 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 
+// The kernel instantiations: plain N <= 8, fused N <= 8, plain N <= 16,
+// plain N <= 32.
+const void *const *kernels() {
+  static const void *const fns[4] = {
+      reinterpret_cast<const void *>(&stream_kernel<false>),
+      reinterpret_cast<const void *>(&stream_kernel<true>),
+      reinterpret_cast<const void *>(&stream_kernel_wide<2>),
+      reinterpret_cast<const void *>(&stream_kernel_wide<4>)};
+  return fns;
+}
+inline int kernel_index(bool fused, int nb) { return nb == 1 ? (fused ? 1 : 0) : nb == 2 ? 2 : 3; }
+// Column blocks of 8 for N columns.
+inline int col_blocks(int N) { return N <= 8 ? 1 : N <= 16 ? 2 : 4; }
+
 vg_status device_info(int *dev_out, DeviceInfo **info) {
   int dev = 0;
   VG_CUDA(cudaGetDevice(&dev));
@@ -1262,10 +1917,9 @@ vg_status device_info(int *dev_out, DeviceInfo **info) {
     VG_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
     d.cc = major * 10 + minor;
     if (d.cc != 103) return VG_ERR_UNSUPPORTED;
-    VG_CUDA(cudaFuncSetAttribute(stream_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes));
-    VG_CUDA(cudaFuncSetAttribute(stream_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes));
+    for (int k = 0; k < 4; ++k)
+      VG_CUDA(cudaFuncSetAttribute(kernels()[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kSmemBytes));
     d.attr_set = true;
   }
   *dev_out = dev;
@@ -1299,12 +1953,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 #define VG_XT_MIN_N 1
 #endif
 constexpr int kXTensorMinN = VG_XT_MIN_N;
-bool make_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units) {
+bool make_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units, int nb = 1) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
   if (!fn || K % kUnitK != 0 || N < kXTensorMinN) return false;
   const cuuint64_t dims[3] = {cuuint64_t(kUnitK), cuuint64_t(N), cuuint64_t(K / kUnitK)};
   const cuuint64_t strides[2] = {cuuint64_t(K) * 2, cuuint64_t(kUnitK) * 2};
-  const cuuint32_t box[3] = {cuuint32_t(kUnitK), 8u, cuuint32_t(units)};
+  const cuuint32_t box[3] = {cuuint32_t(kUnitK), cuuint32_t(8 * nb), cuuint32_t(units)};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(x), dims, strides, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1382,7 +2036,18 @@ int64_t algorithmic_bytes(const MatDev &m) {
 }
 
 // Single-GEMV workspace: [header words | partial slots].
-size_t ws_bytes(int grid) { return kWsHead + size_t(grid) * kPartialWords * sizeof(uint64_t); }
+// Single-GEMV workspace for nb column blocks of 8: one slot of nb blocks'
+// partial sums per thread block.
+size_t ws_bytes(int grid, int nb = 1) {
+  return kWsHead + size_t(grid) * size_t(nb) * kPartialWords * sizeof(uint64_t);
+}
+
+// Whether a matrix can run nb > 1 column blocks: whole items in K (the
+// streaming loops do all the work) and an x slice of 8 nb rows per unit
+// within the slot's x region.
+bool wide_ok(const MatDev &m, int nb) {
+  return nb == 1 || (m.kfull == m.KI && m.iu * nb <= kMaxItemUnits);
+}
 
 void set_head(Params &p, uint8_t *head) {
   p.error = reinterpret_cast<int *>(head);
@@ -1394,8 +2059,7 @@ void set_head(Params &p, uint8_t *head) {
 // other contributors), which a cooperative launch guarantees.
 vg_status launch(const Params &p, vg_stream_t stream) {
   void *args[] = {const_cast<Params *>(&p)};
-  const void *fn = p.fused ? reinterpret_cast<const void *>(&stream_kernel<true>)
-                           : reinterpret_cast<const void *>(&stream_kernel<false>);
+  const void *fn = kernels()[kernel_index(p.fused != 0, p.nb)];
   VG_CUDA(cudaLaunchCooperativeKernel(fn, dim3(p.grid),
                                       dim3(kKernelThreads), args, kSmemBytes, as_cuda(stream)));
   return VG_OK;
@@ -1405,7 +2069,8 @@ vg_status launch(const Params &p, vg_stream_t stream) {
 // what can be resident at once.
 vg_status max_grid(const DeviceInfo &d, int *grid) {
   int per_sm = 0;
-  // both instantiations have the same registers, threads and shared memory
+  // every instantiation has the same threads and shared memory, and the
+  // launch bounds cap their registers alike
   VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<true>, kKernelThreads,
                                                         kSmemBytes));
   if (per_sm < 1) return VG_ERR_UNSUPPORTED;
@@ -1419,15 +2084,18 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   DeviceInfo *di;
   if (vg_status s = device_info(&dev, &di)) return s;
   const int64_t T = int64_t(m0.RB) * m0.KI;
+  const int nb = col_blocks(N);
+  if (!wide_ok(m0, nb)) return VG_ERR_UNSUPPORTED;
   int grid = 0;
   if (vg_status s = max_grid(*di, &grid)) return s;
   grid = int(i64min(grid, T));
-  if (!workspace || workspace_bytes < ws_bytes(grid)) return VG_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < ws_bytes(grid, nb)) return VG_ERR_WORKSPACE;
   if (!aligned16(workspace)) return VG_ERR_ALIGNMENT;
   Params p;
   std::memset(&p, 0, sizeof p);
   p.nphases = 1;
   p.N = N;
+  p.nb = nb;
   p.ordered = 0;
   p.hold_phase = -1;
   p.grid = grid;
@@ -1437,15 +2105,15 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   set_head(p, ws);
   p.partials = reinterpret_cast<uint64_t *>(ws + kWsHead);
-  // every call on this device has at most di->sms blocks, so no slot past
-  // that count is ever written
-  p.clear_slots = int(i64min(int64_t(di->sms),
-                             int64_t((workspace_bytes - kWsHead) / (kPartialWords * sizeof(uint64_t)))));
+  // every call on this device has at most di->sms blocks of at most 4
+  // column blocks, so no word past that is ever written
+  p.clear_words = i64min(int64_t(di->sms) * 4 * kPartialWords,
+                         int64_t((workspace_bytes - kWsHead) / sizeof(uint64_t)));
   p.mat0 = m0;
-  p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu) ? 1 : 0;
-  // items of several chunks, and the block-scaled formats, take x by tensor
-  // copy only
-  if (!p.x0_tensor && (m0.cpi > 1 || m0.fmt >= VG_FMT_MXFP8)) return VG_ERR_UNSUPPORTED;
+  p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu, nb) ? 1 : 0;
+  // items of several chunks, the block-scaled formats and wider passes take
+  // x by tensor copy only
+  if (!p.x0_tensor && (m0.cpi > 1 || m0.fmt >= VG_FMT_MXFP8 || nb > 1)) return VG_ERR_UNSUPPORTED;
   p.phase0.items = int(T);
   p.phase0.rbs = m0.RB;
   p.phase0.mat_begin = 0;
@@ -1486,10 +2154,19 @@ extern "C" vg_status vg_gemv_workspace_size(int64_t M, int64_t K, int format, si
   return VG_OK;
 }
 
+extern "C" vg_status vg_gemv_workspace_size_n(int64_t M, int64_t K, int format, int N,
+                                              size_t *bytes) {
+  if (N < 1 || N > 32) return VG_ERR_INVALID_ARG;
+  size_t one = 0;
+  if (vg_status s = vg_gemv_workspace_size(M, K, format, &one)) return s;
+  *bytes = kWsHead + (one - kWsHead) * size_t(col_blocks(N));
+  return VG_OK;
+}
+
 static vg_status check_gemv_args(const void *w, const void *x, const void *y, int N, int64_t M,
                                  int64_t K) {
   if (vg_status s = check_mk(M, K)) return s;
-  if (N < 1 || N > 8 || !w || !x || !y) return VG_ERR_INVALID_ARG;
+  if (N < 1 || N > 32 || !w || !x || !y) return VG_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(x) || !aligned16(y)) return VG_ERR_ALIGNMENT;
   return VG_OK;
 }
@@ -1568,7 +2245,8 @@ extern "C" vg_status vg_gemv_workspace_check(void *workspace, size_t workspace_b
 extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,
                                               const vg_plan_options *opt,
                                               vg_verify_plan **plan_out) {
-  if (!mats || count < 1 || !plan_out || N < 1 || N > 8) return VG_ERR_INVALID_ARG;
+  if (!mats || count < 1 || !plan_out || N < 1 || N > 32) return VG_ERR_INVALID_ARG;
+  const int nb = col_blocks(N);
   *plan_out = nullptr;
   vg_plan_options o;
   std::memset(&o, 0, sizeof o);
@@ -1589,8 +2267,10 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   for (int i = 0; i < count; ++i) {
     const vg_matrix_desc &d = mats[i];
     if (i > 0 && d.group < mats[i - 1].group) return VG_ERR_INVALID_ARG;
-    // fused operations and dependent x need the group order
+    // fused operations and dependent x need the group order, and 8 columns
+    // at most
     if ((d.op != VG_OP_GEMV || d.x_after_group) && !o.ordered) return VG_ERR_INVALID_ARG;
+    if ((d.op != VG_OP_GEMV || d.x_after_group) && nb > 1) return VG_ERR_UNSUPPORTED;
     if (d.x_after_group && (i == 0 || d.group == mats[0].group)) return VG_ERR_INVALID_ARG;
     if (d.op == VG_OP_RMSNORM) {
       if (vg_status s = check_mk(1, d.K)) return s;
@@ -1624,6 +2304,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
       }
     }
     hm[i].x_after = d.x_after_group ? 1 : 0;
+    if (!wide_ok(hm[i], nb)) return VG_ERR_UNSUPPORTED;
     const bool new_phase = hp.empty() || (o.ordered && d.group != mats[i - 1].group);
     if (new_phase) {
       PhaseDev ph;
@@ -1662,7 +2343,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   plan->nphases = int(hp.size());
   plan->bytes = bytes;
   const size_t done_bytes = size_t((hp.size() * 4 + 255) / 256 * 256);
-  const size_t part_bytes = size_t(grid) * kPartialWords * sizeof(uint64_t);
+  const size_t part_bytes = size_t(grid) * size_t(nb) * kPartialWords * sizeof(uint64_t);
   plan->state_bytes = kWsHead + done_bytes + part_bytes;
   cudaError_t e = cudaMalloc(&plan->d_mats, sizeof(MatDev) * hm.size());
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_phases, sizeof(PhaseDev) * hp.size());
@@ -1673,8 +2354,9 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
     std::vector<CUtensorMap> maps(hm.size());
     for (size_t i = 0; i < hm.size(); ++i) {
       if (hm[i].fmt == kFmtNorm) continue;   // no copies
-      hm[i].xmap = make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].iu) ? plan->d_xmaps + i : nullptr;
-      if (!hm[i].xmap && (hm[i].cpi > 1 || hm[i].fmt >= VG_FMT_MXFP8)) untensored = true;
+      hm[i].xmap =
+          make_xmap(&maps[i], hm[i].x, N, hm[i].K, hm[i].iu, nb) ? plan->d_xmaps + i : nullptr;
+      if (!hm[i].xmap && (hm[i].cpi > 1 || hm[i].fmt >= VG_FMT_MXFP8 || nb > 1)) untensored = true;
     }
     e = cudaMemcpy(plan->d_xmaps, maps.data(), sizeof(CUtensorMap) * maps.size(),
                    cudaMemcpyHostToDevice);
@@ -1700,6 +2382,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   p.phases = plan->d_phases;
   p.nphases = plan->nphases;
   p.N = N;
+  p.nb = nb;
   p.ordered = plan->ordered;
   p.hold_phase = hold_phase;
   p.grid = grid;
@@ -1709,7 +2392,7 @@ extern "C" vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int co
   set_head(p, plan->d_state);
   p.done = plan->ordered ? reinterpret_cast<uint32_t *>(plan->d_state + kWsHead) : nullptr;
   p.partials = reinterpret_cast<uint64_t *>(plan->d_state + kWsHead + done_bytes);
-  p.clear_slots = grid;   // the plan's state is its own
+  p.clear_words = int64_t(grid) * nb * kPartialWords;   // the plan's state is its own
   for (const MatDev &m : hm) p.fused |= m.op != VG_OP_GEMV || m.x_after;
   *plan_out = plan;
   return VG_OK;

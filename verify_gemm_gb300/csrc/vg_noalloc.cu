@@ -53,7 +53,8 @@ extern "C" vg_status vg_gemv_nvfp4_noalloc(const void *w, const void *scales, fl
   // Arguments are checked by vg_gemv_nvfp4 below; the size check needs M, K.
   if (vg_status s = vg::check_mk(M, K)) return s;
   size_t need = 0;
-  if (vg_status s = vg_gemv_workspace_size(M, K, VG_FMT_NVFP4, &need)) return s;
+  if (N < 1 || N > 32) return VG_ERR_INVALID_ARG;
+  if (vg_status s = vg_gemv_workspace_size_n(M, K, VG_FMT_NVFP4, N, &need)) return s;
   if (need > kScratchBytes) return VG_ERR_UNSUPPORTED;   // beyond the fixed maximum
   void *scratch = nullptr;
   if (vg_status s = scratch_address(&scratch)) return s;
