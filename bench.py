@@ -589,7 +589,7 @@ def time_single(workload: str, N: int, steps: int, warmup: int, flush, fmt=None)
     plan = None
     if len(entries) == 1:
         wt, x, y, _ = entries[0]
-        ws = vg.workspace_for(wt)
+        ws = vg.workspace_for(wt, N=N)
 
         def run():
             vg.gemv(wt, x, y, ws)
