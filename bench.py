@@ -252,6 +252,56 @@ def cpu_sample(seconds: float):
                               "sample": "one round of the same sample"}}
 
 
+def run_reference_config(args):
+    """The oracle (as it stands) on one single-product configuration in
+    full: its weights quantised by the oracle, then GEMV rounds on all host
+    threads for at least a second, and one round on one thread."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from verify_gemm_gb300.inputs import WORKLOADS, draw_workload
+
+    orc = oracle.get()
+    key = {"down": "down_head", "head": "down_head"}.get(args.workload, args.workload)
+    title, names = SINGLE[args.workload]
+    Ws, xs = draw_workload(key, args.N)
+    jobs, nbytes = [], 0
+    for m, W in zip(WORKLOADS[key].mats, Ws):
+        if m.name not in names:
+            continue
+        xb = xs[m.K].view(torch.int16).numpy().view(np.uint16)
+        if m.fmt == "nvfp4":
+            nib, sc, gs = orc.nvfp4_quantise(W.numpy())
+            jobs.append(lambda t, a=(nib, sc, gs, xb): orc.gemv_nvfp4(*a, threads=t))
+            nbytes += m.M * m.K // 2 + m.M * m.K // 16 + 4
+        else:
+            q, rs = orc.fp8_quantise(W.numpy())
+            jobs.append(lambda t, a=(q, rs, xb): orc.gemv_fp8(*a, threads=t))
+            nbytes += m.M * m.K + 4 * m.M
+    del Ws
+    threads = os.cpu_count() or 1
+
+    def one(t):
+        t0 = time.perf_counter()
+        for j in jobs:
+            j(t)
+        return time.perf_counter() - t0
+
+    one(threads)
+    per = []
+    while sum(per) < 1.0:
+        per.append(one(threads))
+    single = one(1)
+    med = statistics.median(per)
+    print(json.dumps({"impl": "reference", "metric": METRIC, "unit": "GB/s",
+                      "config": {"workload": title, "N": args.N, "bytes": nbytes},
+                      "value": nbytes / med / 1e9, "ms_per_step": med * 1e3, "cores": threads,
+                      "rounds": len(per),
+                      "single_thread": {"value": nbytes / single / 1e9, "ms": single * 1e3}}),
+          flush=True)
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle as it stands, on all host threads.
     Each step is one round of the bounded sample (about 0.1 s); the line
@@ -717,7 +767,10 @@ def main():
         run_probe(args, int(os.environ.get("LOCAL_RANK", "0")))
         return
     world, rank, local = dist_init(args)
-    if args.impl == "reference":
+    if args.impl == "reference" and args.workload != "stack":
+        if rank == 0:
+            run_reference_config(args)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     elif args.workload != "stack":
         run_single(args, local)
