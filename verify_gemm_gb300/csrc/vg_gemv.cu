@@ -441,19 +441,32 @@ __device__ __forceinline__ void mx_chunk(uint32_t slot, uint32_t scl, int lane, 
 // tensor-copied x): per group the 8 MMAs of its two units run on integer
 // weights q - 8 (exact in BF16) into a fresh FP32 sum, which is then scaled
 // by the group's BF16 scales of rows g and g + 8 and added in.  scl: the
-// lane's 16 scale bytes [group][row g, row g + 8].
+// lane's 16 scale bytes [group][row g, row g + 8].  The next unit's codes
+// and x are loaded before the current one is decoded, and the slot is
+// released (empty: its empty mbarrier, if nonzero) before the last unit is
+// computed, as in nv_chunk_full.
 __device__ __forceinline__ void i4_chunk(uint32_t slot, uint32_t scl, int lane, uint32_t xs,
-                                         int xd, float (&acc)[kAcc][4]) {
+                                         int xd, float (&acc)[kAcc][4], uint32_t empty = 0) {
   const uint4 sv = lds128(scl);
   const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+  uint4 wv = lds128(slot + lane * 16);
+  uint4 xa = lds128(xs), xb = lds128(xs + xd);
 #pragma unroll
   for (int grp = 0; grp < kNvChunkUnits / 2; ++grp) {
     float t4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int u = 2 * grp + h;
-      const uint4 wv = lds128(slot + u * kNvUnitBytes + lane * 16);
-      const uint4 xa = lds128(xs + u * 1024), xb = lds128(xs + u * 1024 + xd);
+      uint4 nwv, nxa, nxb;
+      if (u + 1 < kNvChunkUnits) {
+        nwv = lds128(slot + (u + 1) * kNvUnitBytes + lane * 16);
+        nxa = lds128(xs + (u + 1) * 1024);
+        nxb = lds128(xs + (u + 1) * 1024 + xd);
+      }
+      if (u + 1 == kNvChunkUnits && empty != 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty);
+      }
       uint32_t a0, a1, a2, a3;
       i4_decode(wv.x, a0, a1, a2, a3);
       mma_bf16(t4, a0, a1, a2, a3, xa.x, xa.y);
@@ -463,6 +476,11 @@ __device__ __forceinline__ void i4_chunk(uint32_t slot, uint32_t scl, int lane, 
       mma_bf16(t4, a0, a1, a2, a3, xb.x, xb.y);
       i4_decode(wv.w, a0, a1, a2, a3);
       mma_bf16(t4, a0, a1, a2, a3, xb.z, xb.w);
+      if (u + 1 < kNvChunkUnits) {
+        wv = nwv;
+        xa = nxa;
+        xb = nxb;
+      }
     }
     const float sg = __uint_as_float(sw[grp] << 16), sg8 = __uint_as_float(sw[grp] & 0xFFFF0000u);
     acc[0][0] = fmaf(sg, t4[0], acc[0][0]);
@@ -1740,12 +1758,14 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel_wide(const __
               if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(full0 + 8 * s, par)) &&
                   !__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, par, globaltimer() + p.timeout_ns)))
                 break;
-              if (mx)
+              if (mx) {
                 mx_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc);
-              else
-                i4_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(empty0 + 8 * s);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * s);
+              } else {
+                // releases the slot itself, before computing its last unit
+                i4_chunk(item + code0, item + scl_l, lane, item + xoff_t, xd_t, acc, empty0 + 8 * s);
+              }
               if (++s == kSlots) {
                 s = 0;
                 par ^= 1u;
