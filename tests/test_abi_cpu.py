@@ -109,3 +109,34 @@ def test_oracle_and_product_share_nothing():
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".py", ".c", ".h")):
             assert not imp_pkg.search(open(os.path.join(ROOT, "oracle", f)).read()), f
+
+
+def test_format_sizes_and_host_checks(lib):
+    """Sizes of the block-scaled formats, and the argument checks of the newer
+    entry points, answered on the host without a GPU."""
+    wb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    # MXFP8: E4M3 codes (FP8 units) + 1 E8M0 byte per 32 elements
+    assert lib.vg_weight_sizes(2, 5120, 5120, ctypes.byref(wb), ctypes.byref(sb)) == 0
+    assert wb.value == 5120 * 5120 and sb.value == 5120 * 5120 // 32
+    # groupwise INT4: 4-bit codes + a BF16 scale per 128 elements
+    assert lib.vg_weight_sizes(3, 5120, 5120, ctypes.byref(wb), ctypes.byref(sb)) == 0
+    assert wb.value == 5120 * 5120 // 2 and sb.value == 2 * 5120 * 5120 // 128
+    # NVFP4 and FP8 agree with their own size calls
+    assert lib.vg_weight_sizes(0, 17, 80, ctypes.byref(wb), ctypes.byref(sb)) == 0
+    assert (wb.value, sb.value) == (2 * 2 * 512, 2 * 1 * 512)
+    assert lib.vg_weight_sizes(9, 64, 64, ctypes.byref(wb), ctypes.byref(sb)) == 1
+    p16 = ctypes.c_void_p(0x10000)
+    # K not a multiple of a chunk: the block-scaled packers refuse before any CUDA call
+    assert lib.vg_int4g_pack(p16, 64, 768, p16, p16, None) == 3
+    assert lib.vg_mxfp8_pack(p16, 64, 320, p16, p16, None) == 3
+    assert lib.vg_gemv_int4g(p16, p16, p16, 8, 64, 768, p16, p16, 1 << 20, None) == 3
+    # widths: 1..32
+    n = ctypes.c_size_t()
+    assert lib.vg_gemv_workspace_size_n(64, 512, 0, 33, ctypes.byref(n)) == 1
+    assert lib.vg_gemv_workspace_size_n(64, 512, 0, 0, ctypes.byref(n)) == 1
+    assert lib.vg_gemv_nvfp4(p16, p16, 1.0, p16, 33, 64, 64, p16, p16, 1 << 20, None) == 1
+    # gated pairs need I % 8 == 0
+    gs = (ctypes.c_float * 2)()
+    assert lib.vg_nvfp4_pack_gated(p16, p16, 12, 64, p16, p16, gs, None) == 1
+    # the width word must be 4-byte aligned (checked before the plan is touched)
+    assert lib.vg_verify_plan_set_width(None, None) == 1
