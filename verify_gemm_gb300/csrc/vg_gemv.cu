@@ -631,10 +631,9 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     // ---- x written by the previous phase of this pass: wait until that
     // phase has completed (bounded), bringing this producer's next items
     // into L2 meanwhile; then order the acquire before the x copies
-    if (kFused && xdep && dep_ok != q.ph) {
-      if (!producer_dep_wait(p, mats, phases, q, np)) break;
-      dep_ok = q.ph;
-    }
+    // an x that the previous phase writes: its copy waits for that phase
+    // (below, after the item's weight copies have been issued)
+    const bool need_dep = kFused && xdep && dep_ok != q.ph;
 
     // ---- wait for the slot
     if (!mbar_test_wait(empty0 + 8 * s, par ^ 1u)) {
@@ -645,12 +644,15 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
           if (pf_ahead == 0) pf = q;   // start at the item waiting for this slot
           if (pf.valid) {
             const MatDev &fm = mats[pf.mi];
-            const int ft = min(fm.rt, fm.MT - pf.rb * fm.rt);
-            const int fu = min(fm.iu, fm.KU - pf.c * fm.iu);
-            bulk_prefetch_l2(fm.w + item_code_off(fm, pf.rb, pf.c, ft), uint32_t(ft * fu * fm.ub));
-            if (fm.scb)
-              bulk_prefetch_l2(fm.sc + item_scale_off(fm, pf.rb, pf.c, ft),
-                               uint32_t(ft * fm.cpi * fm.scb));
+            // an RMS-norm item has no weights to bring in (only fused passes have them)
+            if (!(kFused && fm.fmt == kFmtNorm)) {
+              const int ft = min(fm.rt, fm.MT - pf.rb * fm.rt);
+              const int fu = min(fm.iu, fm.KU - pf.c * fm.iu);
+              bulk_prefetch_l2(fm.w + item_code_off(fm, pf.rb, pf.c, ft), uint32_t(ft * fu * fm.ub));
+              if (fm.scb)
+                bulk_prefetch_l2(fm.sc + item_scale_off(fm, pf.rb, pf.c, ft),
+                                 uint32_t(ft * fm.cpi * fm.scb));
+            }
             pf.advance(mats, phases, p);
             ++pf_ahead;
           }
@@ -673,6 +675,11 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
     mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes);
     bulk_g2s(slot, code_src, code_bytes, full, pol_w);
     if (sc) bulk_g2s(slot + kItemScaleOff, scale_src, scale_bytes, full, pol_w);
+    if (kFused && need_dep) {
+      // the weights stream in meanwhile; the slot completes once x lands
+      if (!producer_dep_wait(p, mats, phases, q, np)) break;
+      dep_ok = q.ph;
+    }
     if (tmap) {
       bulk_tensor_3d(slot + kItemXOff, tmap, 0, 0, q.c * iu, full, pol_x);
     } else {
@@ -1127,9 +1134,13 @@ __device__ __forceinline__ bool finish_piece_wide(const Params &p, const MatDev 
 //   y[n][k] = bf16( x[n][k] * inv[n] * gamma[k] ),
 //   inv[n] = 1 / sqrt(sum_k x[n][k]^2 / K + eps),
 // sums in FP32 (per thread, then per warp, then across warps in `red`).
-// Every thread reaches every barrier; `active` false skips the work.  Kept
-// out of line: inlined, it costs the streaming loops registers.
-__device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, bool active) {
+// The norm is split into m.RB items, one per thread block: each computes
+// the whole rows' sums (x is read from L2) and writes its slice `slice` of
+// the 8-element vectors of y.  Every thread reaches every barrier; `active`
+// false skips the work.  Kept out of line: inlined, it costs the streaming
+// loops registers.
+__device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, bool active,
+                                           int slice) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K8 = m.K / 8;
   for (int n = 0; n < N; ++n) {
@@ -1160,11 +1171,12 @@ __device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, b
   named_bar(1, kConsumers);
   if (active) {
     const uint4 *gr = reinterpret_cast<const uint4 *>(m.gamma);
+    const int k0 = int(int64_t(K8) * slice / m.RB), k1 = int(int64_t(K8) * (slice + 1) / m.RB);
     for (int n = 0; n < N; ++n) {
       const float inv = red[8 * kWarps + n];
       const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
       uint4 *yr = reinterpret_cast<uint4 *>(m.y + int64_t(n) * m.K);
-      for (int k = tid; k < K8; k += kConsumers) {
+      for (int k = k0 + tid; k < k1; k += kConsumers) {
         const uint4 v = xr[k], gv = __ldg(gr + k);
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
         uint32_t o[4];
@@ -1338,7 +1350,8 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
           s = 0;
           par ^= 1u;
         }
-        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted);
+        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted,
+                      cons.rb);
         if (tid == 0 && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
         cons.skip(1, mats, phases, p);
         continue;
@@ -1674,7 +1687,8 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel_wide(const __
           s = 0;
           par ^= 1u;
         }
-        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted);
+        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted,
+                      cons.rb);
         if (tid == 0 && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
         cons.skip(1, mats, phases, p);
         continue;
@@ -2020,7 +2034,7 @@ MatDev make_mat(int fmt, int64_t M, int64_t K, const void *w, const void *sc, co
   return m;
 }
 
-// An RMS-norm entry: one item, no weights, no copies.
+// An RMS-norm entry: no weights, no copies; its items are slices of y.
 MatDev make_norm_mat(int64_t K, const uint16_t *x, uint16_t *y, const uint16_t *gamma, float eps) {
   MatDev m;
   std::memset(&m, 0, sizeof m);
@@ -2033,7 +2047,9 @@ MatDev make_norm_mat(int64_t K, const uint16_t *x, uint16_t *y, const uint16_t *
   m.M = 1;
   m.Mo = int(K);
   m.K = int(K);
-  m.MT = m.KU = m.KC = m.RB = m.KI = 1;
+  m.MT = m.KU = m.KC = m.KI = 1;
+  // one slice of the output per thread block of a pass (items = slices)
+  m.RB = int(i64min(kLayoutSMs, K / 8));
   m.cu = kNvChunkUnits;
   m.ub = kNvUnitBytes;
   m.rt = kBlockTiles;
