@@ -670,7 +670,19 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
 
     // ---- issue (an RMS-norm item carries no data: its slot completes at once)
     if (is_norm) {
-      mbar_arrive_expect_tx(full, 0u);
+      // the rows of x, when they fit the slot (else the consumers read them
+      // from global memory), copied once the phase that writes them is done
+      const uint64_t xb = uint64_t(N) * uint64_t(K) * 2u;
+      if (kFused && xb <= uint64_t(kItemSlotBytes)) {
+        mbar_arrive_expect_tx(full, uint32_t(xb));
+        if (need_dep) {
+          if (!producer_dep_wait(p, mats, phases, q, np)) break;
+          dep_ok = q.ph;
+        }
+        bulk_g2s(slot, reinterpret_cast<const uint8_t *>(xg), uint32_t(xb), full, pol_x);
+      } else {
+        mbar_arrive_expect_tx(full, 0u);
+      }
     } else {
     mbar_arrive_expect_tx(full, code_bytes + scale_bytes + x_bytes);
     bulk_g2s(slot, code_src, code_bytes, full, pol_w);
@@ -1135,20 +1147,26 @@ __device__ __forceinline__ bool finish_piece_wide(const Params &p, const MatDev 
 //   inv[n] = 1 / sqrt(sum_k x[n][k]^2 / K + eps),
 // sums in FP32 (per thread, then per warp, then across warps in `red`).
 // The norm is split into m.RB items, one per thread block: each computes
-// the whole rows' sums (x is read from L2) and writes its slice `slice` of
-// the 8-element vectors of y.  Every thread reaches every barrier; `active`
-// false skips the work.  Kept out of line: inlined, it costs the streaming
-// loops registers.
+// the whole rows' sums and writes its slice `slice` of the 8-element vectors
+// of y, one (row, vector) pair per thread.  When the N rows fit an item slot
+// (N K 2 bytes, 80 KB at N = 8, K = 5120) the producer has copied them into
+// the item's slot (xs), so every read is from shared memory; otherwise they
+// are read from L2.  Every thread reaches every barrier; `active` false
+// skips the work.  Kept out of line: inlined, it costs the streaming loops
+// registers.
 __device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, bool active,
-                                           int slice) {
+                                           int slice, uint32_t xs) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K8 = m.K / 8;
+  // sums of squares of every row, from the item's slot when the rows are
+  // there (row n at xs + 16 K8 n), else from global memory (L2: the previous
+  // phase wrote them); the same sums in the same order either way
   for (int n = 0; n < N; ++n) {
     float ss = 0.f;
     if (active) {
       const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
       for (int k = tid; k < K8; k += kConsumers) {
-        const uint4 v = xr[k];
+        const uint4 v = xs != 0u ? lds128(xs + uint32_t(n * K8 + k) * 16u) : xr[k];
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -1170,25 +1188,27 @@ __device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, b
   }
   named_bar(1, kConsumers);
   if (active) {
+    // this block's slice of every row: one 8-element group per thread,
+    // (row, group) pairs spread over all threads
     const uint4 *gr = reinterpret_cast<const uint4 *>(m.gamma);
     const int k0 = int(int64_t(K8) * slice / m.RB), k1 = int(int64_t(K8) * (slice + 1) / m.RB);
-    for (int n = 0; n < N; ++n) {
+    const int L = k1 - k0;
+    for (int i = tid; i < N * L; i += kConsumers) {
+      const int n = i / L, k = k0 + (i - n * L);
       const float inv = red[8 * kWarps + n];
-      const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
-      uint4 *yr = reinterpret_cast<uint4 *>(m.y + int64_t(n) * m.K);
-      for (int k = k0 + tid; k < k1; k += kConsumers) {
-        const uint4 v = xr[k], gv = __ldg(gr + k);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
-        uint32_t o[4];
+      const uint4 v = xs != 0u ? lds128(xs + uint32_t(n * K8 + k) * 16u)
+                               : reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K)[k];
+      const uint4 gv = __ldg(gr + k);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float x0 = __uint_as_float(wv[j] << 16), x1 = __uint_as_float(wv[j] & 0xFFFF0000u);
-          const float g0 = __uint_as_float(gw[j] << 16), g1 = __uint_as_float(gw[j] & 0xFFFF0000u);
-          const __nv_bfloat162 r = __floats2bfloat162_rn(x0 * inv * g0, x1 * inv * g1);
-          o[j] = *reinterpret_cast<const uint32_t *>(&r);
-        }
-        yr[k] = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int j = 0; j < 4; ++j) {
+        const float x0 = __uint_as_float(wv[j] << 16), x1 = __uint_as_float(wv[j] & 0xFFFF0000u);
+        const float g0 = __uint_as_float(gw[j] << 16), g1 = __uint_as_float(gw[j] & 0xFFFF0000u);
+        const __nv_bfloat162 r = __floats2bfloat162_rn(x0 * inv * g0, x1 * inv * g1);
+        o[j] = *reinterpret_cast<const uint32_t *>(&r);
       }
+      reinterpret_cast<uint4 *>(m.y + int64_t(n) * m.K)[k] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     // a later phase copies y in through the async proxy
     fence_proxy_async_global();
@@ -1334,9 +1354,9 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
         xt = p.mats ? mm.xmap != nullptr : p.x0_tensor != 0;
       }
       if (kFused && fmt == kFmtNorm) {
-        // an RMS-norm item: its slot carries no data (take it and give it
-        // back), this block's consumers normalise x into y, and the item
-        // completes its phase
+        // an RMS-norm item: its slot carries the rows of x when they fit
+        // (else nothing), this block's consumers normalise x into y, give
+        // the slot back, and the item completes its phase
         if (!aborted) {
           const bool ready = mbar_wait_for(full0 + 8 * s, par, p.timeout_ns);
           if (!__all_sync(0xFFFFFFFFu, ready)) {
@@ -1344,14 +1364,16 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel(const __grid_
             aborted = true;
           }
         }
+        const bool x_in_slot = uint64_t(N) * uint64_t(K) * 2u <= uint64_t(kItemSlotBytes);
+        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted,
+                      cons.rb, x_in_slot ? ring + s * kItemSlotBytes : 0u);
+        // rms_norm_item ends on a barrier of all consumers: the slot is read
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
         if (++s == kSlots) {
           s = 0;
           par ^= 1u;
         }
-        rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted,
-                      cons.rb);
         if (tid == 0 && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
         cons.skip(1, mats, phases, p);
         continue;
@@ -1688,7 +1710,7 @@ __global__ void __launch_bounds__(kKernelThreads, 1) stream_kernel_wide(const __
           par ^= 1u;
         }
         rms_norm_item(mats[cons.mi], N, reinterpret_cast<float *>(smem + kRedOff), !aborted,
-                      cons.rb);
+                      cons.rb, 0u);
         if (tid == 0 && !aborted && ph != p.hold_phase) red_add_release(p.done + ph, 1u);
         cons.skip(1, mats, phases, p);
         continue;
