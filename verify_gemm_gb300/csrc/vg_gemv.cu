@@ -1158,27 +1158,60 @@ __device__ __noinline__ void rms_norm_item(const MatDev &m, int N, float *red, b
                                            int slice, uint32_t xs) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K8 = m.K / 8;
-  // sums of squares of every row, from the item's slot when the rows are
-  // there (row n at xs + 16 K8 n), else from global memory (L2: the previous
-  // phase wrote them); the same sums in the same order either way
-  for (int n = 0; n < N; ++n) {
-    float ss = 0.f;
-    if (active) {
-      const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
-      for (int k = tid; k < K8; k += kConsumers) {
-        const uint4 v = xs != 0u ? lds128(xs + uint32_t(n * K8 + k) * 16u) : xr[k];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  if (xs != 0u) {
+    // the rows are in the item's slot (row n at xs + 16 K8 n): all rows at
+    // once, so that their sums and shuffle reductions overlap
+    float ss[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(wv[j] << 16), hi = __uint_as_float(wv[j] & 0xFFFF0000u);
-          ss = fmaf(lo, lo, ss);
-          ss = fmaf(hi, hi, ss);
+    for (int n = 0; n < 8; ++n) ss[n] = 0.f;
+    if (active) {
+      for (int k = tid; k < K8; k += kConsumers) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          if (n < N) {
+            const uint4 v = lds128(xs + uint32_t(n * K8 + k) * 16u);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = __uint_as_float(wv[j] << 16), hi = __uint_as_float(wv[j] & 0xFFFF0000u);
+              ss[n] = fmaf(lo, lo, ss[n]);
+              ss[n] = fmaf(hi, hi, ss[n]);
+            }
+          }
         }
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    if (lane == 0) red[n * kWarps + warp] = ss;
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+        if (n < N) ss[n] += __shfl_xor_sync(0xFFFFFFFFu, ss[n], o);
+    if (lane == 0)
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+        if (n < N) red[n * kWarps + warp] = ss[n];
+  } else {
+    // the rows from global memory (L2: the previous phase wrote them); the
+    // same sums in the same order
+    for (int n = 0; n < N; ++n) {
+      float ss = 0.f;
+      if (active) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(m.x + int64_t(n) * m.K);
+        for (int k = tid; k < K8; k += kConsumers) {
+          const uint4 v = xr[k];
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(wv[j] << 16), hi = __uint_as_float(wv[j] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      if (lane == 0) red[n * kWarps + warp] = ss;
+    }
   }
   named_bar(1, kConsumers);
   if (tid < N) {
