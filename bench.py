@@ -76,8 +76,9 @@ def parse():
                     help="skip the single-product configurations (per_config)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="stack",
-                    choices=["stack", "tiny", "proj", "gateup", "down", "head", "probe"],
-                    help="stack: the fused verify pass (headline); others: one product of "
+                    choices=["stack", "fused", "tiny", "proj", "gateup", "down", "head", "probe"],
+                    help="stack: the verify pass (headline); fused: the verify pass with RMS "
+                         "norms, the gated activation and dependent x; others: one product of "
                          "that configuration, timed alone with an L2 flush between launches")
     return ap.parse_args()
 
@@ -700,6 +701,52 @@ def run_single(args, local):
     print(json.dumps(line), flush=True)
 
 
+def run_fused(args, local):
+    """The fused verify stack alone (RMS norms, the gated activation, dependent
+    x; --layers layers, --N columns), ordered, one pass per step.  With 64
+    layers its 16.3 GB exceed L2; a smaller stack is for profiling."""
+    import torch
+
+    from verify_gemm_gb300 import build as vbuild
+    from verify_gemm_gb300.workloads import build_fused_stack
+
+    vbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    fs = build_fused_stack(args.N, layers=args.layers, device=dev, attn_fmt=args.attn_fmt)
+    plan = fs.plan()
+    for _ in range(args.warmup):
+        plan.run()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        plan.run()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    if plan.check() != 0:
+        raise RuntimeError("fused stack reported a device error")
+    plan.close()
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    med = statistics.median(ms)
+    peak, kind = peaks()
+    gbps = fs.bytes / (med / 1e3) / 1e9
+    line = {"metric": METRIC, "value": round(gbps, 1), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "weights": WEIGHTS, "data": "synthetic",
+            "config": {"workload": f"fused verify stack, {args.layers} layers: RMS norms, "
+                                   "gated activation, dependent x",
+                       "N": args.N, "bytes": fs.bytes,
+                       "phases": len({e.group for e in fs.entries}),
+                       "us_p10_p90": [round(1e3 * q, 1) for q in pcts(ms, (10, 90))]},
+            "roofline": {"bound": "hbm", "achieved": round(gbps, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbps / peak, 4), "traffic": None, "peak_kind": kind},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def per_config(steps: int, warmup: int):
     """Every single-product configuration at every width it is quoted at,
     timed alone (median of `steps` launches, L2 flushed before each)."""
@@ -767,11 +814,17 @@ def main():
         run_probe(args, int(os.environ.get("LOCAL_RANK", "0")))
         return
     world, rank, local = dist_init(args)
-    if args.impl == "reference" and args.workload != "stack":
+    if args.impl == "reference" and args.workload == "fused":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle's fused chain is "
+                              "checked in the tests, not timed"}), flush=True)
+    elif args.impl == "reference" and args.workload != "stack":
         if rank == 0:
             run_reference_config(args)
     elif args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "fused":
+        run_fused(args, local)
     elif args.workload != "stack":
         run_single(args, local)
     else:
