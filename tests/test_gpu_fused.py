@@ -153,6 +153,40 @@ def test_rmsnorm_entry(vg, orc, N, K):
     plan.close()
 
 
+@pytest.mark.parametrize("N,K", [(8, 5120), (3, 1024), (8, 17408)])
+def test_rmsnorm_of_a_produced_x(vg, orc, N, K):
+    """GEMV -> RMS norm of its y (dependent x) -> GEMV of the norm's y.  At
+    (N + 1) K 2 bytes within an item slot the producer copies the norm's rows
+    into the item's slot only after the GEMV's group has completed; the
+    widest case reads them from L2 instead.  Intermediates start as canaries."""
+    g = torch.Generator().manual_seed(N * 7 + K)
+    W1 = torch.randn((K, 512), generator=g) * 0.05
+    W2 = torch.randn((640, K), generator=g) * 0.02
+    w1, w2 = vg.nvfp4_pack(W1.cuda()), vg.nvfp4_pack(W2.cuda())
+    x = torch.randn((N, 512), generator=g).to(torch.bfloat16).cuda()
+    gamma = (1 + 0.1 * torch.randn((K,), generator=g)).to(torch.bfloat16).cuda()
+    h = torch.full((N, K), CANARY, dtype=torch.bfloat16, device="cuda")
+    hn = torch.full((N, K), CANARY, dtype=torch.bfloat16, device="cuda")
+    y = torch.full((N, 640), CANARY, dtype=torch.bfloat16, device="cuda")
+    plan = vg.VerifyPlan([(w1, x, h, 0), (vg.RMSNorm(gamma, 1e-6), h, hn, 1, True),
+                          (w2, hn, y, 2, True)], N)
+    for _ in range(2):
+        for t in (h, hn, y):
+            t.fill_(CANARY)
+        plan.run()
+        assert plan.check() == 0
+        q1 = quantise(orc, "nvfp4", W1)
+        h_ref, a1 = gemv_ref(orc, q1, bits(x))
+        bad, worst = orc.check(bits(h), h_ref, a1)
+        assert bad == 0, f"first GEMV: {bad} out of tolerance (worst {worst:.3g})"
+        hn_ref = check_norm(orc, hn, h, gamma, 1e-6, f"norm of a produced x, N={N} K={K}")
+        q2 = quantise(orc, "nvfp4", W2)
+        y_ref, a2 = gemv_ref(orc, q2, hn_ref)
+        bad, worst = orc.check(bits(y), y_ref, a2)
+        assert bad == 0, f"second GEMV: {bad} out of tolerance (worst {worst:.3g})"
+    plan.close()
+
+
 def test_fused_ops_need_the_group_order(vg):
     x = torch.zeros((2, 512), dtype=torch.bfloat16, device="cuda")
     gamma = torch.ones(512, dtype=torch.bfloat16, device="cuda")
