@@ -111,6 +111,8 @@ class VGError(RuntimeError):
 def load():
     """The loaded library (raises if it has not been built)."""
     global _lib
+    if _lib is not None:      # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):

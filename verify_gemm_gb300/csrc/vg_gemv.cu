@@ -1974,6 +1974,7 @@ namespace {
 struct DeviceInfo {
   int sms = 0;
   int cc = 0;
+  int per_sm = 0;          // resident blocks per SM of every kernel instantiation
   bool attr_set = false;
 };
 std::mutex g_mu;
@@ -2009,6 +2010,10 @@ vg_status device_info(int *dev_out, DeviceInfo **info) {
     for (int k = 0; k < 4; ++k)
       VG_CUDA(cudaFuncSetAttribute(kernels()[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSmemBytes));
+    // every instantiation has the same threads and shared memory, and the
+    // launch bounds cap their registers alike
+    VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.per_sm, stream_kernel<true>,
+                                                          kKernelThreads, kSmemBytes));
     d.attr_set = true;
   }
   *dev_out = dev;
@@ -2042,7 +2047,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 #define VG_XT_MIN_N 1
 #endif
 constexpr int kXTensorMinN = VG_XT_MIN_N;
-bool make_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units, int nb = 1) {
+// The x tensor map of single GEMVs, kept per host thread for the last
+// (x, N, K, units, nb): a decode loop calls with the same buffers every
+// step, and encoding a map costs host time on every call otherwise.
+struct XmapCache {
+  const uint16_t *x = nullptr;
+  int N = 0, units = 0, nb = 0;
+  int64_t K = 0;
+  bool ok = false;
+  CUtensorMap map;
+};
+
+bool make_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units, int nb = 1);
+
+bool cached_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units, int nb) {
+  thread_local XmapCache c;
+  if (!(c.x == x && c.N == N && c.K == K && c.units == units && c.nb == nb)) {
+    c.ok = make_xmap(&c.map, x, N, K, units, nb);
+    c.x = x;
+    c.N = N;
+    c.K = K;
+    c.units = units;
+    c.nb = nb;
+  }
+  if (c.ok) std::memcpy(map, &c.map, sizeof(CUtensorMap));
+  return c.ok;
+}
+
+bool make_xmap(CUtensorMap *map, const uint16_t *x, int N, int64_t K, int units, int nb) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
   if (!fn || K % kUnitK != 0 || N < kXTensorMinN) return false;
   const cuuint64_t dims[3] = {cuuint64_t(kUnitK), cuuint64_t(N), cuuint64_t(K / kUnitK)};
@@ -2159,13 +2191,8 @@ vg_status launch(const Params &p, vg_stream_t stream) {
 // Blocks per pass: one per SM (fewer when there are fewer items), capped by
 // what can be resident at once.
 vg_status max_grid(const DeviceInfo &d, int *grid) {
-  int per_sm = 0;
-  // every instantiation has the same threads and shared memory, and the
-  // launch bounds cap their registers alike
-  VG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<true>, kKernelThreads,
-                                                        kSmemBytes));
-  if (per_sm < 1) return VG_ERR_UNSUPPORTED;
-  *grid = std::min(d.sms, per_sm * d.sms);
+  if (d.per_sm < 1) return VG_ERR_UNSUPPORTED;
+  *grid = std::min(d.sms, d.per_sm * d.sms);
   return VG_OK;
 }
 
@@ -2201,7 +2228,7 @@ vg_status gemv_common(const MatDev &m0, int N, void *workspace, size_t workspace
   p.clear_words = i64min(int64_t(di->sms) * 4 * kPartialWords,
                          int64_t((workspace_bytes - kWsHead) / sizeof(uint64_t)));
   p.mat0 = m0;
-  p.x0_tensor = make_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu, nb) ? 1 : 0;
+  p.x0_tensor = cached_xmap(&p.xmap0, m0.x, N, m0.K, m0.iu, nb) ? 1 : 0;
   // items of several chunks, the block-scaled formats and wider passes take
   // x by tensor copy only
   if (!p.x0_tensor && (m0.cpi > 1 || m0.fmt >= VG_FMT_MXFP8 || nb > 1)) return VG_ERR_UNSUPPORTED;
