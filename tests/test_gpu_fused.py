@@ -261,6 +261,43 @@ def test_fused_stack_small(vg, orc, N, mlp_fmt):
     plan.close()
 
 
+def test_fused_stack_width_word(vg):
+    """One fused plan made for 8 columns, run at widths 1, 3, 5 and 8 read
+    from its device word: every entry's first w rows equal, bit for bit,
+    those of a plan made for width w alone over the same inputs (the norms'
+    rows and the gated activation included), and its other rows are not
+    written."""
+    from verify_gemm_gb300.workloads import build_fused_stack
+
+    fs = build_fused_stack(8, layers=2, hidden=512, inter=1408, vocab=1000, seed=33)
+    plan = fs.plan()
+    width = torch.zeros(1, dtype=torch.int32, device="cuda")
+    plan.set_width(width)
+    for w in (1, 3, 5, 8):
+        for e in fs.entries:
+            e.y.fill_(CANARY)
+        width.fill_(w)
+        plan.run()
+        assert plan.check() == 0, w
+        # the same pass made for width w: inputs are the first w rows, and
+        # every x written by the pass is the narrow plan's own output
+        outs = {}
+        narrow = []
+        for e in fs.entries:
+            x = outs[e.x.data_ptr()] if e.after else e.x[:w].contiguous()
+            y = torch.full((w, e.y.shape[1]), CANARY, dtype=torch.bfloat16, device="cuda")
+            outs[e.y.data_ptr()] = y
+            narrow.append((e.op, x, y, e.group, e.after))
+        ref = vg.VerifyPlan(narrow, w)
+        ref.run()
+        assert ref.check() == 0
+        ref.close()
+        for e, (_, _, yn, _, _) in zip(fs.entries, narrow):
+            assert torch.equal(e.y[:w].view(torch.int16), yn.view(torch.int16)), (e.name, w)
+            assert torch.all(e.y[w:] == CANARY), (e.name, w)
+    plan.close()
+
+
 def test_fused_stack_full_size_first_layer_and_head(vg, orc):
     """The 64-layer fused stack at N = 8 as the bench times it: every entry
     of layer 0 (the gated pair and the down projection over all rows, since
