@@ -432,9 +432,10 @@ typedef struct vg_plan_options {
  * plan's descriptor table, counters and partial-sum space once.
  * Descriptors (pointers included) are copied; buffer contents may change
  * between passes.  Each item's slice of x is copied into shared memory by
- * copies that run ahead of the group order, so an x must not alias any
- * matrix's y within the same plan (group order sequences the work; it does
- * not forward one group's y as the next group's x). */
+ * copies that run ahead of the group order, so an x may alias a y of the
+ * same plan only when its descriptor sets x_after_group (its copies then
+ * wait until the previous group has completed, and that group's y is the
+ * x); any other x must not alias any y of the plan. */
 vg_status vg_verify_plan_create(const vg_matrix_desc *mats, int count, int N,
                                 int ordered, vg_verify_plan **plan_out);
 vg_status vg_verify_plan_create_ex(const vg_matrix_desc *mats, int count, int N,
