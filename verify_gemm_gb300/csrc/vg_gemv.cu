@@ -835,8 +835,10 @@ __device__ __forceinline__ bool collect_wide(const Params &p, int b0, int bl, ui
 
 // Epilogue of a gated pair: rows g (gate) and g + 8 (up) of tile mt are
 // gate and up row 8 mt + g; y = SiLU(gate) * up from the FP32 sums, rounded
-// once to BF16.  Out of line, like the other rarely taken paths.
-__device__ __noinline__ void swiglu_epilogue(const MatDev &m, int mt, int g, int t, int N,
+// once to BF16.  Only the fused instantiation compiles it, and there it is
+// inlined: out of line, the call cost the gated pair's piece ends more than
+// the code costs the fused kernel's registers.
+__device__ __forceinline__ void swiglu_epilogue(const MatDev &m, int mt, int g, int t, int N,
                                              const float (&accs)[4]) {
   const int gi = mt * 8 + g;
   if (gi >= m.Mo) return;
