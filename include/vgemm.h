@@ -387,7 +387,8 @@ enum {
  *   card, Checks section: row reductions are checked next to the GEMVs):
  *     y[n][k] = bf16( x[n][k] * gamma[k] / sqrt(sum_k x[n][k]^2 / K + eps) ),
  *   sums and scaling in FP32; x and y [N][K], gamma BF16 [K]; format, M, w,
- *   scales and rowscale are ignored.  It runs as one item of the pass.
+ *   scales and rowscale are ignored.  Every thread block of the pass sums
+ *   whole rows and writes one slice of y (N must be at most 8).
  * x_after_group = 1 says that x is written earlier in the same pass (by the
  *   previous group, e.g. the down projection's x = the gated pair's y, or
  *   q/k/v's x = an RMS norm's y): its copy into the kernel is then issued
