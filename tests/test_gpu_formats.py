@@ -178,6 +178,8 @@ def test_int4g_decode_is_bit_exact(vg, orc, M, K):
 # --------------------------------------------------------------------- GEMV
 
 SHAPES = [
+    (1, 512, (1, 8)),            # a single row: 15 padding rows in its tile
+    (16, 512, (4,)),             # exactly one tile
     (256, 512, (1,)),            # INT4: one chunk; MXFP8: two chunks
     (17, 1024, (1, 3, 8)),       # ragged rows
     (520, 2048, (8,)),           # several row blocks, split between blocks
