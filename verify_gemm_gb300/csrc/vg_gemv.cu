@@ -628,11 +628,10 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
         sc ? sc + (int64_t(q.rb) * rb_scale_chunks + q.c * tiles * cpi) * scb : nullptr;
     const uint32_t slot = ring + s * kItemSlotBytes, full = full0 + 8 * s;
 
-    // ---- x written by the previous phase of this pass: wait until that
-    // phase has completed (bounded), bringing this producer's next items
-    // into L2 meanwhile; then order the acquire before the x copies
-    // an x that the previous phase writes: its copy waits for that phase
-    // (below, after the item's weight copies have been issued)
+    // ---- an x that the previous phase of this pass writes: its copy waits
+    // (bounded) until that phase has completed, after the item's weight
+    // copies have been issued (below); the wait brings this producer's next
+    // items into L2 and orders the acquire before the x copies
     const bool need_dep = kFused && xdep && dep_ok != q.ph;
 
     // ---- wait for the slot
@@ -668,7 +667,8 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
       }
     }
 
-    // ---- issue (an RMS-norm item carries no data: its slot completes at once)
+    // ---- issue (an RMS-norm item has no weights: its slot takes the rows
+    // of x, or nothing)
     if (is_norm) {
       // the rows of x, when they fit the slot (else the consumers read them
       // from global memory), copied once the phase that writes them is done
