@@ -1,6 +1,9 @@
-// vg_gemv.cu -- the weight-streaming GEMV for N = 1..8 BF16 columns over
-// NVFP4 or row-scaled FP8 weights, as a single product and as a fused,
-// ordered verify pass over a layer stack.
+// vg_gemv.cu -- the weight-streaming GEMV over NVFP4, row-scaled FP8,
+// MXFP8 or groupwise-INT4 weights, for N = 1..8 BF16 columns
+// (stream_kernel) or 9..32 (stream_kernel_wide), as a single product and as
+// a fused, ordered verify pass over a layer stack.  The fused instantiation
+// also runs RMS norms, the SiLU-gated epilogue of a gate/up pair and x
+// written earlier in the same pass.
 //
 // What it computes: y[N,M] = x[N,K] . dequant(W)[M,K]^T with FP32
 // accumulation (mtp7-device-confidence engine card, Design table, "GEMVs"
@@ -19,7 +22,8 @@
 //    the packed buffers; L2 evict-first) and one TMA tensor copy of its x
 //    slice (128-byte swizzle; L2 evict-last).  The weights never pass through
 //    registers of the producer.
-//  * A work item is 16 tile-chunks (a chunk is 512 columns NVFP4, 256 FP8):
+//  * A work item is 16 tile-chunks (a chunk is 512 columns NVFP4 and INT4,
+//    256 FP8 and MXFP8):
 //    one chunk of a row block of 16 tiles, or, for matrices with few rows,
 //    16 / rt consecutive chunks of a row block of rt tiles.  Consumer warp w
 //    owns tile-chunk w.  It decodes the codes in registers to BF16 A
