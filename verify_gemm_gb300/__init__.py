@@ -1,8 +1,11 @@
 """GB300 (sm_103a) NVFP4 / row-scaled FP8 verify GEMV.
 
-y[N, M] = x[N, K] . dequant(W)[M, K]^T for N = 1..8 BF16 columns, the
-weight-streaming product of decode and speculative verification (the
-"GEMVs" row of the mtp7-device-confidence engine card's Design table).
+y[N, M] = x[N, K] . dequant(W)[M, K]^T for N = 1..8 BF16 columns (up to 32
+for several requests' drafts in one pass), the weight-streaming product of
+decode and speculative verification (the "GEMVs" row of the
+mtp7-device-confidence engine card's Design table); MXFP8 and groupwise
+INT4 weights as well, and a fused verify pass over a layer stack with RMS
+norms and the gated activation.
 
 Every step runs in the CUDA kernels of ``libvgemm.so`` (C ABI declared in
 ``include/vgemm.h``); this module only marshals torch tensors (device

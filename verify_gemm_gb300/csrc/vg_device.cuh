@@ -1,7 +1,7 @@
 // vg_device.cuh -- device-side building blocks shared by the pack and GEMV
 // kernels: packed-layout constants, inline PTX for mbarriers, bulk copies,
 // BF16 tensor-core MMA and BF16x2 multiplies, and the in-register decode of
-// the packed NVFP4 / FP8 codes.
+// the packed NVFP4, FP8, MXFP8 and INT4 codes.
 #pragma once
 
 #include <cstdint>

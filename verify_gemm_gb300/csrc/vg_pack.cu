@@ -1,5 +1,6 @@
-// vg_pack.cu -- load-time kernels: NVFP4 and row-scaled FP8 round-to-nearest
-// quantisation into the packed layout, unpack to the canonical layout, and
+// vg_pack.cu -- load-time kernels: NVFP4, row-scaled FP8, MXFP8 and
+// groupwise-INT4 round-to-nearest quantisation into the packed layout (and
+// gate/up pairs packed as one matrix), unpack to the canonical layout, and
 // canonical -> packed conversion.
 //
 // The re-encoding of stored weights at load is what the crit landing page's
