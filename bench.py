@@ -80,6 +80,9 @@ def parse():
                     help="stack: the verify pass (headline); fused: the verify pass with RMS "
                          "norms, the gated activation and dependent x; others: one product of "
                          "that configuration, timed alone with an L2 flush between launches")
+    ap.add_argument("--fmt", choices=["nvfp4", "fp8", "mxfp8", "int4g"], default=None,
+                    help="single products: pack the configuration's weights in this format "
+                         "instead of its own")
     return ap.parse_args()
 
 
@@ -681,16 +684,18 @@ def run_single(args, local):
     vbuild.build()
     torch.cuda.set_device(local)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-    nbytes, ms = time_single(args.workload, args.N, args.steps, args.warmup, flush)
+    nbytes, ms = time_single(args.workload, args.N, args.steps, args.warmup, flush, fmt=args.fmt)
     med = statistics.median(ms)
     peak, kind = peaks()
     title, _ = SINGLE[args.workload]
+    if args.fmt:
+        title = f"{title}, weights packed as {args.fmt}"
     line = {"metric": METRIC, "value": round(nbytes / (med / 1e3) / 1e9, 1), "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(med, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "weights": WEIGHTS,
             "data": "synthetic",
-            "config": {"workload": title, "N": args.N, "bytes": nbytes,
+            "config": {"workload": title, "N": args.N, "bytes": nbytes, "fmt": args.fmt,
                        "l2": "flushed by a 512 MB write before every launch",
                        "us_p10_p90": [round(1e3 * q, 2) for q in pcts(ms, (10, 90))]},
             "roofline": {"bound": "hbm", "achieved": round(nbytes / (med / 1e3) / 1e9, 1),
@@ -818,6 +823,10 @@ def main():
         if rank == 0:
             print(json.dumps({"impl": "reference", "unavailable": "the oracle's fused chain is "
                               "checked in the tests, not timed"}), flush=True)
+    elif args.impl == "reference" and args.workload != "stack" and args.fmt:
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle's timing runs each "
+                              "configuration in its own format"}), flush=True)
     elif args.impl == "reference" and args.workload != "stack":
         if rank == 0:
             run_reference_config(args)
