@@ -93,3 +93,18 @@ def test_bench_reference_arm_under_torchrun_two_ranks():
     assert line["ms_per_step"] * line["steps"] < 600_000
     assert line["extrapolated_full_pass_ms"] > line["ms_per_step"]
     assert line["cpu_baseline"]["single_thread"]["cores"] == 1
+
+
+@pytest.mark.parametrize("extra", [["--workload", "fused"], ["--workload", "head", "--fmt", "int4g"]])
+def test_bench_reference_arm_without_an_oracle_timing(extra):
+    """Workloads the oracle does not time (the fused stack, a configuration
+    repacked in another format) make the reference arm print one line that
+    says so and exit 0."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+           "--steps", "1", "--warmup", "0", *extra]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unavailable"]
