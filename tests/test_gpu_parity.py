@@ -591,3 +591,14 @@ def test_quickstart_example_runs(vg):
     exec(compile(open(path).read(), path, "exec"), scope)
     y = scope["y"]
     assert y.shape == (8, 5120) and y.dtype == torch.bfloat16 and torch.isfinite(y.float()).all()
+
+
+def test_fused_layer_example_runs(vg):
+    """examples/fused_layer.py, the fused-pass usage example, runs as written
+    (it checks its gated activation against PyTorch arithmetic itself)."""
+    path = os.path.join(os.path.dirname(os.path.dirname(__file__)), "examples", "fused_layer.py")
+    scope = {"__file__": path, "__name__": "fused_layer"}
+    exec(compile(open(path).read(), path, "exec"), scope)
+    h, y = scope["h"], scope["y"]
+    assert h.shape == (8, 2816) and y.shape == (8, 1024)
+    assert torch.isfinite(h.float()).all() and torch.isfinite(y.float()).all()
