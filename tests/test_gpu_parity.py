@@ -602,3 +602,14 @@ def test_fused_layer_example_runs(vg):
     h, y = scope["h"], scope["y"]
     assert h.shape == (8, 2816) and y.shape == (8, 1024)
     assert torch.isfinite(h.float()).all() and torch.isfinite(y.float()).all()
+
+
+def test_graph_width_example_runs(vg):
+    """examples/graph_width.py, the captured-graph usage example, runs as
+    written (it compares each width's columns with the full-width replay)."""
+    path = os.path.join(os.path.dirname(os.path.dirname(__file__)), "examples", "graph_width.py")
+    scope = {"__file__": path, "__name__": "graph_width"}
+    exec(compile(open(path).read(), path, "exec"), scope)
+    y_full = scope["y_full"]
+    assert y_full.shape == (8, 2048) and torch.isfinite(y_full.float()).all()
+    assert torch.count_nonzero(y_full) > 0
