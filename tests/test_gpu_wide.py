@@ -8,6 +8,9 @@ lanes, each verifying its MTP drafts; concurrent MTP3 decode at C = 1..8).
   MMAs over the same K split);
 * the limits: 16 columns for every layout, 32 for matrices in row blocks of
   16 tiles; wider requests are refused on the host;
+* the wide kernel's decode, bit exact: with x one-hot, 16 or 32 columns per
+  call, every code of each format against every scale it supports comes out
+  as the oracle's dequantised weight, in row blocks of 16, 8 and 4 tiles;
 * the full 64-layer stack at N = 16 in the benchmark's launch configuration
   (sampled rows), and the head at N = 32.
 """
@@ -168,3 +171,102 @@ def test_full_stack_n16_and_head_n32(vg, orc):
     yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
     bad, worst = orc.check(bits(y[:, rows]), yref, a)
     assert bad == 0, f"head N=32: {bad} out of tolerance (worst {worst:.3g})"
+
+
+# ------------------------------------------- wide decode, bit exact (one-hot)
+
+def one_hot_columns_wide(vg, wt, K, N):
+    """Decoded weights recovered N > 8 columns per call (the wide kernel: one
+    decode feeds N / 8 MMAs): x row n is the unit vector e_(k0 + n).  Returns
+    W^ as [M, K] FP64."""
+    M = wt.M
+    out = np.zeros((M, K), np.float64)
+    x = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    ws = vg.workspace_for(wt, N=N)
+    y = torch.empty((N, M), dtype=torch.bfloat16, device="cuda")
+    ar = torch.arange(N, device="cuda")
+    for k0 in range(0, K, N):
+        x.zero_()
+        x[ar, k0 + ar] = 1.0
+        vg.gemv(wt, x, y=y, workspace=ws)
+        out[:, k0:k0 + N] = y.float().cpu().numpy().astype(np.float64).T
+    assert vg.workspace_error(ws) == 0
+    return out
+
+
+def _codes4(M, K):
+    m = np.arange(M)[:, None]
+    k = np.arange(K)[None, :]
+    codes = ((k % 16) + m + k // 16) % 16
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _codes8(M, K):
+    m = np.arange(M)[:, None]
+    k = np.arange(K)[None, :]
+    q = ((k + 37 * m) % 256).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0                               # no NaN codes
+    return q
+
+
+def _one_hot_case(vg, orc, fmt, M, K):
+    """(packed weight, exact decoded weights) with every code of the format
+    against every scale it supports, in every register slot and both rows a
+    lane holds."""
+    m = np.arange(M)[:, None]
+    if fmt == "nvfp4":
+        nib = _codes4(M, K)
+        sc = ((np.arange(K // 16)[None, :] + 5 * m) % 127).astype(np.uint8)
+        assert set(np.unique(sc)) == set(range(127))      # 0x00..0x7E, subnormals too
+        gs = 2.0 ** -4
+        wt = vg.nvfp4_from_canonical(torch.from_numpy(nib).cuda(), torch.from_numpy(sc).cuda(),
+                                     gs)
+        return wt, orc.nvfp4_dequant(nib, sc, gs, M, K)
+    if fmt == "fp8":
+        q = _codes8(M, K)
+        assert len(np.unique(q)) == 254
+        rs = (2.0 ** -(3 + (np.arange(M) % 5))).astype(np.float32)
+        wt = vg.fp8_from_canonical(torch.from_numpy(q).cuda(), torch.from_numpy(rs).cuda())
+        return wt, orc.fp8_dequant(q, rs, M, K)
+    if fmt == "mxfp8":
+        q = _codes8(M, K)
+        sc = (10 + (np.arange(K // 32)[None, :] + 7 * m) % 125).astype(np.uint8)
+        assert set(np.unique(sc)) == set(range(10, 135))
+        wt = vg.mxfp8_from_canonical(torch.from_numpy(q).cuda(), torch.from_numpy(sc).cuda())
+        return wt, orc.mxfp8_dequant(q, sc, M, K)
+    rng = np.random.default_rng(M + K)
+    nib = _codes4(M, K)
+    exps = rng.integers(-20, 21, (M, K // 128))
+    mant = rng.integers(0, 128, (M, K // 128))
+    sc = (((exps + 127) << 7) | mant).astype(np.uint16)
+    sc[0, 0] = 0                                           # a zero scale
+    sc[1, 0] |= 0x8000                                     # a negative scale
+    wt = vg.int4g_from_canonical(torch.from_numpy(nib).cuda(),
+                                 torch.from_numpy(sc.view(np.int16)).cuda())
+    exact = orc.int4g_dequant(nib, sc, M, K)
+    # y is the single BF16 rounding of (q - 8) * s
+    vals, inv = np.unique(exact, return_inverse=True)
+    rounded = np.array([orc.bf16_value(orc.bf16_round(v)) for v in vals])
+    return wt, rounded[inv].reshape(M, K)
+
+
+# (fmt, M, K, N): row blocks of 16 tiles (one chunk per item) at 32 and 16
+# columns; of 8 tiles (two chunks per item) and of 4 tiles (four chunks per
+# item, 8-bit formats), where a warp's x columns start one or more chunks
+# into the item's slice
+WIDE_ONE_HOT = [("nvfp4", 256, 512, 32), ("nvfp4", 256, 512, 16), ("nvfp4", 256, 1024, 16),
+                ("int4g", 256, 512, 32), ("int4g", 256, 1024, 16),
+                ("fp8", 256, 256, 32), ("fp8", 256, 512, 32), ("fp8", 256, 1024, 16),
+                ("mxfp8", 256, 512, 32), ("mxfp8", 256, 1024, 16)]
+
+
+@pytest.mark.parametrize("fmt,M,K,N", WIDE_ONE_HOT)
+def test_wide_decode_is_bit_exact(vg, orc, fmt, M, K, N):
+    wt, want = _one_hot_case(vg, orc, fmt, M, K)
+    if fmt != "int4g":
+        # each decoded weight is a BF16 value: products and sums are exact
+        assert np.array_equal(torch.from_numpy(want).to(torch.bfloat16).double().numpy(), want)
+    got = one_hot_columns_wide(vg, wt, K, N)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (f"{fmt} {M}x{K} N={N}: {len(bad)} decoded weights differ, first at "
+                           f"{bad[0].tolist()}: {got[tuple(bad[0])]} != {want[tuple(bad[0])]}")
