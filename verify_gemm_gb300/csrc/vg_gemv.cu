@@ -726,7 +726,7 @@ __device__ void producer(const Params &p, const MatDev *mats, const PhaseDev *ph
 // no fence is needed on either side.  One round of loads covers kCollectW
 // contributors; while some are not yet published, only their words are read
 // again.  Each round costs an L2 round trip (about 1 us on GB300), but wider
-// rounds need more than the 96 registers a thread gets with 17 warps per SM
+// rounds need more than the 96 registers a thread gets with 18 warps per SM
 // and spill, which costs more than the rounds they save.
 // Returns false if the wait ran out or another block has already failed.
 constexpr int kCollectW = 2;
