@@ -613,3 +613,23 @@ def test_graph_width_example_runs(vg):
     y_full = scope["y_full"]
     assert y_full.shape == (8, 2048) and torch.isfinite(y_full.float()).all()
     assert torch.count_nonzero(y_full) > 0
+
+
+def test_c_example_builds_and_runs(vg, tmp_path):
+    """examples/c_gemv.c drives the C ABI from C with no Python: nvcc
+    compiles and links it against libvgemm.so, and the program packs,
+    runs the GEMV, reads the device error word and checks its own y."""
+    import subprocess
+
+    from verify_gemm_gb300 import build as B
+
+    root = os.path.dirname(os.path.dirname(__file__))
+    exe = str(tmp_path / "c_gemv")
+    cmd = [B.nvcc(), "-x", "c", "-O2", os.path.join(root, "examples", "c_gemv.c"),
+           f"-I{os.path.join(root, 'include')}", f"-L{B.OUT_DIR}", "-lvgemm", "-lm",
+           "-Xlinker", "-rpath", "-Xlinker", B.OUT_DIR, "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "worst error / tolerance" in r.stdout
