@@ -139,10 +139,17 @@ def test_gated_activation(vg, orc, fmt, I, K, Ns):
         assert worst <= 1.0, f"{fmt} {I}x{K} N={N}: worst error / bound {worst:.3g}"
 
 
-@pytest.mark.parametrize("N,K", [(1, 5120), (8, 5120), (3, 512), (8, 17408)])
-def test_rmsnorm_entry(vg, orc, N, K):
+# (N, K): K = 1040 and 48 are not multiples of 64 (rows of 130 and 6 vectors
+# of 8), K = 16 is the smallest K (two slices of one vector each); the last
+# case has an all-zero row (its y is zero: 0 * 1 / sqrt(eps))
+@pytest.mark.parametrize("N,K,zero_row", [(1, 5120, False), (8, 5120, False), (3, 512, False),
+                                          (8, 17408, False), (5, 1040, False), (2, 16, False),
+                                          (8, 48, False), (4, 1024, True)])
+def test_rmsnorm_entry(vg, orc, N, K, zero_row):
     g = torch.Generator().manual_seed(N * K)
     x = (torch.randn((N, K), generator=g) * 2).to(torch.bfloat16).cuda()
+    if zero_row:
+        x[1].zero_()
     gamma = (1 + 0.1 * torch.randn((K,), generator=g)).to(torch.bfloat16).cuda()
     y = torch.full((N, K), CANARY, dtype=torch.bfloat16, device="cuda")
     plan = vg.VerifyPlan([(vg.RMSNorm(gamma, 1e-6), x, y, 0)], N)
