@@ -139,6 +139,37 @@ def test_gated_activation(vg, orc, fmt, I, K, Ns):
         assert worst <= 1.0, f"{fmt} {I}x{K} N={N}: worst error / bound {worst:.3g}"
 
 
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8"])
+def test_gated_activation_saturates(vg, orc, fmt):
+    """Gates far past SiLU's bends: gate rows of constant weight +-0.5 (exact
+    in both formats) against x rows of constant sign give g near +-512 and
+    +-128, where SiLU(g) is g or underflows to zero (exp(-g) overflows FP32
+    below -88.7).  Every h is finite and within the bound."""
+    I, K, N = 64, 1024, 4
+    g = torch.Generator().manual_seed(91)
+    Wg = torch.randn((I, K), generator=g) * 0.02
+    Wg[:32] = 0.5 * torch.sign(torch.randn((32, 1), generator=g))
+    Wu = torch.randn((I, K), generator=g) * 0.02
+    xf = torch.empty((N, K))
+    xf[0], xf[1], xf[3] = 1.0, -1.0, 0.25
+    xf[2] = torch.randn(K, generator=g) * 3
+    x = xf.to(torch.bfloat16).cuda()
+    pair = (vg.nvfp4_pack_gated if fmt == "nvfp4" else vg.fp8_pack_gated)(Wg.cuda(), Wu.cuda())
+    h = torch.full((N, I), CANARY, dtype=torch.bfloat16, device="cuda")
+    plan = vg.VerifyPlan([(pair, x, h, 0)], N)
+    plan.run()
+    assert plan.check() == 0
+    plan.close()
+    gr, ag = gemv_ref(orc, quantise(orc, fmt, Wg), bits(x))
+    ur, au = gemv_ref(orc, quantise(orc, fmt, Wu), bits(x))
+    assert np.abs(gr[:2, :32]).min() > 400          # the gates this test is about
+    href, bound = orc.swiglu(gr, ur, ag, au)
+    hf = h.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(hf).all()
+    worst = float((np.abs(hf - href) / bound).max())
+    assert worst <= 1.0, f"{fmt}: worst error / bound {worst:.3g}"
+
+
 # (N, K): K = 1040 and 48 are not multiples of 64 (rows of 130 and 6 vectors
 # of 8), K = 16 is the smallest K (two slices of one vector each); the last
 # case has an all-zero row (its y is zero: 0 * 1 / sqrt(eps))
