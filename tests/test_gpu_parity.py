@@ -402,6 +402,34 @@ def test_verify_pass_small_stack(vg, orc, N, ordered):
     plan.close()
 
 
+@pytest.mark.parametrize("ctas", [1, 2, 7])
+def test_verify_pass_on_few_blocks(vg, orc, ctas):
+    """The ordered pass on 1, 2 and 7 thread blocks: one block holds every row
+    block whole (no partial sums at all), a few blocks split long ranges of
+    items between them; every product within the tolerance of the oracle."""
+    from verify_gemm_gb300.inputs import draw_stack_matrix
+
+    N = 5
+    st = _small_stack(vg, N, True)
+    plan = st.plan(ordered=True, max_ctas=ctas)
+    assert plan.grid == ctas
+    for _ in range(2):
+        st.y_all.zero_()
+        plan.run()
+        assert plan.check() == 0
+    for m, wt, x, y in zip(st.mats, st.weights, st.xs, st.ys):
+        W, _ = draw_stack_matrix(m, N, 9, "cuda")
+        Wh = W.cpu().numpy()
+        if m.fmt == "nvfp4":
+            nib, sc, gs = orc.nvfp4_quantise(Wh)
+            yref, a = orc.gemv_nvfp4(nib, sc, gs, bits(x), threads=THREADS)
+        else:
+            q, rs = orc.fp8_quantise(Wh)
+            yref, a = orc.gemv_fp8(q, rs, bits(x), threads=THREADS)
+        assert_close(orc, y, yref, a, f"{m.name} on {ctas} blocks")
+    plan.close()
+
+
 @pytest.mark.parametrize("ordered", [True, False])
 @pytest.mark.parametrize("N", [3, 8])
 def test_verify_pass_multi_chunk_items(vg, orc, N, ordered):
